@@ -1,0 +1,395 @@
+"""Checks that pin the CPU oracle to things other than itself.
+
+Every ``check_*`` function takes an ``oracle.Oracle`` and raises
+``AssertionError`` when the oracle disagrees with the fact it pins.  The pins are
+library casts (torch, ml_dtypes), the format definitions' closed forms,
+hand-worked examples (``tests/golden``), brute force over all codes, and
+invariants the pages fix ("Composer 2 Technical Report", section 6.1: a
+token's NVFP4 codes and scales do not depend on the rest of the batch and do not
+see later tokens).  ``test_oracle_pins.py`` runs them against the oracle, and
+``test_oracle_mutants.py`` runs them against deliberately broken copies of it to
+show that each plausible mistake fails at least one of them.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from fp8_moe_expert_gb300 import synth
+from tests.golden import read_cases
+
+E2M1_GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _all_bf16_finite() -> np.ndarray:
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = synth.bf16_float(bits)
+    return bits[np.isfinite(vals)]
+
+
+def _nearest_even(v: float, mags: list[float]) -> int:
+    """Brute force: index of the nearest magnitude, ties to the even index."""
+    a = abs(v)
+    if a >= mags[-1]:
+        return len(mags) - 1
+    best = min(range(len(mags)), key=lambda i: (abs(mags[i] - a), i % 2))
+    return best
+
+
+# ---------------------------------------------------------------- tables ----
+def check_e2m1_decode(orc):
+    """All 16 E2M1 codes: the grid {0, .5, 1, 1.5, 2, 3, 4, 6} with a sign bit."""
+    got = orc.e2m1_value(np.arange(16))
+    want = np.array(E2M1_GRID + [-g for g in E2M1_GRID])
+    assert np.array_equal(got, want) and np.signbit(got[8]), (got, want)
+
+
+def check_e4m3_decode(orc):
+    """All 256 E4M3 codes against torch.float8_e4m3fn."""
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = orc.e4m3_value(codes)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), codes[~same]
+    assert np.array_equal(np.signbit(got[~np.isnan(got)]), np.signbit(want[~np.isnan(want)]))
+
+
+def check_e8m0_decode(orc):
+    """All 256 E8M0 codes against torch.float8_e8m0fnu."""
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = orc.e8m0_value(codes)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), codes[~same]
+
+
+def check_e4m3_encode_all_bf16(orc):
+    """Every finite bf16 value below 464 in magnitude: oracle E4M3 encode equals
+    torch's float -> float8_e4m3fn cast (round to nearest even).  At and above 464
+    torch overflows to NaN while the oracle saturates to 448 (0x7e / 0xfe)."""
+    import torch
+
+    bits = _all_bf16_finite()
+    vals = synth.bf16_float(bits).astype(np.float64)
+    got = orc.e4m3_encode(vals)
+    inr = np.abs(vals) < 464.0
+    want = torch.from_numpy(vals[inr].astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad = got[inr] != want
+    assert not bad.any(), vals[inr][bad][:8]
+    sat = got[~inr]
+    assert np.all((sat == 0x7E) | (sat == 0xFE)), np.unique(sat)
+    assert np.array_equal(sat >> 7, np.signbit(vals[~inr]).astype(np.uint8))
+
+
+def check_e2m1_encode_all_bf16(orc):
+    """Every finite bf16 value: oracle E2M1 encode equals ml_dtypes' float4_e2m1fn
+    cast (nearest even, saturating at 6)."""
+    import ml_dtypes
+
+    bits = _all_bf16_finite()
+    vals = synth.bf16_float(bits)
+    got = orc.e2m1_encode(vals.astype(np.float64))
+    want = vals.astype(ml_dtypes.float4_e2m1fn).view(np.uint8) & 0xF
+    bad = got != want
+    assert not bad.any(), vals[bad][:8]
+
+
+def check_ties_brute_force(orc):
+    """Every midpoint between neighbouring magnitudes goes to the even code, and a
+    hair either side goes to the nearer one (brute-force nearest search)."""
+    e2 = [float(v) for v in E2M1_GRID]
+    e4 = [float(v) for v in orc.e4m3_value(np.arange(127))]
+    for mags, enc, sign in ((e2, orc.e2m1_encode, 8), (e4, orc.e4m3_encode, 0x80)):
+        mids = [(mags[i] + mags[i + 1]) / 2 for i in range(len(mags) - 1)]
+        probes = []
+        for m, lo, hi in zip(mids, mags[:-1], mags[1:]):
+            eps = (hi - lo) * 1e-6
+            probes += [m, m - eps, m + eps, -m, -(m - eps), -(m + eps)]
+        probes = np.array(probes)
+        got = enc(probes)
+        want = np.array([_nearest_even(p, mags) | (sign if np.signbit(p) else 0) for p in probes], np.uint8)
+        assert np.array_equal(got, want), probes[got != want][:8]
+
+
+def check_saturation_and_sign(orc):
+    for enc, top, sign in ((orc.e2m1_encode, 7, 8), (orc.e4m3_encode, 0x7E, 0x80)):
+        got = enc(np.array([1e30, -1e30, 1e6, -1e6, 0.0, -0.0, 1e-30, -1e-30]))
+        want = np.array([top, top | sign, top, top | sign, 0, sign, 0, sign], np.uint8)
+        assert np.array_equal(got, want), (got, want)
+
+
+# --------------------------------------------------------- worked examples ---
+def _parse_floats(s):
+    return np.array([float(v) for v in s.split()], np.float64)
+
+
+def check_nvfp4_worked(orc):
+    for name, case in read_cases("nvfp4_worked.txt").items():
+        x = synth.bf16_bits(_parse_floats(case["x"]).astype(np.float32)).reshape(1, 16)
+        codes, sf, scale = orc.quant_nvfp4(x)
+        s_bits = int(np.array(scale, np.float32).view(np.uint32)[0])
+        assert s_bits == int(case["S_bits"], 16), (name, hex(s_bits))
+        assert int(sf[0, 0]) == int(case["sf"], 16), (name, hex(int(sf[0, 0])))
+        want_codes = [int(c, 16) for c in case["codes"].split()]
+        got_codes = [(int(codes[0, j // 2]) >> (4 * (j % 2))) & 0xF for j in range(16)]
+        assert got_codes == want_codes, (name, got_codes, want_codes)
+        want_packed = [int(c, 16) for c in case["packed"].split()]
+        assert [int(c) for c in codes[0]] == want_packed, (name, codes[0])
+
+
+def check_mxfp8_worked(orc):
+    for name, case in read_cases("mxfp8_worked.txt").items():
+        lead = _parse_floats(case["x"]).astype(np.float32)
+        x = np.zeros(32, np.float32)
+        x[: len(lead)] = lead
+        xb = synth.bf16_bits(x).reshape(1, 32)
+        assert np.array_equal(synth.bf16_float(xb).reshape(-1)[: len(lead)], lead), name
+        codes, sf = orc.quant_mxfp8_rows(xb)
+        assert int(sf[0, 0]) == int(case["scale"]), (name, int(sf[0, 0]))
+        want = [int(c, 16) for c in case["codes"].split()]
+        assert [int(c) for c in codes[0, : len(want)]] == want, (name, codes[0, : len(want)])
+        tail = codes[0, len(want):]
+        assert np.all(tail == 0), (name, tail)
+
+
+# ---------------------------------------------------- NVFP4 invariants -------
+def _rows_with_outliers(rows=64, k=256, seed=11):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, k), dtype=np.float32)
+    x[rng.random((rows, k)) < 0.02] *= 40.0
+    x[:: 7] *= np.float32(1e-3)
+    x[3, 16:32] = 0.0                  # an all-zero block in a non-zero row
+    x[5] = 0.0                         # an all-zero row
+    x[9, :16] *= np.float32(1e-6)      # a block far below the row amax
+    return synth.bf16_bits(x)
+
+
+def check_nvfp4_batch_invariance(orc):
+    """Per-token scales: a row quantized alone, in a shuffled batch, or ahead of
+    appended later rows gets identical codes and scales."""
+    x = _rows_with_outliers()
+    full = orc.quant_nvfp4(x)
+    perm = np.random.default_rng(5).permutation(x.shape[0])
+    shuf = orc.quant_nvfp4(x[perm])
+    for a, b in zip(full, shuf):
+        assert np.array_equal(a[perm], b)
+    for t in (0, 3, 9, 40):
+        one = orc.quant_nvfp4(x[t:t + 1])
+        for a, b in zip(full, one):
+            assert np.array_equal(a[t:t + 1], b), t
+    later = synth.bf16_bits(np.random.default_rng(6).standard_normal((32, x.shape[1]), dtype=np.float32) * 1e4)
+    ext = orc.quant_nvfp4(np.concatenate([x, later]))
+    for a, b in zip(full, ext):
+        assert np.array_equal(a, b[: x.shape[0]])
+
+
+def check_nvfp4_sign_symmetry(orc):
+    """q(-x) = -q(x): negating a row flips exactly the sign bit of every code in
+    blocks with a non-zero scale, and changes nothing else."""
+    x = _rows_with_outliers()
+    neg = x ^ np.uint16(0x8000)
+    c1, s1, t1 = orc.quant_nvfp4(x)
+    c2, s2, t2 = orc.quant_nvfp4(neg)
+    assert np.array_equal(s1, s2) and np.array_equal(t1, t2)
+    lo1, hi1 = c1 & 0xF, c1 >> 4
+    lo2, hi2 = c2 & 0xF, c2 >> 4
+    nib1 = np.stack([lo1, hi1], -1).reshape(x.shape)
+    nib2 = np.stack([lo2, hi2], -1).reshape(x.shape)
+    live = np.repeat(s1 != 0, 16, axis=1)
+    assert np.array_equal(nib1[live] ^ 8, nib2[live])
+    assert np.all(nib1[~live] == 0) and np.all(nib2[~live] == 0)
+
+
+def check_nvfp4_power_of_two_scaling(orc):
+    """Scaling a row by 2^j (no under/overflow) scales S_t by 2^j and leaves every
+    code and block scale unchanged: each step is an IEEE operation on scaled
+    operands."""
+    x = _rows_with_outliers()
+    f = synth.bf16_float(x)
+    for j in (-3, 5):
+        xs = synth.bf16_bits(f * np.float32(2.0 ** j))
+        c1, s1, t1 = orc.quant_nvfp4(x)
+        c2, s2, t2 = orc.quant_nvfp4(xs)
+        rows = np.abs(f).max(axis=1) > 1e-2   # keep S_t and d clear of fp32 subnormals
+        assert np.array_equal(c1[rows], c2[rows]) and np.array_equal(s1[rows], s2[rows])
+        assert np.array_equal(t1[rows] * np.float32(2.0 ** j), t2[rows])
+
+
+def check_nvfp4_amax_maps_to_six(orc):
+    """The row maximum lands in a block whose scale is 448 (0x7e), and every
+    block with a normal E4M3 scale maps its own maximum to |code| = 6."""
+    x = _rows_with_outliers()
+    f = np.abs(synth.bf16_float(x))
+    codes, sf, scale = orc.quant_nvfp4(x)
+    nib = np.stack([codes & 0xF, codes >> 4], -1).reshape(x.shape)
+    for t in range(x.shape[0]):
+        if f[t].max() == 0:
+            assert scale[t] == 0 and np.all(sf[t] == 0)
+            continue
+        j = int(np.argmax(f[t]))
+        assert sf[t, j // 16] == 0x7E, (t, hex(int(sf[t, j // 16])))
+        for b in range(x.shape[1] // 16):
+            if sf[t, b] < 0x08:            # subnormal E4M3 scale: coarser steps
+                continue
+            blk = f[t, 16 * b: 16 * b + 16]
+            jb = int(np.argmax(blk))
+            assert (nib[t, 16 * b + jb] & 7) == 7, (t, b)
+
+
+def check_nvfp4_error_bound(orc):
+    """|x - x_hat| is at most half a grid step of the E2M1 value, times the block's
+    scale e, plus a relative 2^-22 for the fp32 rounding of x/e; saturated
+    elements dequantize to exactly +-6e and, in blocks with a normal E4M3 scale,
+    lie within 6.5e."""
+    x = _rows_with_outliers()
+    f = synth.bf16_float(x).astype(np.float64)
+    codes, sf, scale = orc.quant_nvfp4(x)
+    xh = orc.dequant_nvfp4(codes, sf, scale)
+    e = np.repeat(orc.e4m3_value(sf) * scale[:, None].astype(np.float64), 16, axis=1)
+    e32 = (orc.e4m3_value(sf).astype(np.float32) * scale[:, None]).astype(np.float64)
+    e32 = np.repeat(e32, 16, axis=1)
+    live = e > 0
+    q = np.abs(f[live] / e32[live])
+    step = np.select([q < 2, q < 4], [0.5, 1.0], 2.0)
+    err = np.abs(f[live] - xh[live])
+    sat = q >= 6
+    bound = 0.5 * step * e32[live] * (1 + 2.0 ** -22) + np.abs(f[live]) * 2.0 ** -22
+    assert np.all(err[~sat] <= bound[~sat])
+    assert np.all(np.abs(xh[live][sat]) == 6 * e[live][sat])
+    # a normal E4M3 block scale is within 2^-4 of amax_b / (6 S), so nothing in
+    # such a block lies further out than 6 e (1 + 2^-4) / (1 - 2^-4) < 6.5 e
+    normal = np.repeat(sf >= 0x08, 16, axis=1)[live]
+    assert np.all(np.abs(f[live][normal]) <= 6.5 * e32[live][normal])
+    assert np.all(xh[~live] == 0)
+
+
+def check_nvfp4_exact_grid(orc):
+    """A row whose values all lie on the E2M1 grid with amax 6 (S = fl32(6/2688),
+    every block scale 448, e = fl32(448 S) = 1 exactly, so every quotient is exact)
+    gets the grid codes back, and dequantizes to x * (448 S) exactly."""
+    grid = np.array(E2M1_GRID + [-g for g in E2M1_GRID], np.float32)
+    row = np.tile(grid, 4)[:64]
+    row[0] = 6.0
+    xb = synth.bf16_bits(row).reshape(1, -1)
+    codes, sf, scale = orc.quant_nvfp4(xb)
+    assert np.all(sf == 0x7E)
+    nib = np.stack([codes & 0xF, codes >> 4], -1).reshape(-1)
+    assert np.array_equal(orc.e2m1_value(nib), row.astype(np.float64))
+    xh = orc.dequant_nvfp4(codes, sf, scale)
+    assert np.array_equal(xh.reshape(-1), row.astype(np.float64) * (448.0 * float(scale[0])))
+
+
+# ---------------------------------------------------------- MXFP8 pins -------
+def check_mxfp8_rows(orc):
+    """Row-wise MXFP8 on random data with outliers and tiny blocks:
+      * the scale rule: for a non-zero block, amax / 2^(code-127) lies in [256, 512);
+      * elements: code = torch float8_e4m3fn cast of the exact x / X where that is
+        below 448 in magnitude, 0x7e / 0xfe where it is 448 or more;
+      * error: |x_hat - x| <= 2^-4 |x| in the E4M3 normal range."""
+    import torch
+
+    rng = np.random.default_rng(21)
+    f = rng.standard_normal((48, 256), dtype=np.float32)
+    f[rng.random(f.shape) < 0.01] *= 1000.0
+    f[::5] *= np.float32(1e-30)
+    f[7, :32] = 0.0
+    x = synth.bf16_bits(f)
+    fv = synth.bf16_float(x).astype(np.float64)
+    codes, sf = orc.quant_mxfp8_rows(x)
+    X = np.repeat(np.ldexp(1.0, sf.astype(np.int64) - 127), 32, axis=1)
+    blocks = np.abs(fv).reshape(48, 8, 32).max(axis=2)
+    nz = blocks > 0
+    ratio = blocks[nz] / np.ldexp(1.0, sf[nz].astype(np.int64) - 127)
+    assert np.all((ratio >= 256) & (ratio < 512)), ratio.min()
+    assert np.all(sf[~nz] == 0)
+    q = fv / X
+    small = np.abs(q) < 448
+    want = torch.from_numpy(q[small].astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes[small], want)
+    big = codes[~small]
+    assert np.all((big == 0x7E) | (big == 0xFE))
+    xh = orc.dequant_mxfp8(codes, sf)
+    normal = small & (np.abs(q) >= 2.0 ** -6)
+    assert np.all(np.abs(xh[normal] - fv[normal]) <= 2.0 ** -4 * np.abs(fv[normal]))
+
+
+def check_mxfp8_cols(orc):
+    """Column-wise MXFP8 equals row-wise MXFP8 of each group's transposed rows,
+    zero-padded to a multiple of 128 positions; padded offsets are the running
+    sum of the rounded-up group sizes."""
+    rng = np.random.default_rng(31)
+    counts = np.array([0, 37, 128, 1, 0, 200, 95])
+    off = synth.offsets_from_counts(counts)
+    rows = int(off[-1])
+    x = synth.bf16_bits(rng.standard_normal((rows, 64), dtype=np.float32) * 3)
+    ct, st, poff = orc.quant_mxfp8_cols(x, off)
+    want_poff = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)])
+    assert np.array_equal(poff, want_poff)
+    for g in range(len(counts)):
+        n = counts[g]
+        pad = (n + 127) // 128 * 128
+        seg = np.zeros((pad, 64), np.uint16)
+        seg[:n] = x[off[g]: off[g] + n]
+        rc, rs = orc.quant_mxfp8_rows(np.ascontiguousarray(seg.T))
+        assert np.array_equal(ct[:, poff[g]: poff[g] + pad], rc), g
+        assert np.array_equal(st[:, poff[g] // 32: (poff[g] + pad) // 32], rs), g
+
+
+def check_mxfp8_single_group_is_transpose(orc):
+    """With one group and rows a multiple of 128, column-wise is row-wise of X^T."""
+    rng = np.random.default_rng(32)
+    x = synth.bf16_bits(rng.standard_normal((256, 96), dtype=np.float32))
+    ct, st, _ = orc.quant_mxfp8_cols(x, np.array([0, 256]))
+    rc, rs = orc.quant_mxfp8_rows(np.ascontiguousarray(x.T))
+    assert np.array_equal(ct, rc) and np.array_equal(st, rs)
+
+
+# ----------------------------------------------------------------- GEMM ------
+def check_gemm_vs_torch(orc):
+    """fp64 GEMM on dequantized operands against torch.matmul in float64."""
+    import torch
+
+    rng = np.random.default_rng(41)
+    a = rng.standard_normal((7, 48))
+    b = rng.standard_normal((5, 48))
+    got = orc.gemm_abt(a, b)
+    want = (torch.from_numpy(a) @ torch.from_numpy(b).T).numpy()
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-13)
+    assert got.shape == (7, 5)
+
+
+def check_gemm_identity(orc):
+    """B = I gives Y = A exactly (no transposition, no lost term)."""
+    rng = np.random.default_rng(42)
+    a = rng.standard_normal((6, 32))
+    assert np.array_equal(orc.gemm_abt(a, np.eye(32)), a)
+    perm = rng.permutation(32)
+    assert np.array_equal(orc.gemm_abt(a, np.eye(32)[perm]), a[:, perm])
+
+
+def check_quantized_gemm_end_to_end(orc):
+    """NVFP4 forward on 16-wide rows whose values lie on the E2M1 grid (block
+    scales 448, e = 1, so the codes are the values): the closed form is
+    y = (x . w) * (448 S_x) * (448 S_w)."""
+    grid = np.array(E2M1_GRID, np.float32)
+    xa = np.zeros((2, 16), np.float32)
+    xa[0, :8] = grid
+    xa[1, :8] = -grid[::-1]
+    wa = np.zeros((3, 16), np.float32)
+    wa[0, :8] = grid
+    wa[1, 8:] = grid
+    wa[2, 0] = 6.0
+    xb, wb = synth.bf16_bits(xa), synth.bf16_bits(wa)
+    ca, sa, ta = orc.quant_nvfp4(xb)
+    cb, sb, tb = orc.quant_nvfp4(wb)
+    y = orc.gemm_abt(orc.dequant_nvfp4(ca, sa, ta), orc.dequant_nvfp4(cb, sb, tb))
+    assert np.all(sa == 0x7E) and np.all(sb[sb != 0] == 0x7E)
+    want = (xa.astype(np.float64) @ wa.astype(np.float64).T) * (448.0 * ta[:, None].astype(np.float64)) \
+        * (448.0 * tb[None, :].astype(np.float64))
+    assert np.allclose(y, want, rtol=1e-14, atol=0), (y, want)
+
+
+ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

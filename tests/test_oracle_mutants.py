@@ -1,0 +1,85 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins catch each.
+
+Every mutant is the oracle's C source with one snippet replaced, compiled with
+the oracle's own flags into a temporary folder and loaded as a separate library.
+The test passes when at least one pin of ``tests/pins.py`` fails on every mutant,
+and every snippet still occurs exactly once in the real source (so a stale
+mutation cannot pass silently).  No GPU is involved.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import pins
+
+MUTANTS = {
+    # rounding
+    "ties_away_from_even": ("idx = (lo % 2 == 0) ? lo : hi;", "idx = hi;"),
+    "sign_dropped": ("return (uint8_t)((neg << sign_shift) | idx);", "return (uint8_t)(idx);"),
+    "no_saturation_to_max": ("    if (a >= mag[n - 1]) {\n        idx = n - 1;",
+                             "    if (a >= mag[n - 1]) {\n        idx = n - 2;"),
+    "e4m3_wrong_bias": ("mag = ldexp(1.0 + man / 8.0, exp - 7);", "mag = ldexp(1.0 + man / 8.0, exp - 8);"),
+    # NVFP4 per-token scale
+    "scale_constant_2048": ("float s_t = amax / 2688.0f;", "float s_t = amax / 2048.0f;"),
+    "block_divisor_without_6": ("float d = 6.0f * s_t;", "float d = s_t;"),
+    "reciprocal_multiply": ("float q = bf16_value(xb[j]) / e;", "float q = bf16_value(xb[j]) * (1.0f / e);"),
+    "row_amax_from_first_block": (
+        "        for (int64_t j = 0; j < k; ++j) {\n            float a = fabsf(bf16_value(xr[j]));",
+        "        for (int64_t j = 0; j < 16; ++j) {\n            float a = fabsf(bf16_value(xr[j]));"),
+    "block_amax_half_block": (
+        "            for (int j = 0; j < 16; ++j) {\n                float a = fabsf(bf16_value(xb[j]));",
+        "            for (int j = 0; j < 8; ++j) {\n                float a = fabsf(bf16_value(xb[j]));"),
+    "nibbles_swapped": ("if (kk % 2 == 0)", "if (kk % 2 == 1)"),
+    "zero_scale_block_divided": ("            if (sb_val == 0.0)\n                continue; /* block codes stay 0x0 */\n",
+                                 ""),
+    "dequant_drops_token_scale": ("out[t * k + j] = fme_orc_e2m1_value(c) * sb * (double)scale[t];",
+                                  "out[t * k + j] = fme_orc_e2m1_value(c) * sb;"),
+    # MXFP8
+    "mx_emax_7": ("int code = u - 8 + 127;", "int code = u - 7 + 127;"),
+    "mx_zero_block_scale_127": ("    if (amax == 0.0f)\n        return 0;", "    if (amax == 0.0f)\n        return 127;"),
+    "mx_element_scale_off_by_one": ("double q = ldexp((double)v[j], 127 - (int)sc);",
+                                    "double q = ldexp((double)v[j], 128 - (int)sc);"),
+    "colwise_pads_to_32": ("int64_t padded = ((n_g + 127) / 128) * 128;", "int64_t padded = ((n_g + 31) / 32) * 32;"),
+    # GEMM
+    "gemm_transposed_operand": ("acc += a[i * k + q] * b[j * k + q];", "acc += a[i * k + q] * b[q * n + j];"),
+    "gemm_drops_last_term": ("for (int64_t q = 0; q < k; ++q)\n                acc +=",
+                             "for (int64_t q = 0; q < k - 1; ++q)\n                acc +="),
+}
+
+
+def _run_pins(lib_path):
+    orc = oracle.Oracle(lib=oracle.load(lib_path))
+    failed = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except AssertionError:
+            failed.append(check.__name__)
+        except pytest.skip.Exception:
+            pass
+        except Exception as exc:  # a crash inside a pin also counts as caught
+            failed.append(f"{check.__name__}:{type(exc).__name__}")
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    src = open(oracle.SOURCE).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation snippet for {name} no longer matches the oracle"
+    mutated = tmp_path / f"mutant_{name}.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / f"libmutant_{name}.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(lib), str(mutated), "-lm"], check=True)
+    failed = _run_pins(str(lib))
+    assert failed, f"no pin caught the planted mistake {name}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    lib = tmp_path / "libcopy.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(lib), oracle.SOURCE, "-lm"], check=True)
+    failed = _run_pins(str(lib))
+    assert not failed, failed
