@@ -1,1 +1,235 @@
-"""GB300-native low-precision MoE expert path (NVFP4 forward, MXFP8 backward)."""
+"""GB300-native low-precision MoE expert path: NVFP4 per-token forward, MXFP8 backward.
+
+A thin ctypes binding over ``libfme.so`` (C ABI in ``include/fme.h``).  Every
+step of the path runs in the library's CUDA kernels; this module only turns
+torch tensors into pointers, allocates outputs with torch when the caller does
+not pass them, and turns status codes into exceptions.  There is no fallback:
+if the library is missing or the device is not a GB300, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libfme.so")
+
+ROWWISE = 0
+COLWISE = 1
+MAX_GROUPS = 1024
+DEV_TIMEOUT = 0x1
+DEV_BAD_OFFSETS = 0x2
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FmeError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: status {status}"
+        if _lib is not None:
+            msg += f" ({_lib.fme_error_string(status).decode()})"
+        if detail:
+            msg += f": {detail}"
+        super().__init__(msg)
+
+
+def ensure_built() -> str:
+    """Build libfme.so if it is missing or older than its sources."""
+    from . import build as _build
+
+    if _build.stale():
+        _build.build()
+    return LIBRARY
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise RuntimeError(f"{LIBRARY} is missing: build it with "
+                                   "`python -m fp8_moe_expert_gb300.build` (no CPU fallback exists)")
+            _lib = _declare(ctypes.CDLL(LIBRARY))
+    return _lib
+
+
+SYMBOLS = {
+    # name: (restype, argtypes)
+    "quantize_nvfp4_pertoken": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p"]),
+    "quantize_mxfp8": ("i32", ["p", "i64", "i64", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
+    "grouped_gemm_fwd_nvfp4": ("i32", ["p", "p", "p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p",
+                                       "p"]),
+    "grouped_gemm_dgrad_mxfp8": ("i32", ["p", "p", "p", "p", "i64", "p", "i32", "i64", "i64", "i64", "p", "p",
+                                         "p"]),
+    "grouped_gemm_wgrad_mxfp8": ("i32", ["p", "p", "i64", "p", "p", "i64", "p", "i32", "i64", "i64", "p", "p",
+                                         "p"]),
+    "fme_sf_padded_rows": ("i64", ["i64", "i32"]),
+    "fme_sf_bytes": ("i64", ["i64", "i64", "i32", "i32"]),
+    "fme_colwise_ld": ("i64", ["i64", "i32"]),
+    "fme_read_device_status": ("i32", ["p", "p", "p"]),
+    "fme_error_string": ("s", ["i32"]),
+    "fme_last_cuda_error": ("s", []),
+    "fme_version": ("s", []),
+}
+
+_CT = {"i32": ctypes.c_int32, "i64": ctypes.c_int64, "p": ctypes.c_void_p, "s": ctypes.c_char_p}
+
+
+def _declare(handle):
+    for name, (res, args) in SYMBOLS.items():
+        fn = getattr(handle, name)
+        fn.restype = _CT[res]
+        fn.argtypes = [_CT[a] for a in args]
+    return handle
+
+
+# ------------------------------------------------------------------ helpers --
+def sf_padded_rows(rows: int, num_groups: int = 1) -> int:
+    return int(lib().fme_sf_padded_rows(rows, num_groups))
+
+
+def sf_bytes(rows: int, cols: int, block: int, num_groups: int = 1) -> int:
+    return int(lib().fme_sf_bytes(rows, cols, block, num_groups))
+
+
+def colwise_ld(rows: int, num_groups: int = 1) -> int:
+    return int(lib().fme_colwise_ld(rows, num_groups))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        detail = lib().fme_last_cuda_error().decode() if status == 5 else ""
+        raise FmeError(status, where, detail)
+
+
+def _groups(offsets, num_groups):
+    if offsets is None:
+        return None, 1 if num_groups is None else num_groups
+    n = offsets.numel() - 1 if num_groups is None else num_groups
+    return offsets, n
+
+
+def _empty(shape, dtype, device):
+    import torch
+
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+# --------------------------------------------------------------- the five calls --
+def quantize_nvfp4_pertoken(x, offsets=None, num_groups=None, *, codes=None, sf=None, row_scale=None,
+                            status=None, stream=None):
+    """NVFP4 per-token quantization of bf16 x [rows, k] -> (codes [rows, k/2] u8,
+    sf (tiled E4M3 scales) u8, row_scale [rows] f32)."""
+    import torch
+
+    rows, k = x.shape
+    offsets, g = _groups(offsets, num_groups)
+    dev = x.device
+    if codes is None:
+        codes = _empty((rows, k // 2), torch.uint8, dev)
+    if sf is None:
+        sf = _empty((max(sf_bytes(rows, k, 16, g), 16),), torch.uint8, dev)
+    if row_scale is None:
+        row_scale = _empty((rows,), torch.float32, dev)
+    st = lib().quantize_nvfp4_pertoken(_ptr(x), rows, k, _ptr(offsets), g, _ptr(codes), _ptr(sf), _ptr(row_scale),
+                                       _ptr(status), _stream(stream))
+    _check(st, "quantize_nvfp4_pertoken")
+    return codes, sf, row_scale
+
+
+def quantize_mxfp8(x, axis=ROWWISE, offsets=None, num_groups=None, *, codes=None, sf=None, padded_offsets=None,
+                   status=None, stream=None):
+    """MXFP8 quantization of bf16 x [rows, cols].
+
+    ROWWISE -> (codes [rows, cols] u8, sf tiled E8M0 u8).
+    COLWISE -> (codes [cols, ld] u8, sf tiled u8, padded_offsets [G+1] i32, ld)."""
+    import torch
+
+    rows, cols = x.shape
+    offsets, g = _groups(offsets, num_groups)
+    dev = x.device
+    if axis == ROWWISE:
+        if codes is None:
+            codes = _empty((rows, cols), torch.uint8, dev)
+        if sf is None:
+            sf = _empty((max(sf_bytes(rows, cols, 32, g), 16),), torch.uint8, dev)
+        st = lib().quantize_mxfp8(_ptr(x), rows, cols, axis, _ptr(offsets), g, _ptr(codes), _ptr(sf), None,
+                                  _ptr(status), _stream(stream))
+        _check(st, "quantize_mxfp8")
+        return codes, sf
+    ld = colwise_ld(rows, g)
+    if codes is None:
+        codes = _empty((cols, ld), torch.uint8, dev)
+    if sf is None:
+        sf = _empty((max(sf_bytes(cols, ld, 32, 1), 16),), torch.uint8, dev)
+    if padded_offsets is None:
+        padded_offsets = _empty((g + 1,), torch.int32, dev)
+    st = lib().quantize_mxfp8(_ptr(x), rows, cols, axis, _ptr(offsets), g, _ptr(codes), _ptr(sf),
+                              _ptr(padded_offsets), _ptr(status), _stream(stream))
+    _check(st, "quantize_mxfp8")
+    return codes, sf, padded_offsets, ld
+
+
+def grouped_gemm_fwd_nvfp4(a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offsets, n, k, *, y=None,
+                           status=None, stream=None):
+    import torch
+
+    m = a_codes.shape[0]
+    e = offsets.numel() - 1
+    if y is None:
+        y = _empty((m, n), torch.bfloat16, a_codes.device)
+    st = lib().grouped_gemm_fwd_nvfp4(_ptr(a_codes), _ptr(a_sf), _ptr(a_scale), _ptr(b_codes), _ptr(b_sf),
+                                      _ptr(b_scale), _ptr(offsets), e, m, n, k, _ptr(y), _ptr(status),
+                                      _stream(stream))
+    _check(st, "grouped_gemm_fwd_nvfp4")
+    return y
+
+
+def grouped_gemm_dgrad_mxfp8(a_codes, a_sf, b_codes, b_sf, ldb, offsets, n, k, *, y=None, status=None,
+                             stream=None):
+    import torch
+
+    m = a_codes.shape[0]
+    e = offsets.numel() - 1
+    if y is None:
+        y = _empty((m, n), torch.bfloat16, a_codes.device)
+    st = lib().grouped_gemm_dgrad_mxfp8(_ptr(a_codes), _ptr(a_sf), _ptr(b_codes), _ptr(b_sf), ldb, _ptr(offsets),
+                                        e, m, n, k, _ptr(y), _ptr(status), _stream(stream))
+    _check(st, "grouped_gemm_dgrad_mxfp8")
+    return y
+
+
+def grouped_gemm_wgrad_mxfp8(a_codes, a_sf, lda, b_codes, b_sf, ldb, padded_offsets, m, n, *, y=None,
+                             status=None, stream=None):
+    import torch
+
+    e = padded_offsets.numel() - 1
+    if y is None:
+        y = _empty((e, m, n), torch.bfloat16, padded_offsets.device)
+    st = lib().grouped_gemm_wgrad_mxfp8(_ptr(a_codes), _ptr(a_sf), lda, _ptr(b_codes), _ptr(b_sf), ldb,
+                                        _ptr(padded_offsets), e, m, n, _ptr(y), _ptr(status), _stream(stream))
+    _check(st, "grouped_gemm_wgrad_mxfp8")
+    return y
+
+
+def read_device_status(status, stream=None) -> tuple[int, int]:
+    """Synchronise the stream and read a device status word -> (status code, raw bits)."""
+    raw = ctypes.c_int32(0)
+    st = lib().fme_read_device_status(_ptr(status), _stream(stream), ctypes.byref(raw))
+    return int(st), int(raw.value)

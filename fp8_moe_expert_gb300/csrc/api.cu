@@ -1,0 +1,335 @@
+// api.cu -- the extern "C" boundary of libfme.so (declared in include/fme.h):
+// host-side argument checks, device checks, TMA descriptor encoding, launches.
+// Nothing here allocates device memory or synchronises a stream, except
+// fme_read_device_status, which is documented to synchronise.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/fme.h"
+#include "fme_launch.h"
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+fme_status cuda_fail(cudaError_t err, const char *where) {
+  g_last_cuda_error = std::string(where) + ": " + cudaGetErrorString(err);
+  return FME_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device facts, looked up once per device.
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 unknown, 1 supported, 2 unsupported
+  int num_sms = 0;
+};
+DeviceInfo g_devices[64];
+std::mutex g_device_mutex;
+
+fme_status current_device(int *num_sms) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return FME_ERR_UNSUPPORTED_DEVICE;
+  DeviceInfo &d = g_devices[dev];
+  if (d.state.load(std::memory_order_acquire) == 0) {
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    if (d.state.load(std::memory_order_relaxed) == 0) {
+      int major = 0, minor = 0, sms = 0;
+      if ((err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+          (err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+          (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(err, "cudaDeviceGetAttribute");
+      d.num_sms = sms;
+      d.state.store((major == 10 && minor == 3) ? 1 : 2, std::memory_order_release);
+    }
+  }
+  if (d.state.load(std::memory_order_acquire) != 1) return FME_ERR_UNSUPPORTED_DEVICE;
+  *num_sms = d.num_sms;
+  return FME_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver, fetched once through the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+fme_status get_encoder(EncodeTiledFn *fn) {
+  std::call_once(g_encode_once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (g_encode == nullptr) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled not available from the driver";
+    return FME_ERR_CUDA;
+  }
+  *fn = g_encode;
+  return FME_OK;
+}
+
+// 2-D uint8 tensor [rows x inner] (row stride `stride` bytes), box {128 bytes, box_rows},
+// 128-byte swizzle, zero fill out of bounds.
+fme_status encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint64_t stride,
+                        uint32_t box_rows) {
+  EncodeTiledFn fn;
+  fme_status st = get_encoder(&fn);
+  if (st != FME_OK) return st;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {stride};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    g_last_cuda_error = buf;
+    return FME_ERR_CUDA;
+  }
+  return FME_OK;
+}
+
+int64_t padded_rows_bound(int64_t rows, int32_t groups) {
+  if (rows < 0 || groups < 1) return 0;
+  return ((rows + 127 * static_cast<int64_t>(groups)) / 128) * 128;
+}
+
+fme_status check_groups(int32_t num_groups) {
+  return (num_groups < 1 || num_groups > FME_MAX_GROUPS) ? FME_ERR_INVALID_ARGUMENT : FME_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t fme_sf_padded_rows(int64_t rows, int32_t num_groups) { return padded_rows_bound(rows, num_groups); }
+
+int64_t fme_sf_bytes(int64_t rows, int64_t cols, int32_t block, int32_t num_groups) {
+  if (cols < 0 || block <= 0 || cols % block) return 0;
+  const int64_t c4 = ((cols / block) + 3) / 4 * 4;
+  return padded_rows_bound(rows, num_groups) * c4;
+}
+
+int64_t fme_colwise_ld(int64_t rows, int32_t num_groups) { return padded_rows_bound(rows, num_groups); }
+
+const char *fme_version(void) { return "fme 0.1.0 (sm_103a)"; }
+
+const char *fme_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+const char *fme_error_string(fme_status status) {
+  switch (status) {
+    case FME_OK: return "ok";
+    case FME_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case FME_ERR_MISALIGNED: return "pointer or leading dimension not 16-byte aligned";
+    case FME_ERR_UNSUPPORTED_SHAPE: return "shape outside the supported tiling";
+    case FME_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (GB300)";
+    case FME_ERR_CUDA: return "CUDA error";
+    case FME_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
+    case FME_ERR_DEVICE_BAD_OFFSETS: return "offsets do not rise from 0 to rows";
+    default: return "unknown status";
+  }
+}
+
+fme_status fme_read_device_status(const int32_t *dev_status, void *stream, int32_t *raw) {
+  if (dev_status == nullptr) return FME_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  cudaError_t err = cudaMemcpyAsync(&host, dev_status, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaMemcpyAsync(status)");
+  err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaStreamSynchronize");
+  if (raw) *raw = host;
+  if (host & FME_DEV_BAD_OFFSETS) return FME_ERR_DEVICE_BAD_OFFSETS;
+  if (host & FME_DEV_TIMEOUT) return FME_ERR_DEVICE_TIMEOUT;
+  return FME_OK;
+}
+
+fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const int32_t *offsets,
+                                   int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale,
+                                   int32_t *dev_status, void *stream) {
+  if (rows < 0 || check_groups(num_groups) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (offsets == nullptr && num_groups != 1) return FME_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0 || k < 64 || k > 8192) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (rows > (int64_t(1) << 31) - 1) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return FME_OK;
+  if (!x || !codes || !sf || !row_scale) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) || !aligned16(row_scale)) return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchNvfp4 a{x, rows, k, offsets, num_groups, codes, sf, row_scale, dev_status, sms,
+                     static_cast<cudaStream_t>(stream)};
+  cudaError_t err = fme::launch_quantize_nvfp4(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_nvfp4_pertoken launch");
+}
+
+fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axis, const int32_t *offsets,
+                          int32_t num_groups, uint8_t *codes, uint8_t *sf, int32_t *padded_offsets,
+                          int32_t *dev_status, void *stream) {
+  if (rows < 0 || check_groups(num_groups) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (offsets == nullptr && num_groups != 1) return FME_ERR_INVALID_ARGUMENT;
+  if (axis != FME_ROWWISE && axis != FME_COLWISE) return FME_ERR_INVALID_ARGUMENT;
+  if (rows > (int64_t(1) << 31) - 1 - 128 * static_cast<int64_t>(num_groups)) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (axis == FME_ROWWISE) {
+    if (padded_offsets != nullptr) return FME_ERR_INVALID_ARGUMENT;
+    if (cols % 32 != 0 || cols < 32 || cols > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return FME_OK;
+  } else {
+    if (cols % 128 != 0 || cols < 128 || cols > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
+    if (padded_offsets == nullptr) return FME_ERR_INVALID_ARGUMENT;
+    if (!aligned16(padded_offsets)) return FME_ERR_MISALIGNED;
+  }
+  if (!x || !codes || !sf) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf)) return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchMxfp8 a{x, rows, cols, offsets, num_groups, codes, sf, padded_offsets,
+                     fme_colwise_ld(rows, num_groups), dev_status, sms, static_cast<cudaStream_t>(stream)};
+  cudaError_t err =
+      (axis == FME_ROWWISE) ? fme::launch_quantize_mxfp8_rows(a) : fme::launch_quantize_mxfp8_cols(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_mxfp8 launch");
+}
+
+fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
+                                  const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
+                                  const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n, int64_t k,
+                                  void *y, int32_t *dev_status, void *stream) {
+  if (m < 0 || n < 0 || k < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (n % 256 != 0 || n == 0 || k % 256 != 0 || k == 0 || k > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (m > (int64_t(1) << 31) - 1 || static_cast<int64_t>(num_experts) * n > (int64_t(1) << 31) - 1)
+    return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets) return FME_ERR_INVALID_ARGUMENT;
+  if (m == 0) return FME_OK;
+  if (!a_codes || !a_sf || !a_scale || !b_codes || !b_sf || !b_scale || !y) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a_codes) || !aligned16(a_sf) || !aligned16(a_scale) || !aligned16(b_codes) ||
+      !aligned16(b_sf) || !aligned16(b_scale) || !aligned16(y) || !aligned16(offsets))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchGemm a{};
+  a.kind = fme::GemmKind::kFwdNvfp4;
+  if ((st = encode_u8_2d(&a.map_a, a_codes, k / 2, m, k / 2, 128)) != FME_OK) return st;
+  if ((st = encode_u8_2d(&a.map_b, b_codes, k / 2, static_cast<uint64_t>(num_experts) * n, k / 2, 256)) != FME_OK)
+    return st;
+  a.sfa = a_sf;
+  a.sfb = b_sf;
+  a.a_scale = a_scale;
+  a.b_scale = b_scale;
+  a.offsets = offsets;
+  a.num_experts = num_experts;
+  a.m = m;
+  a.n = n;
+  a.k = k;
+  a.sfa_stride = (k / 16) * 128;  // (C4 / 4) tiles of 512 bytes per 128 rows
+  a.sfb_stride = (k / 16) * 128;
+  a.y = y;
+  a.status = dev_status;
+  a.num_sms = sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t err = fme::launch_grouped_gemm(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_fwd_nvfp4 launch");
+}
+
+fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, const uint8_t *b_codes,
+                                    const uint8_t *b_sf, int64_t ldb, const int32_t *offsets, int32_t num_experts,
+                                    int64_t m, int64_t n, int64_t k, void *y, int32_t *dev_status, void *stream) {
+  if (m < 0 || n < 0 || k < 0 || ldb < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (n % 256 != 0 || n == 0 || k % 128 != 0 || k == 0 || ldb % 128 != 0) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (ldb < static_cast<int64_t>(num_experts) * k) return FME_ERR_INVALID_ARGUMENT;
+  if (m > (int64_t(1) << 31) - 1 || ldb > (int64_t(1) << 31) - 1 || k > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets) return FME_ERR_INVALID_ARGUMENT;
+  if (m == 0) return FME_OK;
+  if (!a_codes || !a_sf || !b_codes || !b_sf || !y) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a_codes) || !aligned16(a_sf) || !aligned16(b_codes) || !aligned16(b_sf) || !aligned16(y) ||
+      !aligned16(offsets))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchGemm a{};
+  a.kind = fme::GemmKind::kDgradMxfp8;
+  if ((st = encode_u8_2d(&a.map_a, a_codes, k, m, k, 128)) != FME_OK) return st;
+  if ((st = encode_u8_2d(&a.map_b, b_codes, ldb, n, ldb, 256)) != FME_OK) return st;
+  a.sfa = a_sf;
+  a.sfb = b_sf;
+  a.offsets = offsets;
+  a.num_experts = num_experts;
+  a.m = m;
+  a.n = n;
+  a.k = k;
+  a.sfa_stride = (k / 32) * 128;
+  a.sfb_stride = (ldb / 32) * 128;
+  a.ldb = ldb;
+  a.y = y;
+  a.status = dev_status;
+  a.num_sms = sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t err = fme::launch_grouped_gemm(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_dgrad_mxfp8 launch");
+}
+
+fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda,
+                                    const uint8_t *b_codes, const uint8_t *b_sf, int64_t ldb,
+                                    const int32_t *padded_offsets, int32_t num_experts, int64_t m, int64_t n,
+                                    void *y, int32_t *dev_status, void *stream) {
+  if (m < 0 || n < 0 || lda < 0 || ldb < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (m % 128 != 0 || m == 0 || n % 256 != 0 || n == 0 || lda % 128 != 0 || ldb % 128 != 0)
+    return FME_ERR_UNSUPPORTED_SHAPE;
+  if (lda > (int64_t(1) << 31) - 1 || ldb > (int64_t(1) << 31) - 1 || m > 65536 || n > 65536)
+    return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!padded_offsets || !y) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(y) || !aligned16(padded_offsets)) return FME_ERR_MISALIGNED;
+  const bool has_positions = lda > 0 && ldb > 0;
+  if (has_positions) {
+    if (!a_codes || !a_sf || !b_codes || !b_sf) return FME_ERR_INVALID_ARGUMENT;
+    if (!aligned16(a_codes) || !aligned16(a_sf) || !aligned16(b_codes) || !aligned16(b_sf))
+      return FME_ERR_MISALIGNED;
+  }
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchGemm a{};
+  a.kind = fme::GemmKind::kWgradMxfp8;
+  // With no positions at all every expert is empty: the maps are never used, so
+  // point them at a one-tile dummy extent of y (always at least 128 x 256 x 2 bytes).
+  const void *abase = has_positions ? static_cast<const void *>(a_codes) : y;
+  const void *bbase = has_positions ? static_cast<const void *>(b_codes) : y;
+  const int64_t lda_e = has_positions ? lda : 128, ldb_e = has_positions ? ldb : 128;
+  if ((st = encode_u8_2d(&a.map_a, abase, lda_e, has_positions ? m : 128, lda_e, 128)) != FME_OK) return st;
+  if ((st = encode_u8_2d(&a.map_b, bbase, ldb_e, has_positions ? n : 256, ldb_e, 256)) != FME_OK) return st;
+  a.sfa = a_sf;
+  a.sfb = b_sf;
+  a.offsets = padded_offsets;
+  a.num_experts = num_experts;
+  a.m = m;
+  a.n = n;
+  a.k = 0;
+  a.sfa_stride = (lda / 32) * 128;
+  a.sfb_stride = (ldb / 32) * 128;
+  a.lda = lda;
+  a.ldb = ldb;
+  a.y = y;
+  a.status = dev_status;
+  a.num_sms = sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t err = fme::launch_grouped_gemm(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_wgrad_mxfp8 launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// fme_launch.h -- host-side launch descriptions passed from the C ABI layer
+// (api.cu, which validates arguments) to the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fme {
+
+struct LaunchNvfp4 {
+  const void *x;
+  int64_t rows, k;
+  const int32_t *offsets;
+  int32_t num_groups;
+  uint8_t *codes, *sf;
+  float *row_scale;
+  int32_t *status;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+struct LaunchMxfp8 {
+  const void *x;
+  int64_t rows, cols;
+  const int32_t *offsets;
+  int32_t num_groups;
+  uint8_t *codes, *sf;
+  int32_t *padded_offsets;  // column-wise only
+  int64_t ld;               // column-wise only
+  int32_t *status;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2 };
+
+struct LaunchGemm {
+  GemmKind kind;
+  CUtensorMap map_a, map_b;
+  const uint8_t *sfa, *sfb;
+  const float *a_scale, *b_scale;  // forward only
+  const int32_t *offsets;          // row offsets (fwd, dgrad) or padded offsets (wgrad)
+  int32_t num_experts;
+  int64_t m, n, k;          // GEMM sizes; k unused for wgrad (per-expert)
+  int64_t sfa_stride;       // bytes between 128-row scale tiles of A
+  int64_t sfb_stride;       // bytes between 128-row scale tiles of B
+  int64_t lda, ldb;         // wgrad: position extents of A and B; dgrad: ldb
+  void *y;
+  int32_t *status;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a);
+cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a);
+cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a);
+cudaError_t launch_grouped_gemm(const LaunchGemm &a);
+
+}  // namespace fme

@@ -1,0 +1,403 @@
+// gemm.cu -- block-scaled grouped GEMMs on the tcgen05 tensor cores.
+//
+// "Composer 2 Technical Report" (papercache.org summary), section 6.1: the MoE
+// layer's grouped GEMMs run as block-scaled tensor-core MMAs on Blackwell (the
+// scales are applied inside the systolic-array multiply); NVFP4 with a per-token
+// FP32 scale applied in the GEMM epilogue for the forward, MXFP8 for the
+// backward.  "Scaling and Optimizing Frontier Model Training", "MXFP8 expert
+// kernels": grouped GEMMs over the experts' routed tokens.
+//
+// One persistent kernel per call, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the 512-byte
+//               scale tiles into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 tensor-memory columns, then one thread copies each
+//               stage's scales into tensor memory (tcgen05.cp) and issues the
+//               block-scaled MMAs (kind::mxf4nvf4 or kind::mxf8f6f4, M=128,
+//               N=256) into a 128 x 256 fp32 accumulator;
+//   warps 2-5   epilogue: tcgen05.ld the accumulator (each warp its 32-lane
+//               quarter), apply the per-token and per-column FP32 scales
+//               (forward), round to bf16, store rows that belong to the expert.
+// Tiles are 128 rows x 256 columns.  Every role walks the same tile sequence,
+// derived in shared memory from the per-expert offsets: forward and dgrad go
+// expert by expert, 128-row blocks of each expert's rows, 256-column blocks
+// fastest; wgrad goes expert by expert in decreasing order of work (largest
+// contraction first) and writes zeros for experts without rows.  There is no
+// split over K: each output element is one accumulation in one CTA, so a row's
+// result does not depend on other rows.
+#include "fme_device.cuh"
+#include "fme_launch.h"
+
+namespace fme {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kStageKBytes = 128;  // bytes of K per row per stage (one swizzle row)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kAccCols = kBN;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kABytes = kBM * kStageKBytes;
+constexpr int kBBytes = kBN * kStageKBytes;
+
+template <GemmKind K>
+struct Cfg {
+  static constexpr bool kFp4 = (K == GemmKind::kFwdNvfp4);
+  static constexpr int kKPerStage = kFp4 ? 256 : 128;    // elements of K per stage
+  static constexpr int kAtoms = kFp4 ? 4 : 1;            // 512-byte scale tiles per 128 rows per stage
+  static constexpr int kSfaBytes = 512 * kAtoms;
+  static constexpr int kSfbBytes = 2 * 512 * kAtoms;     // two 128-row halves of the N tile
+  static constexpr int kSfaCols = 4 * kAtoms;            // tensor-memory columns per stage
+  static constexpr int kSfbCols = 8 * kAtoms;
+  static constexpr int kSfCols = kSfaCols + kSfbCols;
+  static constexpr int kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kSmemBytes = kStages * kStageTx + 1024;  // + alignment slack
+  static_assert(kAccCols + 2 * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
+};
+
+struct SharedState {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int ok_flag;
+  // fwd, dgrad: groups.off = row offsets, groups.tiles = 128-row tile prefix.
+  // wgrad: groups.off = padded offsets, groups.tiles = experts by decreasing work.
+  GroupTable groups;
+};
+
+struct Tile {
+  int32_t e;
+  int32_t num_k;       // K stages; 0 = expert without rows (wgrad): output zeros
+  int32_t rows_valid;  // rows of the tile that belong to the expert
+  int64_t y_off;       // element offset of the tile's first output element
+  int32_t a_y, b_y;    // TMA row coordinates
+  int32_t a_x0, b_x0;  // TMA K coordinates (bytes) of the first stage
+  int64_t sfa0;        // byte offset of A's scales for the first stage
+  int64_t sfb0;        // byte offset of B's scales (first 128-row half) for the first stage
+  int32_t n0;          // first output column
+};
+
+template <GemmKind K>
+__device__ __forceinline__ int64_t total_tiles(const LaunchGemm &p, const SharedState &s) {
+  const int64_t nb = p.n / kBN;
+  if (K == GemmKind::kWgradMxfp8) return static_cast<int64_t>(p.num_experts) * (p.m / kBM) * nb;
+  return static_cast<int64_t>(s.groups.tiles[p.num_experts]) * nb;
+}
+
+template <GemmKind K>
+__device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const SharedState &s, int64_t t) {
+  using C = Cfg<K>;
+  Tile tl;
+  const int64_t nb_count = p.n / kBN;
+  if (K == GemmKind::kWgradMxfp8) {
+    const int64_t mb_count = p.m / kBM;
+    const int64_t per = mb_count * nb_count;
+    const int rank = static_cast<int>(t / per);
+    const int64_t rem = t % per;
+    const int64_t mb = rem / nb_count;
+    const int64_t nb = rem % nb_count;
+    const int e = s.groups.tiles[rank];
+    const int32_t p0 = s.groups.off[e];
+    tl.e = e;
+    tl.num_k = (s.groups.off[e + 1] - p0) / 128;
+    tl.rows_valid = kBM;
+    tl.n0 = static_cast<int32_t>(nb * kBN);
+    tl.y_off = (static_cast<int64_t>(e) * p.m + mb * kBM) * p.n + nb * kBN;
+    tl.a_y = static_cast<int32_t>(mb * kBM);
+    tl.b_y = static_cast<int32_t>(nb * kBN);
+    tl.a_x0 = p0;
+    tl.b_x0 = p0;
+    tl.sfa0 = mb * p.sfa_stride + static_cast<int64_t>(p0 / 128) * 512;
+    tl.sfb0 = (2 * nb) * p.sfb_stride + static_cast<int64_t>(p0 / 128) * 512;
+  } else {
+    const int64_t g = t / nb_count;
+    const int64_t nb = t % nb_count;
+    const int e = find_group(s.groups.tiles, p.num_experts, g);
+    const int64_t mt = g - s.groups.tiles[e];
+    const int64_t r0 = s.groups.off[e] + mt * kBM;
+    const int64_t n_e = s.groups.off[e + 1] - s.groups.off[e];
+    tl.e = e;
+    tl.num_k = static_cast<int32_t>(p.k / C::kKPerStage);
+    tl.rows_valid = static_cast<int32_t>(n_e - mt * kBM < kBM ? n_e - mt * kBM : kBM);
+    tl.n0 = static_cast<int32_t>(nb * kBN);
+    tl.y_off = r0 * p.n + nb * kBN;
+    tl.a_y = static_cast<int32_t>(r0);
+    tl.a_x0 = 0;
+    tl.sfa0 = g * p.sfa_stride;  // padded row block of this tile = tiles[e] + mt = g
+    if (K == GemmKind::kFwdNvfp4) {
+      const int64_t brow = static_cast<int64_t>(e) * p.n + nb * kBN;
+      tl.b_y = static_cast<int32_t>(brow);
+      tl.b_x0 = 0;
+      tl.sfb0 = (brow / 128) * p.sfb_stride;
+    } else {
+      tl.b_y = static_cast<int32_t>(nb * kBN);
+      tl.b_x0 = static_cast<int32_t>(static_cast<int64_t>(e) * p.k);
+      tl.sfb0 = (2 * nb) * p.sfb_stride + (static_cast<int64_t>(e) * p.k / 128) * 512;
+    }
+  }
+  return tl;
+}
+
+// Build the tile tables; returns false (in every thread) for malformed offsets.
+template <GemmKind K>
+__device__ bool prepare(const LaunchGemm &p, SharedState &s) {
+  if (K != GemmKind::kWgradMxfp8) return load_groups(s.groups, p.offsets, p.num_experts, p.m, &s.ok_flag);
+  // wgrad: padded offsets, multiples of 128, rising from 0 within both operands
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    int32_t prev = 0;
+    for (int e = 0; e <= p.num_experts; ++e) {
+      const int32_t v = __ldg(p.offsets + e);
+      if ((e == 0 && v != 0) || v < prev || (v & 127) != 0) ok = false;
+      s.groups.off[e] = v;
+      prev = v;
+    }
+    if (prev > p.lda || prev > p.ldb) ok = false;
+    s.ok_flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s.ok_flag) return false;
+  for (int e = threadIdx.x; e < p.num_experts; e += blockDim.x) {
+    const int32_t w = s.groups.off[e + 1] - s.groups.off[e];
+    int rank = 0;
+    for (int f = 0; f < p.num_experts; ++f) {
+      const int32_t wf = s.groups.off[f + 1] - s.groups.off[f];
+      rank += (wf > w) || (wf == w && f < e);
+    }
+    s.groups.tiles[rank] = e;
+  }
+  __syncthreads();
+  return true;
+}
+
+template <GemmKind K>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ LaunchGemm p) {
+  using C = Cfg<K>;
+  __shared__ SharedState s;
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t *smem_a = smem;
+  uint8_t *smem_b = smem_a + kStages * kABytes;
+  uint8_t *smem_sfa = smem_b + kStages * kBBytes;
+  uint8_t *smem_sfb = smem_sfa + kStages * C::kSfaBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (!prepare<K>(p, s)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(p.status, kDevBadOffsets);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    mbar_init(&s.acc_full, 1);
+    mbar_init(&s.acc_empty, 4 * 32);
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_shared();
+    prefetch_tensormap(&p.map_a);
+    prefetch_tensormap(&p.map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int *abort_flag = &s.abort_flag;
+  const int64_t total = total_tiles<K>(p, s);
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- producer
+    uint32_t stage = 0, phase = 0;
+    bool issued_any[kStages] = {};
+    uint32_t issued_phase[kStages] = {};
+    bool stop = false;
+    for (int64_t t = blockIdx.x; t < total && !stop; t += gridDim.x) {
+      const Tile tl = tile_at<K>(p, s, t);
+      for (int ks = 0; ks < tl.num_k; ++ks) {
+        if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.status)) {
+          stop = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&s.full[stage], C::kStageTx);
+        tma_load_2d(smem_a + stage * kABytes, &p.map_a, &s.full[stage], tl.a_x0 + ks * kStageKBytes, tl.a_y);
+        tma_load_2d(smem_b + stage * kBBytes, &p.map_b, &s.full[stage], tl.b_x0 + ks * kStageKBytes, tl.b_y);
+        bulk_load(smem_sfa + stage * C::kSfaBytes, p.sfa + tl.sfa0 + static_cast<int64_t>(ks) * C::kSfaBytes,
+                  C::kSfaBytes, &s.full[stage]);
+        const uint8_t *sfb_src = p.sfb + tl.sfb0 + static_cast<int64_t>(ks) * (C::kSfbBytes / 2);
+        bulk_load(smem_sfb + stage * C::kSfbBytes, sfb_src, C::kSfbBytes / 2, &s.full[stage]);
+        bulk_load(smem_sfb + stage * C::kSfbBytes + C::kSfbBytes / 2, sfb_src + p.sfb_stride, C::kSfbBytes / 2,
+                  &s.full[stage]);
+        issued_any[stage] = true;
+        issued_phase[stage] = phase;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (stop) {  // let copies in flight land before the CTA exits
+      for (int i = 0; i < kStages; ++i)
+        if (issued_any[i]) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&s.full[i], issued_phase[i]) && globaltimer() - t0 < kWaitLimitNs / 4) {
+          }
+        }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    bool stop = false;
+    const uint32_t sf_base = tmem + kAccCols;
+    for (int64_t t = blockIdx.x; t < total && !stop; t += gridDim.x) {
+      const Tile tl = tile_at<K>(p, s, t);
+      if (tl.num_k == 0) continue;
+      if (!mbar_wait(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      for (int ks = 0; ks < tl.num_k; ++ks) {
+        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa_t = sf_base + (ks & 1) * C::kSfCols;
+        const uint32_t sfb_t = sfa_t + C::kSfaCols;
+        const uint32_t a_s = smem_u32(smem_a + stage * kABytes);
+        const uint32_t b_s = smem_u32(smem_b + stage * kBBytes);
+        const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
+        const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
+#pragma unroll
+        for (int i = 0; i < C::kAtoms; ++i) {
+          tc_copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
+          tc_copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
+          tc_copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = desc_sw128_kmajor(a_s + kk * 32);
+          const uint64_t bd = desc_sw128_kmajor(b_s + kk * 32);
+          const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+          if (C::kFp4)
+            mma_nvf4(tmem, ad, bd, idesc_nvf4(kBN), sfa_t + 4 * kk, sfb_t + 8 * kk, acc);
+          else
+            mma_mxf8(tmem, ad, bd, idesc_mxf8(kBN, kk), sfa_t, sfb_t, acc);
+        }
+        tc_commit(&s.empty[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (stop) break;
+      tc_commit(&s.acc_full);
+      acc_phase ^= 1;
+    }
+    // every tensor-core operation of this CTA has finished before memory is released
+    tc_commit(&s.drain);
+    {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
+      }
+    }
+  } else if (warp >= 2) {
+    // --------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    const int r = q * 32 + lane;
+    uint32_t acc_phase = 0;
+    __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = tile_at<K>(p, s, t);
+      const bool valid = r < tl.rows_valid;
+      __nv_bfloat16 *yrow = y + tl.y_off + static_cast<int64_t>(r) * p.n;
+      if (tl.num_k == 0) {
+        if (valid)
+          for (int c = 0; c < kBN; c += 8) *reinterpret_cast<uint4 *>(yrow + c) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      if (!mbar_wait(&s.acc_full, acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      float sa = 1.0f;
+      const float *sb_row = nullptr;
+      if (K == GemmKind::kFwdNvfp4) {
+        if (valid) sa = __ldg(p.a_scale + tl.a_y + r);
+        sb_row = p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0;
+      }
+#pragma unroll 1
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+        tmem_wait_ld();
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float lo = __uint_as_float(v[2 * j]);
+          float hi = __uint_as_float(v[2 * j + 1]);
+          if (K == GemmKind::kFwdNvfp4) {
+            lo = __fmul_rn(__fmul_rn(lo, sa), __ldg(sb_row + c + 2 * j));
+            hi = __fmul_rn(__fmul_rn(hi, sa), __ldg(sb_row + c + 2 * j + 1));
+          }
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+          packed[j] = *reinterpret_cast<const uint32_t *>(&b2);
+        }
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(yrow + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty);
+      acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <GemmKind K>
+static cudaError_t launch_kind(const LaunchGemm &a) {
+  using C = Cfg<K>;
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  int64_t bound;
+  if (K == GemmKind::kWgradMxfp8)
+    bound = static_cast<int64_t>(a.num_experts) * (a.m / kBM) * (a.n / kBN);
+  else
+    bound = (a.m / kBM + a.num_experts) * (a.n / kBN);
+  int grid = a.num_sms;
+  if (bound < grid) grid = static_cast<int>(bound > 0 ? bound : 1);
+  grouped_gemm_kernel<K><<<grid, kThreads, C::kSmemBytes, a.stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const LaunchGemm &a) {
+  switch (a.kind) {
+    case GemmKind::kFwdNvfp4:
+      return launch_kind<GemmKind::kFwdNvfp4>(a);
+    case GemmKind::kDgradMxfp8:
+      return launch_kind<GemmKind::kDgradMxfp8>(a);
+    case GemmKind::kWgradMxfp8:
+      return launch_kind<GemmKind::kWgradMxfp8>(a);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fme

@@ -1,0 +1,227 @@
+// quant_mxfp8.cu -- MXFP8 quantizers of the backward (row-wise and column-wise).
+//
+// "Composer 2 Technical Report" (papercache.org summary), section 6.1, paragraph
+// on MXFP8 in the MoE backward: standard MXFP8, FP8 E4M3 values with an FP8
+// E8M0 scale per block of 32.  Scale rule of the OCP MX v1.0 format the report
+// cites: X = 2^(floor(log2 amax) - 8), code = clamp(floor(log2 amax) + 119, 0, 254).
+// For a bf16 amax that is max(0, exponent field - 8), read straight from the
+// bits; x / X is then one exact fp32 multiply by 2^(127 - code), so the fast
+// division the pages allow for MXFP8 and a correctly rounded one give the same
+// codes.  Elements convert with cvt.rn.satfinite (nearest even, saturating at 448).
+#include "fme_device.cuh"
+#include "fme_launch.h"
+
+namespace fme {
+
+__device__ __forceinline__ uint32_t mx_code_from_bf16_amax(uint32_t amax_bits) {
+  const int e = static_cast<int>((amax_bits >> 7) & 0xFF);
+  return static_cast<uint32_t>(e > 8 ? e - 8 : 0);
+}
+
+// 2^(127 - code) as an fp32 (code in [0, 246] for bf16 inputs: always normal).
+__device__ __forceinline__ float mx_inv_scale(uint32_t code) { return __uint_as_float((254u - code) << 23); }
+
+// Two E4M3 codes: `lo` in bits 0..7, `hi` in bits 8..15.
+__device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four bf16 (two words) times s -> four E4M3 codes in one word.
+__device__ __forceinline__ uint32_t quad_codes(uint32_t w0, uint32_t w1, float s) {
+  const uint32_t p0 = e4m3_pair(__fmul_rn(bf16_bits_to_float(w0 & 0xFFFFu), s),
+                                __fmul_rn(bf16_bits_to_float(w0 >> 16), s));
+  const uint32_t p1 = e4m3_pair(__fmul_rn(bf16_bits_to_float(w1 & 0xFFFFu), s),
+                                __fmul_rn(bf16_bits_to_float(w1 >> 16), s));
+  return p0 | (p1 << 16);
+}
+
+// ---------------------------------------------------------------- row-wise --
+// One warp per row; lane l handles 8 consecutive values of every 256-wide
+// chunk, four lanes form a 32-block (two shuffles for its amax).  Codes leave as
+// 8-byte stores (256 contiguous bytes per warp); lanes 0 and 16 each store four
+// consecutive scales as one word of the tiled layout.
+constexpr int kRowUnroll = 4;
+
+__global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
+                                                         const int32_t *__restrict__ offsets, int num_groups,
+                                                         uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
+                                                         int32_t *status) {
+  __shared__ GroupTable groups;
+  __shared__ int ok_flag;
+  if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(status, kDevBadOffsets);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  const int64_t c4 = ((cols / 32) + 3) & ~3;
+
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); row < rows;
+       row += static_cast<int64_t>(gridDim.x) * warps) {
+    const int g = find_group(groups.off, num_groups, row);
+    const int64_t prow = 128 * static_cast<int64_t>(groups.tiles[g]) + (row - groups.off[g]);
+    const uint16_t *xr = x + row * cols;
+    uint8_t *cr = codes + row * cols;
+    for (int base = 0; base < cols; base += 256 * kRowUnroll) {
+      uint4 v[kRowUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int col = base + u * 256 + lane * 8;
+        v[u] = (col < cols) ? __ldcs(reinterpret_cast<const uint4 *>(xr + col)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int col = base + u * 256 + lane * 8;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t bmax = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          bmax = max(bmax, w[i] & 0x7FFFu);
+          bmax = max(bmax, (w[i] >> 16) & 0x7FFFu);
+        }
+        bmax = max(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
+        bmax = max(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 2));
+        const uint32_t code = mx_code_from_bf16_amax(bmax);
+        const float s = mx_inv_scale(code);
+        uint2 out;
+        out.x = quad_codes(w[0], w[1], s);
+        out.y = quad_codes(w[2], w[3], s);
+        if (col < cols) *reinterpret_cast<uint2 *>(cr + col) = out;
+        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 4);
+        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 8);
+        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, code, 12);
+        if ((lane & 15) == 0 && col < cols) {
+          const int64_t cb = (base + u * 256) / 32 + lane / 4;
+          const uint32_t word = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+          *reinterpret_cast<uint32_t *>(sf + sf_offset(prow, cb, c4)) = word;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------- column-wise --
+// Tile = 128 padded positions (one 128-chunk of one group) x 128 columns.  The
+// CTA stages the 128 x 128 bf16 tile in shared memory (rows past the group's end
+// read as zeros), each thread quantizes two 32-blocks of one column, the codes
+// are staged transposed and leave as 128-byte rows, and the 128 x 4 scales of
+// the tile are exactly one 512-byte tile of the scale layout.
+constexpr int kColTilePad = 8;  // bf16 elements of padding per staged row
+constexpr int kColTileBytes = 128 * (128 + kColTilePad) * 2;
+constexpr int kColOutBytes = 128 * (128 + 16);
+constexpr int kColSmemBytes = kColTileBytes + kColOutBytes + 512;
+
+__global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
+                                                         const int32_t *__restrict__ offsets, int num_groups,
+                                                         uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
+                                                         int64_t ld, int32_t *__restrict__ padded_offsets,
+                                                         int32_t *status) {
+  __shared__ GroupTable groups;
+  __shared__ int ok_flag;
+  extern __shared__ __align__(16) uint8_t col_smem[];
+  auto tile = reinterpret_cast<uint16_t(*)[128 + kColTilePad]>(col_smem);
+  auto outq = reinterpret_cast<uint8_t(*)[128 + 16]>(col_smem + kColTileBytes);
+  uint8_t *sfs = col_smem + kColTileBytes + kColOutBytes;
+
+  if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(status, kDevBadOffsets);
+    return;
+  }
+  const int tid = threadIdx.x;
+  if (blockIdx.x == 0)
+    for (int g = tid; g <= num_groups; g += blockDim.x) padded_offsets[g] = 128 * groups.tiles[g];
+
+  const int64_t chunks = groups.tiles[num_groups];
+  if (chunks * 128 > ld) {  // cannot happen for ld = fme_colwise_ld(); guards the stores
+    if (blockIdx.x == 0 && tid == 0) report(status, kDevBadOffsets);
+    return;
+  }
+  const int cblocks = cols / 128;
+  const int64_t total = chunks * cblocks;
+
+  for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    const int64_t j = t / cblocks;
+    const int cb = static_cast<int>(t % cblocks);
+    const int g = find_group(groups.tiles, num_groups, j);
+    const int64_t local0 = 128 * (j - groups.tiles[g]);
+    const int64_t n_g = groups.off[g + 1] - groups.off[g];
+    const int valid = static_cast<int>(n_g - local0 < 128 ? n_g - local0 : 128);
+    const int64_t src0 = groups.off[g] + local0;
+
+    __syncthreads();  // the previous tile's shared buffers are free
+#pragma unroll
+    for (int pass = 0; pass < 8; ++pass) {
+      const int r = pass * 16 + (tid >> 4);
+      const int seg = tid & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < valid)
+        v = __ldcs(reinterpret_cast<const uint4 *>(x + (src0 + r) * cols + cb * 128 + seg * 8));
+      *reinterpret_cast<uint4 *>(&tile[r][seg * 8]) = v;
+    }
+    __syncthreads();
+
+    const int c = tid & 127;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int b = (tid >> 7) + 2 * h;
+      uint32_t vals[32];
+      uint32_t bmax = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        vals[i] = tile[32 * b + i][c];
+        bmax = max(bmax, vals[i] & 0x7FFFu);
+      }
+      const uint32_t code = mx_code_from_bf16_amax(bmax);
+      const float s = mx_inv_scale(code);
+      uint32_t words[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        words[q] = quad_codes(vals[4 * q] | (vals[4 * q + 1] << 16), vals[4 * q + 2] | (vals[4 * q + 3] << 16), s);
+      *reinterpret_cast<uint4 *>(&outq[c][32 * b]) = make_uint4(words[0], words[1], words[2], words[3]);
+      *reinterpret_cast<uint4 *>(&outq[c][32 * b + 16]) = make_uint4(words[4], words[5], words[6], words[7]);
+      sfs[(c & 31) * 16 + (c >> 5) * 4 + b] = static_cast<uint8_t>(code);
+    }
+    __syncthreads();
+
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+      const int ch = pass * 32 + (tid >> 3);
+      const int seg = tid & 7;
+      const uint4 v = *reinterpret_cast<const uint4 *>(&outq[ch][seg * 16]);
+      *reinterpret_cast<uint4 *>(codes_t + (static_cast<int64_t>(cb) * 128 + ch) * ld + j * 128 + seg * 16) = v;
+    }
+    if (tid < 32) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
+      *reinterpret_cast<uint4 *>(sf_t + (static_cast<int64_t>(cb) * (ld / 128) + j) * 512 + tid * 16) = v;
+    }
+  }
+}
+
+cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a) {
+  const int threads = 256;
+  const int64_t need = (a.rows + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
+  const int blocks = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+  mxfp8_rows_kernel<<<blocks, threads, 0, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows,
+                                                       static_cast<int>(a.cols), a.offsets, a.num_groups,
+                                                       a.codes, a.sf, a.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a) {
+  const int threads = 256;
+  const int64_t tiles = (a.ld / 128) * (a.cols / 128);
+  const int64_t cap = static_cast<int64_t>(a.num_sms) * 4;
+  const int blocks = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
+  cudaError_t err = cudaFuncSetAttribute(mxfp8_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kColSmemBytes);
+  if (err != cudaSuccess) return err;
+  mxfp8_cols_kernel<<<blocks, threads, kColSmemBytes, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows,
+                                                       static_cast<int>(a.cols), a.offsets, a.num_groups,
+                                                       a.codes, a.sf, a.ld, a.padded_offsets, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace fme

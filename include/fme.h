@@ -1,0 +1,228 @@
+/*
+ * fme.h -- C ABI of the GB300 low-precision MoE expert path (libfme.so).
+ *
+ * Five calls, named after the operations of the MoE expert layer:
+ *   quantize_nvfp4_pertoken   NVFP4 variant of the forward: E2M1 codes, one E4M3
+ *                             scale per 16 values along K, one FP32 scale per token.
+ *   quantize_mxfp8            standard MXFP8 of the backward: E4M3 codes, one E8M0
+ *                             scale per 32 values, row-wise or column-wise.
+ *   grouped_gemm_fwd_nvfp4    Y_e = X_e W_e^T per expert, per-token scales applied
+ *                             in the epilogue, bf16 out.
+ *   grouped_gemm_dgrad_mxfp8  dX_e = dY_e W_e per expert, bf16 out.
+ *   grouped_gemm_wgrad_mxfp8  dW_e = dY_e^T H_e per expert, bf16 out.
+ *
+ * Source passages ("Composer 2 Technical Report", papercache.org summary,
+ * section 6.1): the NVFP4-variant paragraph (E2M1, E4M3 per block of 16, FP32
+ * per token, scale applied at the cost of quantize and GEMM-epilogue latency),
+ * the MXFP8-backward paragraph (E4M3 values, E8M0 scale per 32), the
+ * hardware-math paragraph (IEEE-compliant division when quantizing NVFP4), and
+ * the block-scaled tensor-core GEMM sentence (dequantization inside the
+ * systolic-array multiply).  "Scaling and Optimizing Frontier Model Training",
+ * "MXFP8 expert kernels": native block-scaled grouped GEMMs for expert shapes
+ * (32 experts per rank, hidden 7168, intermediate 2048).
+ *
+ * Conventions for every call
+ *   - Pointers are device pointers, allocated and owned by the caller.  The
+ *     library allocates nothing, frees nothing and never synchronises a stream
+ *     (except fme_read_device_status, which says so).
+ *   - Every call enqueues its work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns at once.
+ *   - Arguments are checked on the host before anything is launched; a failed
+ *     check returns its status and launches nothing.
+ *   - bf16 tensors are row-major with the last dimension contiguous.  Every
+ *     pointer must be 16-byte aligned.
+ *   - Inputs must be finite; NaN or Inf inputs are outside the contract.
+ *   - Errors the kernels detect (malformed offsets, a bounded wait that ran out)
+ *     are OR-ed as FME_DEV_* bits into `dev_status`, a caller-owned device int32
+ *     that the caller zeroes; dev_status may be NULL to ignore them.  A kernel
+ *     that detects an error writes nothing more and returns.
+ *   - Calls are thread-safe; the library keeps no per-call state.
+ *
+ * Grouped rows (experts)
+ *   `offsets` is a device int32 array of num_groups + 1 non-decreasing prefix
+ *   sums, offsets[0] = 0 and offsets[num_groups] = rows: group g owns rows
+ *   [offsets[g], offsets[g+1]).  NULL means one group holding every row.
+ *
+ * Scale-factor layout (this library's contract; the pages give none)
+ *   A scale matrix with logical shape [R x C] (R rows of the quantized tensor,
+ *   C = cols / block) is stored padded: each group's rows start at a multiple
+ *   of 128 (padded row pr = 128 * sum_{g'<g} ceil(n_g'/128) + local row), and
+ *   C is rounded up to C4 = 4 * ceil(C / 4).  Element (pr, c) lives at byte
+ *      ((pr / 128) * (C4 / 4) + c / 4) * 512 + (pr % 32) * 16 + ((pr % 128) / 32) * 4 + c % 4
+ *   i.e. 512-byte tiles of 128 rows x 4 scales, the order in which the tensor
+ *   core's block-scale operand is copied into tensor memory.  Bytes of padding
+ *   rows and padding columns are left unwritten.  fme_sf_bytes() gives the
+ *   buffer size.
+ */
+#ifndef FME_H
+#define FME_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t fme_status;
+
+#define FME_OK 0
+#define FME_ERR_INVALID_ARGUMENT 1   /* null pointer, negative size, bad axis  */
+#define FME_ERR_MISALIGNED 2         /* a pointer or a leading dimension not 16-byte aligned */
+#define FME_ERR_UNSUPPORTED_SHAPE 3  /* a size outside the supported tiling (see each call) */
+#define FME_ERR_UNSUPPORTED_DEVICE 4 /* the current device is not compute capability 10.3 */
+#define FME_ERR_CUDA 5               /* a CUDA runtime or driver call failed; see fme_last_cuda_error() */
+#define FME_ERR_DEVICE_TIMEOUT 6     /* reported by fme_read_device_status() */
+#define FME_ERR_DEVICE_BAD_OFFSETS 7 /* reported by fme_read_device_status() */
+
+/* Bits a kernel ORs into *dev_status. */
+#define FME_DEV_TIMEOUT 0x1     /* a bounded wait inside a GEMM ran out; the kernel gave up */
+#define FME_DEV_BAD_OFFSETS 0x2 /* offsets not rising from 0 to rows (or padded offsets invalid) */
+
+#define FME_ROWWISE 0
+#define FME_COLWISE 1
+
+#define FME_MAX_GROUPS 1024
+
+/*
+ * quantize_nvfp4_pertoken -- the NVFP4 variant of the MoE forward.
+ *
+ * Per row t of x [rows x k] (bf16): amax_t = max |x|, S_t = amax_t / 2688 (fp32,
+ * IEEE correctly rounded division), per block b of 16: sb = E4M3(amax_b /
+ * fl32(6 S_t)) (IEEE division), e = fl32(dec(sb) S_t), q = E2M1(x / e) (IEEE
+ * division), round to nearest even, saturating.  A row with amax 0 or a block
+ * whose scale code is 0 gets codes 0.  Rows are independent: a token's outputs
+ * do not depend on any other row.
+ *
+ *   x          device bf16 [rows x k]
+ *   rows, k    rows >= 0; k a multiple of 64, 64 <= k <= 8192
+ *   offsets    device int32 [num_groups + 1] or NULL (see "Grouped rows");
+ *              the groups only decide the padding of the scale layout
+ *   num_groups 1 .. FME_MAX_GROUPS
+ *   codes      device uint8 [rows x k/2]; element 2j in the low nibble of byte j
+ *   sf         device uint8, fme_sf_bytes(rows, k, 16, num_groups) bytes, E4M3
+ *   row_scale  device float [rows], S_t
+ *   dev_status device int32 or NULL
+ *   stream     cudaStream_t
+ */
+fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const int32_t *offsets,
+                                   int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale,
+                                   int32_t *dev_status, void *stream);
+
+/*
+ * quantize_mxfp8 -- standard MXFP8 (OCP MX v1.0 rule) of the MoE backward.
+ *
+ * Per block of 32: X = 2^(floor(log2 amax) - 8) stored as the E8M0 code
+ * clamp(floor(log2 amax) + 119, 0, 254) (code 0 for an all-zero block);
+ * q = E4M3(x / X), round to nearest even, saturating at 448.  X is a power of
+ * two, so x / X is exact and the fast division the pages allow for MXFP8 gives
+ * the same codes.
+ *
+ * axis = FME_ROWWISE: blocks run along each row of x [rows x cols].
+ *   cols a multiple of 32, 32 <= cols <= 65536.
+ *   codes  device uint8 [rows x cols] (E4M3)
+ *   sf     device uint8, fme_sf_bytes(rows, cols, 32, num_groups) bytes (E8M0)
+ *   padded_offsets must be NULL.
+ *
+ * axis = FME_COLWISE: blocks run down the columns, over the rows of one group at
+ * a time.  Group g's rows are placed at padded positions starting at
+ * P_g = 128 * sum_{g'<g} ceil(n_g'/128) and zero-filled up to the next multiple
+ * of 128; blocks of 32 start at P_g.  The output is transposed so that the
+ * position axis is contiguous:
+ *   cols a multiple of 128.
+ *   codes  device uint8 [cols x ld], ld = fme_colwise_ld(rows, num_groups);
+ *          positions P_G .. ld-1 are left unwritten
+ *   sf     device uint8, fme_sf_bytes(cols, ld, 32, 1) bytes: the scale matrix
+ *          [cols x ld/32] in the tiled layout (rows = columns of x)
+ *   padded_offsets device int32 [num_groups + 1]: P_0 .. P_G
+ */
+fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axis, const int32_t *offsets,
+                          int32_t num_groups, uint8_t *codes, uint8_t *sf, int32_t *padded_offsets,
+                          int32_t *dev_status, void *stream);
+
+/*
+ * grouped_gemm_fwd_nvfp4 -- Y[t, :] = S_x[t] * S_w[e, :] * sum_k A'[t,k] B'_e[:,k]
+ * for every row t of expert e, where A', B' are the E2M1 codes times their E4M3
+ * block scales, multiplied on the tensor cores with fp32 accumulation; the
+ * epilogue applies (acc * S_x[t]) * S_w[e, n] in fp32 and rounds to bf16.
+ * No split over K: a row's output does not depend on any other row.
+ *
+ *   a_codes, a_sf, a_scale  quantize_nvfp4_pertoken of X [m x k] with these offsets
+ *   b_codes, b_sf, b_scale  quantize_nvfp4_pertoken of W [num_experts * n x k]
+ *                           (expert e's rows are e*n .. e*n+n-1), one group
+ *   offsets        device int32 [num_experts + 1], rows of X per expert
+ *   m, n, k        n a multiple of 256; k a multiple of 256
+ *   y              device bf16 [m x n]
+ */
+fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
+                                  const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
+                                  const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n,
+                                  int64_t k, void *y, int32_t *dev_status, void *stream);
+
+/*
+ * grouped_gemm_dgrad_mxfp8 -- Y[t, :] = sum_j A'[t, j] B'[:, e*k + j] for every
+ * row t of expert e (A', B' = E4M3 codes times E8M0 block scales), fp32
+ * accumulation, bf16 out.  This is the data gradient dX_e = dY_e W_e when A is
+ * the row-wise MXFP8 of dY [m x k] and B the column-wise MXFP8 of the stacked
+ * weights W [num_experts * k x n] (one group), whose codes are [n x ldb].
+ *
+ *   a_codes, a_sf  quantize_mxfp8(ROWWISE) of A [m x k] with these offsets
+ *   b_codes, b_sf  codes [n x ldb] and their scales (tiled, rows = n); expert e
+ *                  uses columns e*k .. e*k+k-1, so ldb >= num_experts * k
+ *   offsets        device int32 [num_experts + 1]
+ *   m, n, k        n a multiple of 256; k a multiple of 128; ldb a multiple of 128
+ *   y              device bf16 [m x n]
+ */
+fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, const uint8_t *b_codes,
+                                    const uint8_t *b_sf, int64_t ldb, const int32_t *offsets,
+                                    int32_t num_experts, int64_t m, int64_t n, int64_t k, void *y,
+                                    int32_t *dev_status, void *stream);
+
+/*
+ * grouped_gemm_wgrad_mxfp8 -- Y_e[i, j] = sum_p A'[i, p] B'[j, p] over the padded
+ * positions p of expert e, [P_e, P_e+1), fp32 accumulation over all of them (no
+ * split), bf16 out.  With A = column-wise MXFP8 of dY and B = column-wise MXFP8
+ * of H (same offsets) this is the weight gradient dW_e = dY_e^T H_e.  An
+ * expert with no rows gets an all-zero Y_e.
+ *
+ *   a_codes, a_sf, lda  quantize_mxfp8(COLWISE) of dY [rows x m]: codes [m x lda]
+ *   b_codes, b_sf, ldb  quantize_mxfp8(COLWISE) of H [rows x n]:  codes [n x ldb]
+ *   padded_offsets  device int32 [num_experts + 1] written by those calls
+ *   m, n            m a multiple of 128, n a multiple of 256
+ *   y               device bf16 [num_experts x m x n]
+ */
+fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda,
+                                    const uint8_t *b_codes, const uint8_t *b_sf, int64_t ldb,
+                                    const int32_t *padded_offsets, int32_t num_experts, int64_t m,
+                                    int64_t n, void *y, int32_t *dev_status, void *stream);
+
+/* Rows of the padded scale layout for `rows` rows in `num_groups` groups: an
+ * upper bound of 128 * sum ceil(n_g / 128) that needs no offsets. */
+int64_t fme_sf_padded_rows(int64_t rows, int32_t num_groups);
+
+/* Bytes of a tiled scale buffer for a [rows x cols] tensor quantized in blocks
+ * of `block` (16 or 32) along cols, in `num_groups` groups. */
+int64_t fme_sf_bytes(int64_t rows, int64_t cols, int32_t block, int32_t num_groups);
+
+/* Leading dimension (positions per column) of the column-wise MXFP8 outputs. */
+int64_t fme_colwise_ld(int64_t rows, int32_t num_groups);
+
+/* Synchronises `stream`, copies *dev_status to the host and maps it to a status:
+ * FME_OK, FME_ERR_DEVICE_BAD_OFFSETS or FME_ERR_DEVICE_TIMEOUT.  `raw` (may be
+ * NULL) receives the raw bits. */
+fme_status fme_read_device_status(const int32_t *dev_status, void *stream, int32_t *raw);
+
+/* Static text for a status code. */
+const char *fme_error_string(fme_status status);
+
+/* Text of the last CUDA error seen by a call on this thread ("" if none). */
+const char *fme_last_cuda_error(void);
+
+/* Library version string. */
+const char *fme_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FME_H */

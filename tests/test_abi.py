@@ -1,0 +1,97 @@
+"""The C ABI without a GPU: libfme.so loads, exports every function include/fme.h
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_moe_expert_gb300 as fme
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fme.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fme.ensure_built()
+    return fme.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^(?:fme_status|int64_t|const char \*)\s*(\w+)\(", text, flags=re.M)
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for call in ("quantize_nvfp4_pertoken", "quantize_mxfp8", "grouped_gemm_fwd_nvfp4",
+                 "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8"):
+        assert call in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in fme.SYMBOLS, f"binding does not declare {name}"
+
+
+def test_helpers_closed_forms(lib):
+    # padded rows: floor((rows + 127 G) / 128) * 128
+    assert fme.sf_padded_rows(0, 1) == 0
+    assert fme.sf_padded_rows(1, 1) == 128
+    assert fme.sf_padded_rows(128, 1) == 128
+    assert fme.sf_padded_rows(129, 1) == 256
+    assert fme.sf_padded_rows(16384, 32) == 20352
+    assert fme.sf_bytes(16384, 7168, 16, 32) == 20352 * 448
+    assert fme.sf_bytes(100, 96, 32, 1) == 128 * 4          # 3 scales per row, rounded up to 4
+    assert fme.colwise_ld(65536, 32) == ((65536 + 127 * 32) // 128) * 128
+    assert lib.fme_version().startswith(b"fme")
+    for code in range(8):
+        assert lib.fme_error_string(code)
+
+
+def _stream():
+    return ctypes.c_void_p(0)
+
+
+def test_host_argument_checks(lib):
+    P = ctypes.c_void_p
+    good = P(0x100000)      # never dereferenced: every call below fails before launching
+    odd = P(0x100001)
+    q = lib.quantize_nvfp4_pertoken
+    assert q(good, -1, 256, None, 1, good, good, good, None, _stream()) == 1
+    assert q(good, 10, 63, None, 1, good, good, good, None, _stream()) == 3
+    assert q(good, 10, 8256, None, 1, good, good, good, None, _stream()) == 3
+    assert q(good, 10, 256, None, 0, good, good, good, None, _stream()) == 1
+    assert q(good, 10, 256, None, 2, good, good, good, None, _stream()) == 1
+    assert q(None, 10, 256, None, 1, good, good, good, None, _stream()) == 1
+    assert q(odd, 10, 256, None, 1, good, good, good, None, _stream()) == 2
+    assert q(good, 0, 256, None, 1, None, None, None, None, _stream()) == 0     # nothing to do
+    m = lib.quantize_mxfp8
+    assert m(good, 10, 256, 2, None, 1, good, good, None, None, _stream()) == 1
+    assert m(good, 10, 256, 0, None, 1, good, good, good, None, _stream()) == 1  # row-wise takes no padded offsets
+    assert m(good, 10, 48, 0, None, 1, good, good, None, None, _stream()) == 3
+    assert m(good, 10, 96, 1, None, 1, good, good, good, None, _stream()) == 3   # column-wise needs cols % 128
+    assert m(good, 10, 256, 1, None, 1, good, good, None, None, _stream()) == 1
+    assert m(good, 10, 256, 1, None, 1, good, odd, good, None, _stream()) == 2
+    f = lib.grouped_gemm_fwd_nvfp4
+    assert f(good, good, good, good, good, good, good, 4, 100, 100, 256, good, None, _stream()) == 3
+    assert f(good, good, good, good, good, good, good, 4, 100, 256, 100, good, None, _stream()) == 3
+    assert f(good, good, good, good, good, good, None, 4, 100, 256, 256, good, None, _stream()) == 1
+    assert f(good, good, good, good, good, good, good, 0, 100, 256, 256, good, None, _stream()) == 1
+    assert f(good, good, good, good, good, good, good, 4, 100, 256, 256, odd, None, _stream()) == 2
+    d = lib.grouped_gemm_dgrad_mxfp8
+    assert d(good, good, good, good, 1024, good, 4, 100, 256, 512, good, None, _stream()) == 1  # ldb < E k
+    assert d(good, good, good, good, 2048, good, 4, 100, 256, 96, good, None, _stream()) == 3
+    w = lib.grouped_gemm_wgrad_mxfp8
+    assert w(good, good, 128, good, good, 128, good, 4, 100, 256, good, None, _stream()) == 3
+    assert w(good, good, 128, good, good, 128, good, 4, 128, 128, good, None, _stream()) == 3
+    assert w(good, good, 128, good, good, 128, None, 4, 128, 256, good, None, _stream()) == 1
+    assert lib.fme_read_device_status(None, _stream(), None) == 1
+
+
+def test_binding_refuses_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(fme, "LIBRARY", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(fme, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        fme.lib()

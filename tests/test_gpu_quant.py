@@ -1,0 +1,247 @@
+"""Quantizers on the GPU against the CPU oracle: codes and scales bit-exact.
+
+Workloads: the tiny one-expert case, the 16384 x 7168 heterogeneous quantizer
+batch, and edge shapes (ragged groups, empty groups, zero rows and blocks,
+subnormal and tiny inputs, saturating outliers).  Invariants from "Composer 2
+Technical Report" section 6.1 (per-token scales: no dependence on the rest of
+the batch, no leakage from later tokens) are checked on the GPU bit for bit.
+"""
+import numpy as np
+import pytest
+
+from fp8_moe_expert_gb300 import synth
+from tests.fmetest import bf16_tensor, to_np, unswizzle
+from tests.golden import read_cases
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev_offsets(offsets):
+    import torch
+
+    return None if offsets is None else torch.from_numpy(np.asarray(offsets, np.int32)).cuda()
+
+
+def _status():
+    import torch
+
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def run_nvfp4(fme, x_bits, offsets=None):
+    import torch
+
+    x = bf16_tensor(x_bits)
+    st = _status()
+    codes, sf, scale = fme.quantize_nvfp4_pertoken(x, _dev_offsets(offsets), status=st)
+    code, raw = fme.read_device_status(st)
+    assert code == 0, raw
+    rows, k = x_bits.shape
+    return to_np(codes), unswizzle(to_np(sf), rows, k // 16, offsets), to_np(scale)
+
+
+def check_nvfp4(fme, orc, x_bits, offsets=None):
+    codes, sf, scale = run_nvfp4(fme, x_bits, offsets)
+    oc, osf, oscale = orc.quant_nvfp4(x_bits)
+    assert np.array_equal(scale.view(np.uint32), oscale.view(np.uint32)), "per-token scales differ"
+    assert np.array_equal(sf, osf), f"block scales differ at {np.argwhere(sf != osf)[:5].tolist()}"
+    bad = np.argwhere(codes != oc)
+    assert bad.size == 0, f"{len(bad)} code bytes differ, first {bad[:5].tolist()}"
+    return codes, sf, scale
+
+
+def run_mx_rows(fme, x_bits, offsets=None):
+    x = bf16_tensor(x_bits)
+    st = _status()
+    codes, sf = fme.quantize_mxfp8(x, fme.ROWWISE, _dev_offsets(offsets), status=st)
+    assert fme.read_device_status(st)[0] == 0
+    rows, cols = x_bits.shape
+    return to_np(codes), unswizzle(to_np(sf), rows, cols // 32, offsets)
+
+
+def run_mx_cols(fme, x_bits, offsets):
+    x = bf16_tensor(x_bits)
+    st = _status()
+    codes, sf, poff, ld = fme.quantize_mxfp8(x, fme.COLWISE, _dev_offsets(offsets), status=st)
+    assert fme.read_device_status(st)[0] == 0
+    cols = x_bits.shape[1]
+    return to_np(codes), unswizzle(to_np(sf), cols, ld // 32), to_np(poff), ld
+
+
+def check_mx_rows(fme, orc, x_bits, offsets=None):
+    codes, sf = run_mx_rows(fme, x_bits, offsets)
+    oc, osf = orc.quant_mxfp8_rows(x_bits)
+    assert np.array_equal(sf, osf), f"scales differ at {np.argwhere(sf != osf)[:5].tolist()}"
+    bad = np.argwhere(codes != oc)
+    assert bad.size == 0, f"{len(bad)} codes differ, first {bad[:5].tolist()}"
+
+
+def check_mx_cols(fme, orc, x_bits, offsets):
+    codes, sf, poff, ld = run_mx_cols(fme, x_bits, offsets)
+    oc, osf, opoff = orc.quant_mxfp8_cols(x_bits, offsets, ld=ld)
+    assert np.array_equal(poff, opoff)
+    p = int(opoff[-1])
+    assert np.array_equal(sf[:, : p // 32], osf[:, : p // 32]), "column-wise scales differ"
+    bad = np.argwhere(codes[:, :p] != oc[:, :p])
+    assert bad.size == 0, f"{len(bad)} codes differ, first {bad[:5].tolist()}"
+
+
+# ------------------------------------------------------------------- NVFP4 --
+def test_nvfp4_worked_examples(fme, orc):
+    """The hand-worked rows of tests/golden, each embedded in a 64-wide row of zeros."""
+    cases = read_cases("nvfp4_worked.txt")
+    rows = []
+    for case in cases.values():
+        r = np.zeros(64, np.float32)
+        r[:16] = [float(v) for v in case["x"].split()]
+        rows.append(r)
+    x_bits = synth.bf16_bits(np.stack(rows))
+    codes, sf, scale = run_nvfp4(fme, x_bits)
+    for i, case in enumerate(cases.values()):
+        assert int(scale[i:i + 1].view(np.uint32)[0]) == int(case["S_bits"], 16)
+        assert int(sf[i, 0]) == int(case["sf"], 16)
+        assert [int(c) for c in codes[i, :8]] == [int(c, 16) for c in case["packed"].split()]
+        assert np.all(codes[i, 8:] == 0) and np.all(sf[i, 1:] == 0)
+
+
+def test_nvfp4_tiny(fme, orc):
+    x, w = synth.tiny(0)
+    check_nvfp4(fme, orc, x)
+    check_nvfp4(fme, orc, w)
+
+
+def test_nvfp4_quantizer_batch(fme, orc):
+    x, _, _ = synth.quantizer_batch()
+    check_nvfp4(fme, orc, x)
+
+
+@pytest.mark.parametrize("rows", [1, 31, 32, 33, 127, 128, 129])
+@pytest.mark.parametrize("k", [64, 192, 2048, 8192])
+def test_nvfp4_edge_shapes(fme, orc, rows, k):
+    rng = np.random.default_rng(rows * 1000 + k)
+    f = rng.standard_normal((rows, k), dtype=np.float32)
+    f[rng.random(f.shape) < 0.01] *= 500.0
+    if rows > 3:
+        f[1] = 0.0                                # zero row
+        f[2] *= np.float32(2.0 ** -140)           # bf16 subnormals
+        f[3, : min(k, 48)] = 0.0                  # zero blocks
+    check_nvfp4(fme, orc, synth.bf16_bits(f))
+
+
+def test_nvfp4_groups_pad_scale_rows(fme, orc):
+    counts = np.array([0, 1, 127, 128, 129, 0, 300, 0])
+    off = synth.offsets_from_counts(counts)
+    rng = np.random.default_rng(7)
+    x = synth.bf16_bits(rng.standard_normal((int(off[-1]), 256), dtype=np.float32))
+    check_nvfp4(fme, orc, x, off)
+
+
+def test_nvfp4_batch_invariance_and_causality(fme, orc):
+    """Per-token scales: shuffling, splitting and appending later rows leave every
+    row's codes and scales bit-identical."""
+    x, _, _ = synth.quantizer_batch(rows=2048)
+    full = run_nvfp4(fme, x)
+    perm = np.random.default_rng(3).permutation(x.shape[0])
+    shuf = run_nvfp4(fme, x[perm])
+    for a, b in zip(full, shuf):
+        assert np.array_equal(a[perm], b)
+    cuts = [0, 1, 700, 701, 1500, 2048]
+    for lo, hi in zip(cuts[:-1], cuts[1:]):
+        part = run_nvfp4(fme, x[lo:hi])
+        for a, b in zip(full, part):
+            assert np.array_equal(a[lo:hi], b)
+    later = synth.normal_bits((512, x.shape[1]), 1e3, seed=9)
+    ext = run_nvfp4(fme, np.concatenate([x, later]))
+    for a, b in zip(full, ext):
+        assert np.array_equal(a, b[: x.shape[0]])
+
+
+def test_nvfp4_deterministic(fme):
+    x, _, _ = synth.quantizer_batch(rows=1024)
+    a = run_nvfp4(fme, x)
+    b = run_nvfp4(fme, x)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+# ------------------------------------------------------------------- MXFP8 --
+def test_mxfp8_worked_examples(fme):
+    cases = read_cases("mxfp8_worked.txt")
+    rows = []
+    for case in cases.values():
+        r = np.zeros(32, np.float32)
+        lead = [float(v) for v in case["x"].split()]
+        r[: len(lead)] = lead
+        rows.append(r)
+    codes, sf = run_mx_rows(fme, synth.bf16_bits(np.stack(rows)))
+    for i, case in enumerate(cases.values()):
+        want = [int(c, 16) for c in case["codes"].split()]
+        assert int(sf[i, 0]) == int(case["scale"]), case
+        assert [int(c) for c in codes[i, : len(want)]] == want, case
+
+
+def test_mxfp8_rows_tiny(fme, orc):
+    x, w = synth.tiny(0)
+    check_mx_rows(fme, orc, x)
+    check_mx_rows(fme, orc, w)
+
+
+def test_mxfp8_rows_quantizer_batch(fme, orc):
+    x, _, _ = synth.quantizer_batch()
+    check_mx_rows(fme, orc, x)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (33, 96), (129, 1056), (257, 7168)])
+def test_mxfp8_rows_edges(fme, orc, rows, cols):
+    rng = np.random.default_rng(rows + cols)
+    f = rng.standard_normal((rows, cols), dtype=np.float32)
+    f[rng.random(f.shape) < 0.02] *= 1e4
+    f[0, :32] = 0.0
+    if rows > 2:
+        f[2] *= np.float32(2.0 ** -135)
+    counts = np.array([rows // 3, 0, rows - rows // 3])
+    check_mx_rows(fme, orc, synth.bf16_bits(f), synth.offsets_from_counts(counts))
+
+
+def test_mxfp8_cols_quantizer_batch(fme, orc):
+    x, _, _ = synth.quantizer_batch()
+    counts = synth.dirichlet_counts(rows=x.shape[0], seed=1)
+    check_mx_cols(fme, orc, x, synth.offsets_from_counts(counts))
+
+
+@pytest.mark.parametrize("counts", [[1], [128], [0, 5, 0], [37, 0, 200, 1, 129], [0, 0, 0]])
+def test_mxfp8_cols_edges(fme, orc, counts):
+    off = synth.offsets_from_counts(counts)
+    rng = np.random.default_rng(len(counts) + int(off[-1]))
+    f = rng.standard_normal((int(off[-1]), 256), dtype=np.float32)
+    f[rng.random(f.shape) < 0.02] *= 300.0
+    x = synth.bf16_bits(f)
+    if off[-1] == 0:
+        codes, sf, poff, ld = run_mx_cols(fme, x, off)
+        assert np.all(poff == 0)
+        return
+    check_mx_cols(fme, orc, x, off)
+
+
+def test_mxfp8_rows_cols_deterministic(fme):
+    x, _, _ = synth.quantizer_batch(rows=512)
+    off = synth.offsets_from_counts([100, 0, 412])
+    assert all(np.array_equal(a, b) for a, b in zip(run_mx_rows(fme, x, off), run_mx_rows(fme, x, off)))
+    a, b = run_mx_cols(fme, x, off), run_mx_cols(fme, x, off)
+    p = int(a[2][-1])
+    assert np.array_equal(a[0][:, :p], b[0][:, :p]) and np.array_equal(a[1][:, : p // 32], b[1][:, : p // 32])
+
+
+def test_bad_offsets_set_device_status(fme):
+    import torch
+
+    x = bf16_tensor(synth.normal_bits((64, 256), 1.0, seed=1))
+    st = _status()
+    bad = torch.tensor([0, 40, 30, 64], dtype=torch.int32, device="cuda")
+    fme.quantize_nvfp4_pertoken(x, bad, status=st)
+    code, raw = fme.read_device_status(st)
+    assert raw & fme.DEV_BAD_OFFSETS and code == 7
+    st.zero_()
+    short = torch.tensor([0, 10, 20], dtype=torch.int32, device="cuda")   # does not reach rows
+    fme.quantize_mxfp8(x, fme.COLWISE, short, status=st)
+    assert fme.read_device_status(st)[1] & fme.DEV_BAD_OFFSETS
