@@ -1,0 +1,551 @@
+#!/usr/bin/env python3
+"""Benchmark of the low-precision MoE expert path on GB300.
+
+One step = one pass of the whole hot path over one batch of the skewed
+long-batch MoE workload (32 experts, hidden 7168, intermediate 2048, 262144
+routed rows, Zipf(1.2) loads with 3 empty experts):
+
+  forward (NVFP4):  quantize X and W_gate/up -> grouped GEMM gate/up,
+                    quantize H and W_down    -> grouped GEMM down
+  backward (MXFP8): quantize dY row-wise and W_down column-wise -> dgrad,
+                    quantize dY and H column-wise              -> wgrad
+
+12 launches of libfme.so per step, inputs resident in HBM (every input is
+larger than the 129 MB L2).  The headline value is grouped-GEMM TFLOP/s over
+the whole step (GEMM FLOPs / step time, quantizers included); each call's time,
+GB/s or TFLOP/s and roofline fraction are reported in "breakdown".
+
+--impl reference times the CPU oracle (oracle/) on a bounded sample of the
+same workload, the only other place this file runs the oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grouped expert GEMM TFLOP/s & quantize GB/s on 1 GB300, % of FP4/FP8/HBM roofline"
+WORKLOADS = {
+    # the skewed long-batch stress case: the largest single-GPU workload, every step of the path
+    "moe-fwd-bwd-zipf-262144": dict(rows=262144, experts=32, loads="zipf", seed=4),
+    # the forward/backward pair at 65536 routed rows with Dirichlet(1) loads
+    "moe-fwd-bwd-dirichlet-65536": dict(rows=65536, experts=32, loads="dirichlet", seed=2),
+    # a small case (8 experts, about 2 GB on the device) for ncu captures
+    "profile-8x16384": dict(rows=16384, experts=8, loads="dirichlet", seed=2),
+}
+DEFAULT_WORKLOAD = "moe-fwd-bwd-zipf-262144"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dense tensor-core throughput relative to bf16 (nominal GB300 figures: bf16 2.25, fp8 4.5, fp4 13.5 PF)
+DTYPE_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}
+
+
+# --------------------------------------------------------------------- helpers --
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def counts_for(wl):
+    from fp8_moe_expert_gb300 import synth
+
+    if wl["loads"] == "zipf":
+        return synth.zipf_counts(rows=wl["rows"], experts=wl["experts"], seed=wl["seed"])
+    return synth.dirichlet_counts(rows=wl["rows"], experts=wl["experts"], seed=wl["seed"])
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the step --
+class MoEStep:
+    """Device buffers of one MoE-layer forward+backward and the 12 calls over them."""
+
+    CALLS = ["quant_x_nvfp4", "quant_wgu_nvfp4", "gemm_fwd_gate_up", "quant_h_nvfp4", "quant_wd_nvfp4",
+             "gemm_fwd_down", "quant_dy_rows_mxfp8", "quant_wd_cols_mxfp8", "gemm_dgrad",
+             "quant_dy_cols_mxfp8", "quant_h_cols_mxfp8", "gemm_wgrad"]
+
+    def __init__(self, counts, seed, device, inputs_only=False):
+        import torch
+
+        import fp8_moe_expert_gb300 as fme
+        from fp8_moe_expert_gb300 import synth
+
+        self.fme = fme
+        self.counts = counts
+        E, H, I = len(counts), synth.HIDDEN, synth.INTERMEDIATE
+        R = int(sum(counts))
+        self.E, self.H, self.I, self.R = E, H, I, R
+        dev = device
+        self.dev = dev
+        self.offsets = torch.from_numpy(synth.offsets_from_counts(counts)).to(dev)
+        # inputs (bf16, seeded, made on the device)
+        self.x = synth.torch_normal((R, H), 1.0, seed * 10 + 1, dev)
+        self.w_gu = synth.torch_normal((E * 2 * I, H), 0.02, seed * 10 + 2, dev)
+        self.h = synth.torch_normal((R, I), 1.0, seed * 10 + 3, dev)
+        self.w_d = synth.torch_normal((E * H, I), 0.02, seed * 10 + 4, dev)
+        self.dy = synth.torch_normal((R, H), 1e-2, seed * 10 + 5, dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if inputs_only:
+            return
+        u8, f32, bf16, i32 = torch.uint8, torch.float32, torch.bfloat16, torch.int32
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
+        # quantized operands and outputs, allocated once
+        self.xq = (e((R, H // 2), u8), e((fme.sf_bytes(R, H, 16, E),), u8), e((R,), f32))
+        self.wguq = (e((E * 2 * I, H // 2), u8), e((fme.sf_bytes(E * 2 * I, H, 16, 1),), u8), e((E * 2 * I,), f32))
+        self.hq = (e((R, I // 2), u8), e((fme.sf_bytes(R, I, 16, E),), u8), e((R,), f32))
+        self.wdq = (e((E * H, I // 2), u8), e((fme.sf_bytes(E * H, I, 16, 1),), u8), e((E * H,), f32))
+        self.y_gu = e((R, 2 * I), bf16)
+        self.y_d = e((R, H), bf16)
+        self.dyr = (e((R, H), u8), e((fme.sf_bytes(R, H, 32, E),), u8))
+        self.ld_w = fme.colwise_ld(E * H, 1)
+        self.wdc = (e((I, self.ld_w), u8), e((fme.sf_bytes(I, self.ld_w, 32, 1),), u8), e((2,), i32))
+        self.dh = e((R, I), bf16)
+        self.ld_r = fme.colwise_ld(R, E)
+        self.dyc = (e((H, self.ld_r), u8), e((fme.sf_bytes(H, self.ld_r, 32, 1),), u8), e((E + 1,), i32))
+        self.hc = (e((I, self.ld_r), u8), e((fme.sf_bytes(I, self.ld_r, 32, 1),), u8), e((E + 1,), i32))
+        self.dw = e((E, H, I), bf16)
+
+    # algorithmic work per call: ("bytes"|"flops", amount)
+    def work(self):
+        R, H, I, E = self.R, self.H, self.I, self.E
+        nv = lambda rows, k: rows * (2 * k + k // 2 + k // 16 + 4)  # noqa: E731
+        mx = lambda rows, c: rows * (2 * c + c + c // 32)  # noqa: E731
+        return {
+            "quant_x_nvfp4": ("bytes", nv(R, H)),
+            "quant_wgu_nvfp4": ("bytes", nv(E * 2 * I, H)),
+            "gemm_fwd_gate_up": ("flops", 2 * R * 2 * I * H),
+            "quant_h_nvfp4": ("bytes", nv(R, I)),
+            "quant_wd_nvfp4": ("bytes", nv(E * H, I)),
+            "gemm_fwd_down": ("flops", 2 * R * H * I),
+            "quant_dy_rows_mxfp8": ("bytes", mx(R, H)),
+            "quant_wd_cols_mxfp8": ("bytes", mx(E * H, I)),
+            "gemm_dgrad": ("flops", 2 * R * I * H),
+            "quant_dy_cols_mxfp8": ("bytes", mx(R, H)),
+            "quant_h_cols_mxfp8": ("bytes", mx(R, I)),
+            "gemm_wgrad": ("flops", 2 * R * H * I),
+        }
+
+    def gemm_dtype(self, call):
+        return "fp4" if call.startswith("gemm_fwd") else "fp8"
+
+    def calls(self):
+        f, off, st, E, H, I = self.fme, self.offsets, self.status, self.E, self.H, self.I
+        return [
+            lambda: f.quantize_nvfp4_pertoken(self.x, off, codes=self.xq[0], sf=self.xq[1], row_scale=self.xq[2],
+                                              status=st),
+            lambda: f.quantize_nvfp4_pertoken(self.w_gu, codes=self.wguq[0], sf=self.wguq[1], row_scale=self.wguq[2],
+                                              status=st),
+            lambda: f.grouped_gemm_fwd_nvfp4(*self.xq, *self.wguq, off, 2 * I, H, y=self.y_gu, status=st),
+            lambda: f.quantize_nvfp4_pertoken(self.h, off, codes=self.hq[0], sf=self.hq[1], row_scale=self.hq[2],
+                                              status=st),
+            lambda: f.quantize_nvfp4_pertoken(self.w_d, codes=self.wdq[0], sf=self.wdq[1], row_scale=self.wdq[2],
+                                              status=st),
+            lambda: f.grouped_gemm_fwd_nvfp4(*self.hq, *self.wdq, off, H, I, y=self.y_d, status=st),
+            lambda: f.quantize_mxfp8(self.dy, f.ROWWISE, off, codes=self.dyr[0], sf=self.dyr[1], status=st),
+            lambda: f.quantize_mxfp8(self.w_d, f.COLWISE, codes=self.wdc[0], sf=self.wdc[1], padded_offsets=self.wdc[2],
+                                     status=st),
+            lambda: f.grouped_gemm_dgrad_mxfp8(*self.dyr, self.wdc[0], self.wdc[1], self.ld_w, off, I, H, y=self.dh,
+                                               status=st),
+            lambda: f.quantize_mxfp8(self.dy, f.COLWISE, off, codes=self.dyc[0], sf=self.dyc[1],
+                                     padded_offsets=self.dyc[2], status=st),
+            lambda: f.quantize_mxfp8(self.h, f.COLWISE, off, codes=self.hc[0], sf=self.hc[1], padded_offsets=self.hc[2],
+                                     status=st),
+            lambda: f.grouped_gemm_wgrad_mxfp8(self.dyc[0], self.dyc[1], self.ld_r, self.hc[0], self.hc[1], self.ld_r,
+                                               self.dyc[2], H, I, y=self.dw, status=st),
+        ]
+
+    def gemm_flops(self):
+        return sum(v for k, (kind, v) in self.work().items() if kind == "flops")
+
+    def inputs(self):
+        return [self.x, self.w_gu, self.h, self.w_d, self.dy]
+
+    def outputs(self):
+        return [self.y_gu, self.y_d, self.dh, self.dw]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    import fp8_moe_expert_gb300 as fme
+
+    fme.lib()  # fails loudly without the CUDA library
+    wl = WORKLOADS[args.workload]
+    counts = counts_for(wl)
+    step = MoEStep(counts, wl["seed"], dev)
+    calls = step.calls()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    code, raw = fme.read_device_status(step.status)
+    if code != 0:
+        raise RuntimeError(f"device status {raw:#x} after warm-up")
+
+    # ------------------------------------------------------------ timed region
+    n_calls = len(calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        start.record(stream)
+        for s in range(args.steps):
+            for i, c in enumerate(calls):
+                ev[s][i].record(stream)
+                c()
+            ev[s][n_calls].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    code, raw = fme.read_device_status(step.status)
+    if code != 0:
+        raise RuntimeError(f"device status {raw:#x} in the timed region")
+
+    per_call = {name: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
+                for i, name in enumerate(MoEStep.CALLS)}
+    ms_per_step = elapsed_ms / args.steps
+    flops = step.gemm_flops()
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_kind = load_peaks()
+    bf16_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    hbm = float(peaks["hbm_gbs"])
+    breakdown = {}
+    for name, (kind, amount) in step.work().items():
+        ms = per_call[name]
+        if kind == "bytes":
+            ach = amount / (ms * 1e-3) / 1e9
+            breakdown[name] = {"ms": round(ms, 4), "GB/s": round(ach, 1), "frac_hbm": round(ach / hbm, 3)}
+        else:
+            ach = amount / (ms * 1e-3) / 1e12
+            pk = bf16_sus * DTYPE_RATIO[step.gemm_dtype(name)]
+            breakdown[name] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1),
+                               f"frac_{step.gemm_dtype(name)}": round(ach / pk, 3)}
+    top = max(per_call, key=per_call.get)
+    kind, amount = step.work()[top]
+    if kind == "flops":
+        pk = bf16_sus * DTYPE_RATIO[step.gemm_dtype(top)]
+        ach = amount / (per_call[top] * 1e-3) / 1e12
+        roof = {"kernel": top, "bound": "tensor", "achieved": round(ach, 1), "peak": round(pk, 1),
+                "unit": "TFLOP/s", "frac": round(ach / pk, 3),
+                "peak_source": f"{peak_kind} bf16_tflops_sustained x {DTYPE_RATIO[step.gemm_dtype(top)]:g} "
+                               f"({step.gemm_dtype(top)} / bf16 nominal ratio)"}
+    else:
+        ach = amount / (per_call[top] * 1e-3) / 1e9
+        roof = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 3), "peak_source": f"{peak_kind} hbm_gbs"}
+    roof["traffic"] = lookup_traffic(top, args.workload)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 fwd / mxfp8 bwd, fp32 accumulate",
+        "data": "synthetic (seeded torch normal on device; Zipf/Dirichlet expert loads from numpy)",
+        "config": {"workload": args.workload, "experts": step.E, "hidden": step.H, "intermediate": step.I,
+                   "routed_rows": step.R, "expert_rows_max": int(max(counts)),
+                   "empty_experts": int(sum(1 for c in counts if c == 0)),
+                   "l2": "inputs larger than L2 (129 MB) every call", "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "breakdown": breakdown,
+        "gpu_launches": n_calls * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(step, calls, args, world)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(step, counts)
+    elif rank == 0 and world > 1:
+        line["cpu_baseline"] = None
+    return line
+
+
+def run_e2e(step, calls, args, world):
+    """Same metric through the public API with host buffers: each step copies the
+    inputs from pinned host memory, runs the 12 calls and copies every output back."""
+    import torch
+
+    ins = step.inputs()
+    outs = step.outputs()
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    for h, d in zip(h_in, ins):
+        h.copy_(d)
+    steps = max(1, min(args.steps, 5))
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        for c in calls:
+            c()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    if world > 1:
+        t = torch.tensor([ms], device=step.dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    bi = sum(t.numel() * t.element_size() for t in ins)
+    bo = sum(t.numel() * t.element_size() for t in outs)
+    return {"value": round(world * step.gemm_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "steps": steps, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+# --------------------------------------------------------- oracle (CPU) timing --
+def oracle_sample(step, counts, rows_per_gemm, cols, rng_seed=0):
+    """Time the CPU oracle on a sample of the step: `rows_per_gemm` token rows of
+    one expert through every GEMM (all output columns if cols is None, else
+    `cols` sampled output columns; only the weight rows or columns those need
+    are quantized), plus `rows_per_gemm` channel rows of that expert's wgrad.
+    Inputs are copied to the host before the clock starts.
+    Returns (seconds, gemm_flops, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from tests.fmetest import bf16_bits_np
+
+    orc = oracle.Oracle()
+    E, H, I = step.E, step.H, step.I
+    off = np.concatenate([[0], np.cumsum(counts)])
+    live = [g for g, c in enumerate(counts) if c >= 2 * rows_per_gemm]
+    g = min(live, key=lambda e: counts[e])  # smallest expert that holds the sample
+    rng = np.random.default_rng(rng_seed)
+    r = np.sort(rng.choice(np.arange(off[g], off[g + 1]), size=rows_per_gemm, replace=False))
+    ri = torch.from_numpy(r).to(step.dev)
+
+    def colsel(n):
+        return np.arange(n) if cols is None else np.sort(rng.choice(n, size=min(cols, n), replace=False))
+
+    c_gu, c_d, c_dg, c_wg = colsel(2 * I), colsel(H), colsel(I), colsel(I)
+    ch = np.sort(rng.choice(H, size=rows_per_gemm, replace=False))
+    host = {
+        "x": bf16_bits_np(step.x[ri]), "h": bf16_bits_np(step.h[ri]), "dy": bf16_bits_np(step.dy[ri]),
+        "wgu": bf16_bits_np(step.w_gu[g * 2 * I:(g + 1) * 2 * I][torch.from_numpy(c_gu).to(step.dev)]),
+        "wd": bf16_bits_np(step.w_d[g * H:(g + 1) * H]),
+        "dy_e": bf16_bits_np(step.dy[off[g]:off[g + 1]]), "h_e": bf16_bits_np(step.h[off[g]:off[g + 1]]),
+    }
+    n_e = int(counts[g])
+    t0 = time.perf_counter()
+    # forward, NVFP4
+    a = orc.dequant_nvfp4(*orc.quant_nvfp4(host["x"]))
+    b = orc.dequant_nvfp4(*orc.quant_nvfp4(host["wgu"]))
+    orc.gemm_abt(a, b)
+    a = orc.dequant_nvfp4(*orc.quant_nvfp4(host["h"]))
+    b = orc.dequant_nvfp4(*orc.quant_nvfp4(np.ascontiguousarray(host["wd"][c_d])))
+    orc.gemm_abt(a, b)
+    # backward, MXFP8: dgrad (W_down column-wise along the 7168 axis)
+    a = orc.dequant_mxfp8(*orc.quant_mxfp8_rows(host["dy"]))
+    wcols = np.ascontiguousarray(host["wd"][:, c_dg])
+    ct, st, _ = orc.quant_mxfp8_cols(wcols, np.array([0, H]))
+    orc.gemm_abt(a, orc.dequant_mxfp8(ct, st)[:, :H])
+    # wgrad: dY_e and H_e column-wise over the expert's rows
+    e_off = np.array([0, n_e])
+    ca, sa, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(host["dy_e"][:, ch]), e_off)
+    cb, sb, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(host["h_e"][:, c_wg]), e_off)
+    orc.gemm_abt(orc.dequant_mxfp8(ca, sa), orc.dequant_mxfp8(cb, sb))
+    secs = time.perf_counter() - t0
+    k = len(r)
+    flops = 2 * k * (len(c_gu) * H + len(c_d) * I + len(c_dg) * H) + 2 * len(ch) * len(c_wg) * n_e
+    desc = (f"expert {g} ({n_e} rows): {k} token rows through gate/up ({len(c_gu)} cols), down ({len(c_d)} cols), "
+            f"dgrad ({len(c_dg)} cols); wgrad {len(ch)} x {len(c_wg)} over {n_e} rows; quantization of every "
+            f"operand row/column those need included")
+    return secs, flops, desc
+
+
+def cpu_baseline(step, counts):
+    secs, flops, desc = oracle_sample(step, counts, rows_per_gemm=16, cols=None)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": desc, "seconds": round(secs, 3)}
+
+
+def run_reference(args, rank, world, local_rank):
+    """Reference arm: the CPU oracle, as it stands, on bounded samples of the workload."""
+    import torch
+
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local_rank)
+    wl = WORKLOADS[args.workload]
+    counts = counts_for(wl)
+    step = MoEStep(counts, wl["seed"], f"cuda:{local_rank}", inputs_only=True)
+    for i in range(args.warmup):
+        oracle_sample(step, counts, rows_per_gemm=4, cols=64, rng_seed=i)
+    total_s, total_f, desc = 0.0, 0, ""
+    for i in range(args.steps):
+        s, f, desc = oracle_sample(step, counts, rows_per_gemm=4, cols=64, rng_seed=1000 + i)
+        total_s += s
+        total_f += f
+    value = total_f / total_s / 1e12
+    ms = total_s / args.steps * 1e3
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 GEMM on exactly dequantized operands; fp32 quantizers",
+        "data": "synthetic (same seeded workload as the CUDA arm)",
+        "config": {"workload": args.workload, "experts": step.E, "hidden": step.H, "intermediate": step.I,
+                   "routed_rows": step.R},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------- traffic --
+def lookup_traffic(call, workload):
+    """ncu DRAM bytes per launch for `call`, from profiles/ncu_traffic.json, or None
+    when absent or taken on a kernel source that has changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        table = json.load(fh)
+    entry = table.get(workload, {}).get(call)
+    if not entry:
+        return None
+    if entry.get("source_sha256") != source_digest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_moe_expert_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch
+
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    line = run_reference(args, rank, world, local_rank) if args.impl == "reference" else \
+        run_ours(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -193,7 +193,7 @@ fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axi
     if (padded_offsets == nullptr) return FME_ERR_INVALID_ARGUMENT;
     if (!aligned16(padded_offsets)) return FME_ERR_MISALIGNED;
   }
-  if (!x || !codes || !sf) return FME_ERR_INVALID_ARGUMENT;
+  if ((!x && rows > 0) || !codes || !sf) return FME_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(sf)) return FME_ERR_MISALIGNED;
   int sms = 0;
   fme_status st = current_device(&sms);
