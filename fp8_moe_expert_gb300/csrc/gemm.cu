@@ -7,16 +7,18 @@
 // backward.  "Scaling and Optimizing Frontier Model Training", "MXFP8 expert
 // kernels": grouped GEMMs over the experts' routed tokens.
 //
-// One persistent kernel per call, one CTA per SM, 6 warps:
+// One persistent kernel per call, one CTA per SM, 10 warps:
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the 512-byte
 //               scale tiles into a 4-stage shared-memory ring;
 //   warp 1      allocates 512 tensor-memory columns, then one thread copies each
 //               stage's scales into tensor memory (tcgen05.cp) and issues the
 //               block-scaled MMAs (kind::mxf4nvf4 or kind::mxf8f6f4, M=128,
 //               N=256) into a 128 x 256 fp32 accumulator;
-//   warps 2-5   epilogue: tcgen05.ld the accumulator (each warp its 32-lane
-//               quarter), apply the per-token and per-column FP32 scales
-//               (forward), round to bf16, store rows that belong to the expert.
+//   warps 2-9   epilogue: tcgen05.ld the accumulator (each warp a 32-lane
+//               quarter and half of the columns) into registers, release it to
+//               the MMA warp, then apply the per-token and per-column FP32
+//               scales (forward), round to bf16 and store the rows that belong
+//               to the expert, overlapping the next tile's MMAs.
 // Tiles are 128 rows x 256 columns.  Every role walks the same tile sequence,
 // derived in shared memory from the per-expert offsets: forward and dgrad go
 // expert by expert, 128-row blocks of each expert's rows, 256-column blocks
@@ -33,7 +35,7 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kStageKBytes = 128;  // bytes of K per row per stage (one swizzle row)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
 constexpr int kAccCols = kBN;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kStageKBytes;
@@ -173,6 +175,33 @@ __device__ bool prepare(const LaunchGemm &p, SharedState &s) {
   return true;
 }
 
+// Scale (forward: (acc * S_x[t]) * S_w[n], fp32), round to bf16 and store 32
+// consecutive outputs of one row.
+template <GemmKind K>
+__device__ __forceinline__ void store_chunk(__nv_bfloat16 *dst, const uint32_t (&v)[32], float sa,
+                                            const float *sb) {
+  uint32_t packed[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float f[4] = {__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                  __uint_as_float(v[4 * j + 3])};
+    if (K == GemmKind::kFwdNvfp4) {
+      const float4 b = __ldg(reinterpret_cast<const float4 *>(sb) + j);
+      f[0] = __fmul_rn(__fmul_rn(f[0], sa), b.x);
+      f[1] = __fmul_rn(__fmul_rn(f[1], sa), b.y);
+      f[2] = __fmul_rn(__fmul_rn(f[2], sa), b.z);
+      f[3] = __fmul_rn(__fmul_rn(f[3], sa), b.w);
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
+    packed[2 * j] = *reinterpret_cast<const uint32_t *>(&lo);
+    packed[2 * j + 1] = *reinterpret_cast<const uint32_t *>(&hi);
+  }
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+}
+
 template <GemmKind K>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ LaunchGemm p) {
   using C = Cfg<K>;
@@ -197,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&s.empty[i], 1);
     }
     mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 4 * 32);
+    mbar_init(&s.acc_empty, 8 * 32);
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     fence_barrier_init();
@@ -311,54 +340,49 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else if (warp >= 2) {
     // --------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    // 8 warps: warp w reads tensor-memory lane quarter w % 4 (rows 32(w%4) ..
+    // +31) and column half (w - 2) / 4.  All 128 accumulator columns of a thread
+    // are loaded before the accumulator is released to the MMA warp, so the next
+    // tile's MMAs run while this tile is scaled, rounded and stored.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
+    const int c0 = half * (kBN / 2);
     uint32_t acc_phase = 0;
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = tile_at<K>(p, s, t);
       const bool valid = r < tl.rows_valid;
-      __nv_bfloat16 *yrow = y + tl.y_off + static_cast<int64_t>(r) * p.n;
+      __nv_bfloat16 *yrow = y + tl.y_off + static_cast<int64_t>(r) * p.n + c0;
       if (tl.num_k == 0) {
         if (valid)
-          for (int c = 0; c < kBN; c += 8) *reinterpret_cast<uint4 *>(yrow + c) = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < kBN / 2; c += 8) *reinterpret_cast<uint4 *>(yrow + c) = make_uint4(0, 0, 0, 0);
         continue;
       }
       if (!mbar_wait(&s.acc_full, acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + c0;
+      tmem_ld_32x32(taddr, v0);
+      tmem_ld_32x32(taddr + 32, v1);
+      tmem_ld_32x32(taddr + 64, v2);
+      tmem_ld_32x32(taddr + 96, v3);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty);
+      acc_phase ^= 1;
       float sa = 1.0f;
       const float *sb_row = nullptr;
       if (K == GemmKind::kFwdNvfp4) {
         if (valid) sa = __ldg(p.a_scale + tl.a_y + r);
-        sb_row = p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0;
+        sb_row = p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0 + c0;
       }
-#pragma unroll 1
-      for (int c = 0; c < kBN; c += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
-        tmem_wait_ld();
-        uint32_t packed[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float lo = __uint_as_float(v[2 * j]);
-          float hi = __uint_as_float(v[2 * j + 1]);
-          if (K == GemmKind::kFwdNvfp4) {
-            lo = __fmul_rn(__fmul_rn(lo, sa), __ldg(sb_row + c + 2 * j));
-            hi = __fmul_rn(__fmul_rn(hi, sa), __ldg(sb_row + c + 2 * j + 1));
-          }
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-          packed[j] = *reinterpret_cast<const uint32_t *>(&b2);
-        }
-        if (valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(yrow + c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-        }
+      if (valid) {
+        store_chunk<K>(yrow, v0, sa, sb_row);
+        store_chunk<K>(yrow + 32, v1, sa, sb_row ? sb_row + 32 : nullptr);
+        store_chunk<K>(yrow + 64, v2, sa, sb_row ? sb_row + 64 : nullptr);
+        store_chunk<K>(yrow + 96, v3, sa, sb_row ? sb_row + 96 : nullptr);
       }
-      tc_fence_before();
-      mbar_arrive(&s.acc_empty);
-      acc_phase ^= 1;
     }
   }
 

@@ -7,12 +7,16 @@
 // q = E2M1(x / e), all divisions correctly rounded (__fdiv_rn), all conversions
 // round-to-nearest-even with saturation.
 //
-// One warp owns one row.  Lane l holds elements [256 c + 8 l, 256 c + 8 l + 8) of
-// every 256-wide chunk c in registers (one 16-byte load per chunk), so the row
-// is read from HBM once: the row amax is a warp max-reduction, a 16-block spans
-// a lane pair (one shuffle), codes leave as one 4-byte store per lane per chunk
-// (128 contiguous bytes per warp) and the four scales of four consecutive blocks
-// leave as one 4-byte store into the tiled scale layout.
+// One to four warps own one row (rows longer than 2048 values are split).  Lane
+// l of a warp holds elements [256 c + 8 l, 256 c + 8 l + 8) of each 256-wide chunk
+// c it owns in registers (one 16-byte load per chunk), so the row is read from
+// HBM once: the row amax is a warp max-reduction (plus a shared-memory exchange
+// between the row's warps), a 16-block spans a lane pair (one shuffle), codes
+// leave as one 4-byte store per lane per chunk (128 contiguous bytes per warp)
+// and the four scales of four consecutive blocks leave as one 4-byte store into
+// the tiled scale layout.  The element codes come from the correctly rounded
+// quotient fl32(x/e), found without a division unless the quotient sits next to
+// an E2M1 rounding boundary (see e2m1_codes_of_quotients).
 #include "fme_device.cuh"
 #include "fme_launch.h"
 
@@ -40,39 +44,80 @@ __device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
   return r & 0xFFu;
 }
 
-template <int NCH>
-__global__ void __launch_bounds__(128) nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows,
-                                                             int k, const int32_t *__restrict__ offsets,
-                                                             int num_groups, uint8_t *__restrict__ codes,
-                                                             uint8_t *__restrict__ sf,
-                                                             float *__restrict__ row_scale, int32_t *status) {
+// E2M1 codes of the correctly rounded quotients fl32(x0/e), fl32(x1/e) (x0 in the
+// low nibble), without dividing unless a quotient sits next to a rounding
+// boundary of the E2M1 grid.
+//
+// With r = fl32(1/e) (correctly rounded) and e a normal fp32, q = fl32(x r)
+// differs from the exact x/e by less than 2^-22.9 relative, and Q = fl32(x/e) by
+// less than 2^-24, so Q lies strictly between fl32(q (1 - 2^-19)) and
+// fl32(q (1 + 2^-19)).  Rounding to the E2M1 grid is monotone in |v| (same sign
+// throughout), so when both ends round to the same code Q does too.  Otherwise
+// (a quotient within 2^-19 of a grid midpoint, e.g. an exact tie) the code comes
+// from the IEEE quotient itself.  Quotients far below 0.25 round to (signed) zero
+// on every path.  The result is always the code of fl32(x/e).
+__device__ __forceinline__ uint32_t e2m1_codes_of_quotients(float x0, float x1, float e, float r, bool normal_e) {
+  constexpr float kBelow = 1.0f - 1.0f / 524288.0f;  // 1 - 2^-19, exact in fp32
+  constexpr float kAbove = 1.0f + 1.0f / 524288.0f;  // 1 + 2^-19
+  if (normal_e) {
+    const float q0 = __fmul_rn(x0, r);
+    const float q1 = __fmul_rn(x1, r);
+    const uint32_t lo = e2m1_pair(__fmul_rn(q0, kBelow), __fmul_rn(q1, kBelow));
+    const uint32_t hi = e2m1_pair(__fmul_rn(q0, kAbove), __fmul_rn(q1, kAbove));
+    if (lo == hi) return lo;
+  }
+  return e2m1_pair(__fdiv_rn(x0, e), __fdiv_rn(x1, e));
+}
+
+// Row split: WPR warps share one row; warp w of the row takes chunks w, w + WPR,
+// ... (NCH of them), so every warp keeps at most 8 chunks (64 registers of data)
+// in flight and the SM runs more warps.  The row amax is combined through shared
+// memory behind a named barrier of the row's warps (slot parity alternates per
+// row, so one barrier per row suffices).
+constexpr int kNvThreads = 256;
+
+__device__ __forceinline__ void row_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+template <int NCH, int WPR>
+__global__ void __launch_bounds__(kNvThreads) nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                    int k, const int32_t *__restrict__ offsets,
+                                                                    int num_groups, uint8_t *__restrict__ codes,
+                                                                    uint8_t *__restrict__ sf,
+                                                                    float *__restrict__ row_scale, int32_t *status) {
+  constexpr int kRowsPerCta = (kNvThreads / 32) / WPR;
   __shared__ GroupTable groups;
   __shared__ int ok_flag;
+  __shared__ uint32_t partial[2][kRowsPerCta][WPR];
   if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(status, kDevBadOffsets);
     return;
   }
   const int lane = threadIdx.x & 31;
-  const int warps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int slot = warp / WPR;  // row slot of this CTA
+  const int wr = warp % WPR;    // part of the row
   const int64_t c4 = ((k / 16) + 3) & ~3;
+  int parity = 0;
 
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); row < rows;
-       row += static_cast<int64_t>(gridDim.x) * warps) {
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + slot; row < rows;
+       row += static_cast<int64_t>(gridDim.x) * kRowsPerCta, parity ^= 1) {
     const uint16_t *xr = x + row * k;
     uint4 v[NCH];
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const int col = c * 256 + lane * 8;
+    for (int j = 0; j < NCH; ++j) {
+      const int col = (wr + WPR * j) * 256 + lane * 8;
       if (col < k)
-        v[c] = __ldcs(reinterpret_cast<const uint4 *>(xr + col));
+        v[j] = __ldcs(reinterpret_cast<const uint4 *>(xr + col));
       else
-        v[c] = make_uint4(0, 0, 0, 0);
+        v[j] = make_uint4(0, 0, 0, 0);
     }
     // row amax (|x| as bits: bf16 magnitudes order like integers)
     uint32_t amax_bits = 0;
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+    for (int j = 0; j < NCH; ++j) {
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         amax_bits = max(amax_bits, w[i] & 0x7FFFu);
@@ -81,6 +126,12 @@ __global__ void __launch_bounds__(128) nvfp4_pertoken_kernel(const uint16_t *__r
     }
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, s));
+    if (WPR > 1) {
+      if (lane == 0) partial[parity][slot][wr] = amax_bits;
+      row_barrier(1 + slot, WPR * 32);
+#pragma unroll
+      for (int i = 0; i < WPR; ++i) amax_bits = max(amax_bits, partial[parity][slot][i]);
+    }
     const float amax = bf16_bits_to_float(amax_bits);
     const float s_t = (amax_bits == 0) ? 0.0f : __fdiv_rn(amax, 2688.0f);
     const float d = __fmul_rn(6.0f, s_t);
@@ -91,9 +142,10 @@ __global__ void __launch_bounds__(128) nvfp4_pertoken_kernel(const uint16_t *__r
     uint8_t *codes_row = codes + row * (k / 2);
 
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
+    for (int j = 0; j < NCH; ++j) {
+      const int c = wr + WPR * j;
       const int col = c * 256 + lane * 8;
-      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
       uint32_t bmax = 0;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -106,15 +158,17 @@ __global__ void __launch_bounds__(128) nvfp4_pertoken_kernel(const uint16_t *__r
       uint32_t packed = 0;
       if (sb != 0) {
         const float e = __fmul_rn(e4m3_value(sb), s_t);
+        const float r = __frcp_rn(e);
+        const bool normal_e = e >= 1.17549435e-38f;  // 1/e finite
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float lo = __fdiv_rn(bf16_bits_to_float(w[i] & 0xFFFFu), e);
-          const float hi = __fdiv_rn(bf16_bits_to_float(w[i] >> 16), e);
-          packed |= e2m1_pair(lo, hi) << (8 * i);
+          const float x0 = bf16_bits_to_float(w[i] & 0xFFFFu);
+          const float x1 = bf16_bits_to_float(w[i] >> 16);
+          packed |= e2m1_codes_of_quotients(x0, x1, e, r, normal_e) << (8 * i);
         }
       }
       if (col < k) *reinterpret_cast<uint32_t *>(codes_row + col / 2) = packed;
-      // scales: block (c*16 + lane/2) is held by the even lane of each pair; lanes
+      // scales: block (16 c + lane/2) is held by the even lane of each pair; lanes
       // 0, 8, 16, 24 gather four consecutive blocks and store them as one word.
       const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
       const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
@@ -125,34 +179,32 @@ __global__ void __launch_bounds__(128) nvfp4_pertoken_kernel(const uint16_t *__r
         *reinterpret_cast<uint32_t *>(sf + sf_offset(prow, cb, c4)) = word;
       }
     }
-    if (lane == 0) row_scale[row] = s_t;
+    if (lane == 0 && wr == 0) row_scale[row] = s_t;
   }
 }
 
-template <int NCH>
+template <int NCH, int WPR>
 static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
-  const int threads = 128;
-  const int64_t blocks_needed = (a.rows + 3) / 4;
-  const int64_t cap = static_cast<int64_t>(a.num_sms) * 16;
+  constexpr int rows_per_cta = (kNvThreads / 32) / WPR;
+  const int64_t blocks_needed = (a.rows + rows_per_cta - 1) / rows_per_cta;
+  const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
   const int blocks = static_cast<int>(blocks_needed < cap ? (blocks_needed > 0 ? blocks_needed : 1) : cap);
-  nvfp4_pertoken_kernel<NCH><<<blocks, threads, 0, a.stream>>>(
+  nvfp4_pertoken_kernel<NCH, WPR><<<blocks, kNvThreads, 0, a.stream>>>(
       static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k), a.offsets, a.num_groups, a.codes, a.sf,
       a.row_scale, a.status);
   return cudaGetLastError();
 }
 
+// Chunks of 256 values per row: up to 8 per warp, rows of more than 8 chunks
+// are split over 2 or 4 warps (k <= 8192 = 32 chunks).
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
-  const int nch = static_cast<int>((a.k + 255) / 256);
-  if (nch <= 1) return launch_nvfp4<1>(a);
-  if (nch <= 2) return launch_nvfp4<2>(a);
-  if (nch <= 4) return launch_nvfp4<4>(a);
-  if (nch <= 8) return launch_nvfp4<8>(a);
-  if (nch <= 12) return launch_nvfp4<12>(a);
-  if (nch <= 16) return launch_nvfp4<16>(a);
-  if (nch <= 20) return launch_nvfp4<20>(a);
-  if (nch <= 24) return launch_nvfp4<24>(a);
-  if (nch <= 28) return launch_nvfp4<28>(a);
-  return launch_nvfp4<32>(a);
+  const int chunks = static_cast<int>((a.k + 255) / 256);
+  if (chunks <= 1) return launch_nvfp4<1, 1>(a);
+  if (chunks <= 2) return launch_nvfp4<2, 1>(a);
+  if (chunks <= 4) return launch_nvfp4<4, 1>(a);
+  if (chunks <= 8) return launch_nvfp4<8, 1>(a);
+  if (chunks <= 16) return launch_nvfp4<8, 2>(a);
+  return launch_nvfp4<8, 4>(a);
 }
 
 }  // namespace fme
