@@ -141,7 +141,9 @@ __global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restr
   const int cblocks = cols / 128;
   const int64_t total = chunks * cblocks;
 
-  for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+  // Tile t -> (chunk j, column block cb); the next tile's 32 KB is loaded into
+  // registers while the current one is quantized and stored.
+  auto load_tile = [&](int64_t t, uint4 (&dst)[8]) {
     const int64_t j = t / cblocks;
     const int cb = static_cast<int>(t % cblocks);
     const int g = find_group(groups.tiles, num_groups, j);
@@ -149,18 +151,27 @@ __global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restr
     const int64_t n_g = groups.off[g + 1] - groups.off[g];
     const int valid = static_cast<int>(n_g - local0 < 128 ? n_g - local0 : 128);
     const int64_t src0 = groups.off[g] + local0;
-
-    __syncthreads();  // the previous tile's shared buffers are free
 #pragma unroll
     for (int pass = 0; pass < 8; ++pass) {
       const int r = pass * 16 + (tid >> 4);
       const int seg = tid & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < valid)
-        v = __ldcs(reinterpret_cast<const uint4 *>(x + (src0 + r) * cols + cb * 128 + seg * 8));
-      *reinterpret_cast<uint4 *>(&tile[r][seg * 8]) = v;
+      dst[pass] = (r < valid)
+                      ? __ldcs(reinterpret_cast<const uint4 *>(x + (src0 + r) * cols + cb * 128 + seg * 8))
+                      : make_uint4(0, 0, 0, 0);
     }
+  };
+  uint4 pre[8];
+  if (static_cast<int64_t>(blockIdx.x) < total) load_tile(blockIdx.x, pre);
+
+  for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    const int64_t j = t / cblocks;
+    const int cb = static_cast<int>(t % cblocks);
+    __syncthreads();  // the previous tile's shared buffers are free
+#pragma unroll
+    for (int pass = 0; pass < 8; ++pass)
+      *reinterpret_cast<uint4 *>(&tile[pass * 16 + (tid >> 4)][(tid & 15) * 8]) = pre[pass];
     __syncthreads();
+    if (t + gridDim.x < total) load_tile(t + gridDim.x, pre);
 
     const int c = tid & 127;
 #pragma unroll

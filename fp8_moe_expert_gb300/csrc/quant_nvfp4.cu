@@ -35,6 +35,20 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu)));
 }
 
+// Per-halfword unsigned max of two words of packed bf16 magnitudes.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Largest |x| of the 8 bf16 in a uint4, as bf16 magnitude bits.
+__device__ __forceinline__ uint32_t amax8_bits(const uint4 &v) {
+  const uint32_t m = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
 // Two E2M1 codes: `lo` in bits 0..3, `hi` in bits 4..7.
 __device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
   uint16_t r;
@@ -81,7 +95,7 @@ __device__ __forceinline__ void row_barrier(int id, int threads) {
 }
 
 template <int NCH, int WPR>
-__global__ void __launch_bounds__(kNvThreads) nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(kNvThreads, 3) nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                     int k, const int32_t *__restrict__ offsets,
                                                                     int num_groups, uint8_t *__restrict__ codes,
                                                                     uint8_t *__restrict__ sf,
@@ -113,16 +127,13 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_pertoken_kernel(const uint16
       else
         v[j] = make_uint4(0, 0, 0, 0);
     }
-    // row amax (|x| as bits: bf16 magnitudes order like integers)
+    // per-chunk lane amax (|x| as bits: bf16 magnitudes order like integers), then row amax
+    uint32_t lane_max[NCH];
     uint32_t amax_bits = 0;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        amax_bits = max(amax_bits, w[i] & 0x7FFFu);
-        amax_bits = max(amax_bits, (w[i] >> 16) & 0x7FFFu);
-      }
+      lane_max[j] = amax8_bits(v[j]);
+      amax_bits = max(amax_bits, lane_max[j]);
     }
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, s));
@@ -146,13 +157,7 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_pertoken_kernel(const uint16
       const int c = wr + WPR * j;
       const int col = c * 256 + lane * 8;
       const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      uint32_t bmax = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        bmax = max(bmax, w[i] & 0x7FFFu);
-        bmax = max(bmax, (w[i] >> 16) & 0x7FFFu);
-      }
-      bmax = max(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
+      const uint32_t bmax = max(lane_max[j], __shfl_xor_sync(0xFFFFFFFFu, lane_max[j], 1));
       uint32_t sb = 0;
       if (bmax != 0) sb = e4m3_code(__fdiv_rn(bf16_bits_to_float(bmax), d));
       uint32_t packed = 0;
@@ -162,8 +167,8 @@ __global__ void __launch_bounds__(kNvThreads) nvfp4_pertoken_kernel(const uint16
         const bool normal_e = e >= 1.17549435e-38f;  // 1/e finite
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float x0 = bf16_bits_to_float(w[i] & 0xFFFFu);
-          const float x1 = bf16_bits_to_float(w[i] >> 16);
+          const float x0 = __uint_as_float(w[i] << 16);
+          const float x1 = __uint_as_float(w[i] & 0xFFFF0000u);
           packed |= e2m1_codes_of_quotients(x0, x1, e, r, normal_e) << (8 * i);
         }
       }
