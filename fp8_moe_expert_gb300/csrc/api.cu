@@ -103,6 +103,30 @@ fme_status encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint
   return FME_OK;
 }
 
+// Tiled scales of a tensor as a 2-D map of 8-byte words: one row per 128-row
+// block (`row_bytes` bytes each), boxes of `box_tiles` 512-byte tiles x `box_rows`
+// blocks, no swizzle, zero fill out of bounds.
+fme_status encode_scales_2d(CUtensorMap *map, const void *base, uint64_t row_blocks, uint64_t row_bytes,
+                            uint32_t box_tiles, uint32_t box_rows) {
+  EncodeTiledFn fn;
+  fme_status st = get_encoder(&fn);
+  if (st != FME_OK) return st;
+  cuuint64_t dims[2] = {row_bytes / 8, row_blocks};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {64 * box_tiles, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (scales) failed (CUresult %d)", static_cast<int>(r));
+    g_last_cuda_error = buf;
+    return FME_ERR_CUDA;
+  }
+  return FME_OK;
+}
+
 int64_t padded_rows_bound(int64_t rows, int32_t groups) {
   if (rows < 0 || groups < 1) return 0;
   return ((rows + 127 * static_cast<int64_t>(groups)) / 128) * 128;
@@ -225,10 +249,15 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   fme::LaunchGemm a{};
   a.kind = fme::GemmKind::kFwdNvfp4;
   if ((st = encode_u8_2d(&a.map_a, a_codes, k / 2, m, k / 2, 128)) != FME_OK) return st;
-  if ((st = encode_u8_2d(&a.map_b, b_codes, k / 2, static_cast<uint64_t>(num_experts) * n, k / 2, 256)) != FME_OK)
+  if ((st = encode_u8_2d(&a.map_b, b_codes, k / 2, static_cast<uint64_t>(num_experts) * n, k / 2, 128)) != FME_OK)
     return st;
-  a.sfa = a_sf;
-  a.sfb = b_sf;
+  // scales: (k / 64) tiles of 512 bytes per 128-row block; a stage takes 4 tiles
+  if ((st = encode_scales_2d(&a.map_sfa, a_sf, padded_rows_bound(m, num_experts) / 128, (k / 64) * 512, 4, 1)) !=
+      FME_OK)
+    return st;
+  if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * n / 128, (k / 64) * 512, 4, 2)) !=
+      FME_OK)
+    return st;
   a.a_scale = a_scale;
   a.b_scale = b_scale;
   a.offsets = offsets;
@@ -236,8 +265,6 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   a.m = m;
   a.n = n;
   a.k = k;
-  a.sfa_stride = (k / 16) * 128;  // (C4 / 4) tiles of 512 bytes per 128 rows
-  a.sfb_stride = (k / 16) * 128;
   a.y = y;
   a.status = dev_status;
   a.num_sms = sms;
@@ -265,16 +292,16 @@ fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
   fme::LaunchGemm a{};
   a.kind = fme::GemmKind::kDgradMxfp8;
   if ((st = encode_u8_2d(&a.map_a, a_codes, k, m, k, 128)) != FME_OK) return st;
-  if ((st = encode_u8_2d(&a.map_b, b_codes, ldb, n, ldb, 256)) != FME_OK) return st;
-  a.sfa = a_sf;
-  a.sfb = b_sf;
+  if ((st = encode_u8_2d(&a.map_b, b_codes, ldb, n, ldb, 128)) != FME_OK) return st;
+  if ((st = encode_scales_2d(&a.map_sfa, a_sf, padded_rows_bound(m, num_experts) / 128, (k / 128) * 512, 1, 1)) !=
+      FME_OK)
+    return st;
+  if ((st = encode_scales_2d(&a.map_sfb, b_sf, n / 128, (ldb / 128) * 512, 1, 2)) != FME_OK) return st;
   a.offsets = offsets;
   a.num_experts = num_experts;
   a.m = m;
   a.n = n;
   a.k = k;
-  a.sfa_stride = (k / 32) * 128;
-  a.sfb_stride = (ldb / 32) * 128;
   a.ldb = ldb;
   a.y = y;
   a.status = dev_status;
@@ -289,7 +316,7 @@ fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
                                     const int32_t *padded_offsets, int32_t num_experts, int64_t m, int64_t n,
                                     void *y, int32_t *dev_status, void *stream) {
   if (m < 0 || n < 0 || lda < 0 || ldb < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
-  if (m % 128 != 0 || m == 0 || n % 256 != 0 || n == 0 || lda % 128 != 0 || ldb % 128 != 0)
+  if (m % 256 != 0 || m == 0 || n % 256 != 0 || n == 0 || lda % 128 != 0 || ldb % 128 != 0)
     return FME_ERR_UNSUPPORTED_SHAPE;
   if (lda > (int64_t(1) << 31) - 1 || ldb > (int64_t(1) << 31) - 1 || m > 65536 || n > 65536)
     return FME_ERR_UNSUPPORTED_SHAPE;
@@ -307,21 +334,23 @@ fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
   fme::LaunchGemm a{};
   a.kind = fme::GemmKind::kWgradMxfp8;
   // With no positions at all every expert is empty: the maps are never used, so
-  // point them at a one-tile dummy extent of y (always at least 128 x 256 x 2 bytes).
+  // point them at a small dummy extent of y (always at least 256 x 256 x 2 bytes).
   const void *abase = has_positions ? static_cast<const void *>(a_codes) : y;
   const void *bbase = has_positions ? static_cast<const void *>(b_codes) : y;
+  const void *sabase = has_positions ? static_cast<const void *>(a_sf) : y;
+  const void *sbbase = has_positions ? static_cast<const void *>(b_sf) : y;
   const int64_t lda_e = has_positions ? lda : 128, ldb_e = has_positions ? ldb : 128;
   if ((st = encode_u8_2d(&a.map_a, abase, lda_e, has_positions ? m : 128, lda_e, 128)) != FME_OK) return st;
-  if ((st = encode_u8_2d(&a.map_b, bbase, ldb_e, has_positions ? n : 256, ldb_e, 256)) != FME_OK) return st;
-  a.sfa = a_sf;
-  a.sfb = b_sf;
+  if ((st = encode_u8_2d(&a.map_b, bbase, ldb_e, has_positions ? n : 128, ldb_e, 128)) != FME_OK) return st;
+  if ((st = encode_scales_2d(&a.map_sfa, sabase, has_positions ? m / 128 : 1, (lda_e / 128) * 512, 1, 1)) != FME_OK)
+    return st;
+  if ((st = encode_scales_2d(&a.map_sfb, sbbase, has_positions ? n / 128 : 2, (ldb_e / 128) * 512, 1, 2)) != FME_OK)
+    return st;
   a.offsets = padded_offsets;
   a.num_experts = num_experts;
   a.m = m;
   a.n = n;
   a.k = 0;
-  a.sfa_stride = (lda / 32) * 128;
-  a.sfb_stride = (ldb / 32) * 128;
   a.lda = lda;
   a.ldb = ldb;
   a.y = y;

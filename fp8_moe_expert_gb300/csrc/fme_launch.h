@@ -37,14 +37,12 @@ enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2 };
 
 struct LaunchGemm {
   GemmKind kind;
-  CUtensorMap map_a, map_b;
-  const uint8_t *sfa, *sfb;
+  CUtensorMap map_a, map_b;      // operand codes, uint8, 128-byte swizzle
+  CUtensorMap map_sfa, map_sfb;  // tiled scales viewed as [128-row blocks x 8-byte words]
   const float *a_scale, *b_scale;  // forward only
   const int32_t *offsets;          // row offsets (fwd, dgrad) or padded offsets (wgrad)
   int32_t num_experts;
   int64_t m, n, k;          // GEMM sizes; k unused for wgrad (per-expert)
-  int64_t sfa_stride;       // bytes between 128-row scale tiles of A
-  int64_t sfb_stride;       // bytes between 128-row scale tiles of B
   int64_t lda, ldb;         // wgrad: position extents of A and B; dgrad: ldb
   void *y;
   int32_t *status;

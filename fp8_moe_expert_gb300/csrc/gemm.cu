@@ -1,4 +1,4 @@
-// gemm.cu -- block-scaled grouped GEMMs on the tcgen05 tensor cores.
+// gemm.cu -- block-scaled grouped GEMMs on the tcgen05 tensor cores, CTA pairs.
 //
 // "Composer 2 Technical Report" (papercache.org summary), section 6.1: the MoE
 // layer's grouped GEMMs run as block-scaled tensor-core MMAs on Blackwell (the
@@ -7,146 +7,181 @@
 // backward.  "Scaling and Optimizing Frontier Model Training", "MXFP8 expert
 // kernels": grouped GEMMs over the experts' routed tokens.
 //
-// One persistent kernel per call, one CTA per SM, 10 warps:
-//   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the 512-byte
-//               scale tiles into a 4-stage shared-memory ring;
-//   warp 1      allocates 512 tensor-memory columns, then one thread copies each
-//               stage's scales into tensor memory (tcgen05.cp) and issues the
-//               block-scaled MMAs (kind::mxf4nvf4 or kind::mxf8f6f4, M=128,
-//               N=256) into a 128 x 256 fp32 accumulator;
-//   warps 2-9   epilogue: tcgen05.ld the accumulator (each warp a 32-lane
-//               quarter and half of the columns) into registers, release it to
-//               the MMA warp, then apply the per-token and per-column FP32
-//               scales (forward), round to bf16 and store the rows that belong
-//               to the expert, overlapping the next tile's MMAs.
-// Tiles are 128 rows x 256 columns.  Every role walks the same tile sequence,
-// derived in shared memory from the per-expert offsets: forward and dgrad go
-// expert by expert, 128-row blocks of each expert's rows, 256-column blocks
-// fastest; wgrad goes expert by expert in decreasing order of work (largest
-// contraction first) and writes zeros for experts without rows.  There is no
-// split over K: each output element is one accumulation in one CTA, so a row's
-// result does not depend on other rows.
+// One persistent kernel per call.  CTAs run in pairs (a cluster of 2 on two
+// SMs); a pair computes 256 x 256 output tiles with cta_group::2 MMAs (M = 256:
+// 128 rows in each CTA's tensor memory).  Each CTA stages its own 128 rows of A
+// and its half (128 rows) of the tile's 256 B rows, so a pair moves 1.5x fewer
+// operand bytes per flop than a single CTA with a 128 x 256 tile, and each
+// scale copy into tensor memory serves twice the MMA work.  10 warps per CTA:
+//   warp 0      TMA producer (both CTAs): A, B and their scale tiles into a
+//               5-6 stage ring; every copy of the pair completes on the leader
+//               CTA's "full" barrier;
+//   warp 1      allocates 512 tensor-memory columns in both CTAs together; in the
+//               leader, one thread copies each stage's scales into tensor memory
+//               (tcgen05.cp) and issues the block-scaled MMAs (kind::mxf4nvf4 or
+//               kind::mxf8f6f4, M = 256, N = 256); commits free the stage in both
+//               CTAs and, at the end of a tile, fill both CTAs' accumulators;
+//   warps 2-9   epilogue (both CTAs): tcgen05.ld its own 128 x 256 fp32
+//               accumulator (each warp a 32-lane quarter and half the columns)
+//               into registers, release it to the leader, then apply the
+//               per-token and per-column FP32 scales (forward), round to bf16 and
+//               store the rows that belong to the expert, overlapping the next
+//               tile's MMAs.
+// Both CTAs walk the same tile sequence, derived in shared memory from the
+// per-expert offsets: forward and dgrad go expert by expert, 256-row blocks of
+// each expert's rows, 256-column blocks fastest; wgrad goes expert by expert in
+// decreasing order of work (largest contraction first) and writes zeros for
+// experts without rows.  There is no split over K: each output element is one
+// accumulation, so a row's result does not depend on other rows.
 #include "fme_device.cuh"
 #include "fme_launch.h"
 
 namespace fme {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBM = 128;           // rows per CTA
+constexpr int kPairM = 256;        // rows per pair tile
+constexpr int kBN = 256;           // columns per tile
+constexpr int kHalfN = kBN / 2;    // B rows staged by each CTA
 constexpr int kStageKBytes = 128;  // bytes of K per row per stage (one swizzle row)
-constexpr int kStages = 4;
-constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
-constexpr int kAccCols = kBN;
+constexpr int kThreads = 320;      // producer, MMA, 8 epilogue warps
+constexpr int kMaxStages = 6;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kStageKBytes;
-constexpr int kBBytes = kBN * kStageKBytes;
+constexpr int kBBytes = kHalfN * kStageKBytes;
+constexpr int kAccEmptyArrivals = 2 * 8;  // one per epilogue warp of the pair
 
 template <GemmKind K>
 struct Cfg {
   static constexpr bool kFp4 = (K == GemmKind::kFwdNvfp4);
-  static constexpr int kKPerStage = kFp4 ? 256 : 128;    // elements of K per stage
-  static constexpr int kAtoms = kFp4 ? 4 : 1;            // 512-byte scale tiles per 128 rows per stage
-  static constexpr int kSfaBytes = 512 * kAtoms;
-  static constexpr int kSfbBytes = 2 * 512 * kAtoms;     // two 128-row halves of the N tile
-  static constexpr int kSfaCols = 4 * kAtoms;            // tensor-memory columns per stage
+  static constexpr int kKPerStage = kFp4 ? 256 : 128;  // elements of K per stage
+  static constexpr int kAtoms = kFp4 ? 4 : 1;          // 512-byte scale tiles per 128 rows per stage
+  static constexpr int kSfaBytes = 512 * kAtoms;       // this CTA's 128 rows
+  static constexpr int kSfbBytes = 2 * 512 * kAtoms;   // all 256 B rows of the tile
+  static constexpr int kSfaCols = 4 * kAtoms;          // tensor-memory columns per stage
   static constexpr int kSfbCols = 8 * kAtoms;
   static constexpr int kSfCols = kSfaCols + kSfbCols;
-  static constexpr int kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kSmemBytes = kStages * kStageTx + 1024;  // + alignment slack
-  static_assert(kAccCols + 2 * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
+  static constexpr int kStages = kFp4 ? 5 : 6;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStageTx = 2 * kStageBytes;  // both CTAs' copies land on the leader's barrier
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+  static_assert(kStages <= kMaxStages, "stage count");
+  static_assert(kBN + 2 * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
 };
 
 struct SharedState {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
   int ok_flag;
-  // fwd, dgrad: groups.off = row offsets, groups.tiles = 128-row tile prefix.
-  // wgrad: groups.off = padded offsets, groups.tiles = experts by decreasing work.
+  // fwd, dgrad: groups.off = row offsets, groups.tiles = 128-row tile prefix,
+  //             pair_tiles = 256-row tile prefix.
+  // wgrad:      groups.off = padded offsets, groups.tiles = experts by decreasing work.
   GroupTable groups;
+  int32_t pair_tiles[kMaxGroups + 1];
 };
 
 struct Tile {
   int32_t e;
-  int32_t num_k;       // K stages; 0 = expert without rows (wgrad): output zeros
-  int32_t rows_valid;  // rows of the tile that belong to the expert
-  int64_t y_off;       // element offset of the tile's first output element
-  int32_t a_y, b_y;    // TMA row coordinates
-  int32_t a_x0, b_x0;  // TMA K coordinates (bytes) of the first stage
-  int64_t sfa0;        // byte offset of A's scales for the first stage
-  int64_t sfb0;        // byte offset of B's scales (first 128-row half) for the first stage
-  int32_t n0;          // first output column
+  int32_t num_k;           // K stages; 0 = expert without rows (wgrad): output zeros
+  int32_t rows_valid;      // rows of this CTA's 128 that belong to the expert (may be <= 0)
+  int64_t y_off;           // element offset of this CTA's first output element
+  int32_t a_y, b_y;        // TMA row coordinates of this CTA's A rows and B half
+  int32_t a_x0, b_x0;      // TMA K coordinates (bytes) of the first stage
+  int32_t sfa_row;         // 128-row scale block of this CTA's A rows
+  int32_t sfb_row;         // first of the two 128-row scale blocks of the tile's B rows
+  int32_t sfa_x0, sfb_x0;  // 512-byte scale tile index of the first stage
+  int32_t n0;              // first output column
 };
 
 template <GemmKind K>
 __device__ __forceinline__ int64_t total_tiles(const LaunchGemm &p, const SharedState &s) {
   const int64_t nb = p.n / kBN;
-  if (K == GemmKind::kWgradMxfp8) return static_cast<int64_t>(p.num_experts) * (p.m / kBM) * nb;
-  return static_cast<int64_t>(s.groups.tiles[p.num_experts]) * nb;
+  if (K == GemmKind::kWgradMxfp8) return static_cast<int64_t>(p.num_experts) * (p.m / kPairM) * nb;
+  return static_cast<int64_t>(s.pair_tiles[p.num_experts]) * nb;
 }
 
 template <GemmKind K>
-__device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const SharedState &s, int64_t t) {
+__device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const SharedState &s, int64_t t, int rank) {
   using C = Cfg<K>;
   Tile tl;
   const int64_t nb_count = p.n / kBN;
   if (K == GemmKind::kWgradMxfp8) {
-    const int64_t mb_count = p.m / kBM;
+    const int64_t mb_count = p.m / kPairM;
     const int64_t per = mb_count * nb_count;
-    const int rank = static_cast<int>(t / per);
+    const int order = static_cast<int>(t / per);
     const int64_t rem = t % per;
     const int64_t mb = rem / nb_count;
     const int64_t nb = rem % nb_count;
-    const int e = s.groups.tiles[rank];
+    const int e = s.groups.tiles[order];
     const int32_t p0 = s.groups.off[e];
+    const int64_t row0 = mb * kPairM + rank * kBM;
     tl.e = e;
     tl.num_k = (s.groups.off[e + 1] - p0) / 128;
     tl.rows_valid = kBM;
     tl.n0 = static_cast<int32_t>(nb * kBN);
-    tl.y_off = (static_cast<int64_t>(e) * p.m + mb * kBM) * p.n + nb * kBN;
-    tl.a_y = static_cast<int32_t>(mb * kBM);
-    tl.b_y = static_cast<int32_t>(nb * kBN);
+    tl.y_off = (static_cast<int64_t>(e) * p.m + row0) * p.n + nb * kBN;
+    tl.a_y = static_cast<int32_t>(row0);
+    tl.b_y = static_cast<int32_t>(nb * kBN + rank * kHalfN);
     tl.a_x0 = p0;
     tl.b_x0 = p0;
-    tl.sfa0 = mb * p.sfa_stride + static_cast<int64_t>(p0 / 128) * 512;
-    tl.sfb0 = (2 * nb) * p.sfb_stride + static_cast<int64_t>(p0 / 128) * 512;
+    tl.sfa_row = static_cast<int32_t>(row0 / 128);
+    tl.sfb_row = static_cast<int32_t>(2 * nb);
+    tl.sfa_x0 = p0 / 128;
+    tl.sfb_x0 = p0 / 128;
   } else {
     const int64_t g = t / nb_count;
     const int64_t nb = t % nb_count;
-    const int e = find_group(s.groups.tiles, p.num_experts, g);
-    const int64_t mt = g - s.groups.tiles[e];
-    const int64_t r0 = s.groups.off[e] + mt * kBM;
+    const int e = find_group(s.pair_tiles, p.num_experts, g);
+    const int64_t mb = 2 * (g - s.pair_tiles[e]) + rank;  // this CTA's 128-row block within the expert
+    const int64_t r0 = s.groups.off[e] + mb * kBM;
     const int64_t n_e = s.groups.off[e + 1] - s.groups.off[e];
+    const int64_t left = n_e - mb * kBM;
     tl.e = e;
     tl.num_k = static_cast<int32_t>(p.k / C::kKPerStage);
-    tl.rows_valid = static_cast<int32_t>(n_e - mt * kBM < kBM ? n_e - mt * kBM : kBM);
+    tl.rows_valid = static_cast<int32_t>(left < kBM ? left : kBM);
     tl.n0 = static_cast<int32_t>(nb * kBN);
     tl.y_off = r0 * p.n + nb * kBN;
     tl.a_y = static_cast<int32_t>(r0);
     tl.a_x0 = 0;
-    tl.sfa0 = g * p.sfa_stride;  // padded row block of this tile = tiles[e] + mt = g
+    tl.sfa_row = s.groups.tiles[e] + static_cast<int32_t>(mb);
+    tl.sfa_x0 = 0;
     if (K == GemmKind::kFwdNvfp4) {
       const int64_t brow = static_cast<int64_t>(e) * p.n + nb * kBN;
-      tl.b_y = static_cast<int32_t>(brow);
+      tl.b_y = static_cast<int32_t>(brow + rank * kHalfN);
       tl.b_x0 = 0;
-      tl.sfb0 = (brow / 128) * p.sfb_stride;
+      tl.sfb_row = static_cast<int32_t>(brow / 128);
+      tl.sfb_x0 = 0;
     } else {
-      tl.b_y = static_cast<int32_t>(nb * kBN);
+      tl.b_y = static_cast<int32_t>(nb * kBN + rank * kHalfN);
       tl.b_x0 = static_cast<int32_t>(static_cast<int64_t>(e) * p.k);
-      tl.sfb0 = (2 * nb) * p.sfb_stride + (static_cast<int64_t>(e) * p.k / 128) * 512;
+      tl.sfb_row = static_cast<int32_t>(2 * nb);
+      tl.sfb_x0 = static_cast<int32_t>(static_cast<int64_t>(e) * p.k / 128);
     }
   }
   return tl;
 }
 
-// Build the tile tables; returns false (in every thread) for malformed offsets.
+// Build the tile tables (the same in both CTAs of a pair); returns false in
+// every thread for malformed offsets.
 template <GemmKind K>
 __device__ bool prepare(const LaunchGemm &p, SharedState &s) {
-  if (K != GemmKind::kWgradMxfp8) return load_groups(s.groups, p.offsets, p.num_experts, p.m, &s.ok_flag);
+  if (K != GemmKind::kWgradMxfp8) {
+    if (!load_groups(s.groups, p.offsets, p.num_experts, p.m, &s.ok_flag)) return false;
+    if (threadIdx.x == 0) {
+      int32_t acc = 0;
+      for (int e = 0; e < p.num_experts; ++e) {
+        s.pair_tiles[e] = acc;
+        acc += (s.groups.off[e + 1] - s.groups.off[e] + kPairM - 1) / kPairM;
+      }
+      s.pair_tiles[p.num_experts] = acc;
+    }
+    __syncthreads();
+    return true;
+  }
   // wgrad: padded offsets, multiples of 128, rising from 0 within both operands
   if (threadIdx.x == 0) {
     bool ok = true;
@@ -209,37 +244,45 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   extern __shared__ uint8_t dyn_smem[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   uint8_t *smem_a = smem;
-  uint8_t *smem_b = smem_a + kStages * kABytes;
-  uint8_t *smem_sfa = smem_b + kStages * kBBytes;
-  uint8_t *smem_sfb = smem_sfa + kStages * C::kSfaBytes;
+  uint8_t *smem_b = smem_a + C::kStages * kABytes;
+  uint8_t *smem_sfa = smem_b + C::kStages * kBBytes;
+  uint8_t *smem_sfb = smem_sfa + C::kStages * C::kSfaBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(pair::cta_rank());
+  const int64_t pair_id = blockIdx.x >> 1;
+  const int64_t pairs = gridDim.x >> 1;
 
+  // Both CTAs of a pair see the same offsets, so both return here or neither does.
   if (!prepare<K>(p, s)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(p.status, kDevBadOffsets);
     return;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
     mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 8 * 32);
+    mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
     prefetch_tensormap(&p.map_a);
     prefetch_tensormap(&p.map_b);
+    prefetch_tensormap(&p.map_sfa);
+    prefetch_tensormap(&p.map_sfb);
   }
   if (warp == 1) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
-    tmem_relinquish();
+    pair::tmem_alloc(&s.tmem_base, kTmemCols);
+    pair::tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
+  __syncwarp();
+  pair::cluster_sync();  // both CTAs' barriers exist before any copy or arrive crosses the pair
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   volatile int *abort_flag = &s.abort_flag;
@@ -248,48 +291,36 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
     uint32_t stage = 0, phase = 0;
-    bool issued_any[kStages] = {};
-    uint32_t issued_phase[kStages] = {};
-    bool stop = false;
-    for (int64_t t = blockIdx.x; t < total && !stop; t += gridDim.x) {
-      const Tile tl = tile_at<K>(p, s, t);
+    for (int64_t t = pair_id; t < total; t += pairs) {
+      const Tile tl = tile_at<K>(p, s, t, rank);
+      bool stop = false;
       for (int ks = 0; ks < tl.num_k; ++ks) {
         if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.status)) {
           stop = true;
           break;
         }
-        mbar_arrive_expect_tx(&s.full[stage], C::kStageTx);
-        tma_load_2d(smem_a + stage * kABytes, &p.map_a, &s.full[stage], tl.a_x0 + ks * kStageKBytes, tl.a_y);
-        tma_load_2d(smem_b + stage * kBBytes, &p.map_b, &s.full[stage], tl.b_x0 + ks * kStageKBytes, tl.b_y);
-        bulk_load(smem_sfa + stage * C::kSfaBytes, p.sfa + tl.sfa0 + static_cast<int64_t>(ks) * C::kSfaBytes,
-                  C::kSfaBytes, &s.full[stage]);
-        const uint8_t *sfb_src = p.sfb + tl.sfb0 + static_cast<int64_t>(ks) * (C::kSfbBytes / 2);
-        bulk_load(smem_sfb + stage * C::kSfbBytes, sfb_src, C::kSfbBytes / 2, &s.full[stage]);
-        bulk_load(smem_sfb + stage * C::kSfbBytes + C::kSfbBytes / 2, sfb_src + p.sfb_stride, C::kSfbBytes / 2,
-                  &s.full[stage]);
-        issued_any[stage] = true;
-        issued_phase[stage] = phase;
-        if (++stage == kStages) {
+        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], C::kStageTx);
+        const uint32_t bar = pair::map_to_rank(&s.full[stage], 0);
+        pair::tma_load_2d(smem_a + stage * kABytes, &p.map_a, bar, tl.a_x0 + ks * kStageKBytes, tl.a_y);
+        pair::tma_load_2d(smem_b + stage * kBBytes, &p.map_b, bar, tl.b_x0 + ks * kStageKBytes, tl.b_y);
+        pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, bar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
+                          tl.sfa_row);
+        pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
+                          tl.sfb_row);
+        if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
         }
       }
+      if (stop) break;
     }
-    if (stop) {  // let copies in flight land before the CTA exits
-      for (int i = 0; i < kStages; ++i)
-        if (issued_any[i]) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&s.full[i], issued_phase[i]) && globaltimer() - t0 < kWaitLimitNs / 4) {
-          }
-        }
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------ MMA issuer (leader)
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool stop = false;
-    const uint32_t sf_base = tmem + kAccCols;
-    for (int64_t t = blockIdx.x; t < total && !stop; t += gridDim.x) {
-      const Tile tl = tile_at<K>(p, s, t);
+    const uint32_t sf_base = tmem + kBN;
+    for (int64_t t = pair_id; t < total && !stop; t += pairs) {
+      const Tile tl = tile_at<K>(p, s, t, 0);
       if (tl.num_k == 0) continue;
       if (!mbar_wait(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
       tc_fence_after();
@@ -307,9 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
 #pragma unroll
         for (int i = 0; i < C::kAtoms; ++i) {
-          tc_copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
-          tc_copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
-          tc_copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+          pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
+          pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
+          pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -317,41 +348,39 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const uint64_t bd = desc_sw128_kmajor(b_s + kk * 32);
           const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
           if (C::kFp4)
-            mma_nvf4(tmem, ad, bd, idesc_nvf4(kBN), sfa_t + 4 * kk, sfb_t + 8 * kk, acc);
+            pair::mma_nvf4(tmem, ad, bd, pair::idesc_nvf4(kBN), sfa_t + 4 * kk, sfb_t + 8 * kk, acc);
           else
-            mma_mxf8(tmem, ad, bd, idesc_mxf8(kBN, kk), sfa_t, sfb_t, acc);
+            pair::mma_mxf8(tmem, ad, bd, pair::idesc_mxf8(kBN, kk), sfa_t, sfb_t, acc);
         }
-        tc_commit(&s.empty[stage]);
-        if (++stage == kStages) {
+        pair::commit_both(&s.empty[stage]);
+        if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (stop) break;
-      tc_commit(&s.acc_full);
+      pair::commit_both(&s.acc_full);
       acc_phase ^= 1;
     }
-    // every tensor-core operation of this CTA has finished before memory is released
-    tc_commit(&s.drain);
-    {
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
-      }
+    // every tensor-core operation of the pair has finished before memory is released
+    pair::commit_local(&s.drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
   } else if (warp >= 2) {
     // --------------------------------------------------------------- epilogue
-    // 8 warps: warp w reads tensor-memory lane quarter w % 4 (rows 32(w%4) ..
-    // +31) and column half (w - 2) / 4.  All 128 accumulator columns of a thread
-    // are loaded before the accumulator is released to the MMA warp, so the next
-    // tile's MMAs run while this tile is scaled, rounded and stored.
+    // Warp w reads tensor-memory lane quarter w % 4 (rows 32(w%4) .. +31) and
+    // column half (w - 2) / 4.  All 128 accumulator columns of a thread are
+    // loaded before the accumulator is released to the leader.
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const int c0 = half * (kBN / 2);
+    const uint32_t leader_acc_empty = pair::map_to_rank(&s.acc_empty, 0);
     uint32_t acc_phase = 0;
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = tile_at<K>(p, s, t);
+    for (int64_t t = pair_id; t < total; t += pairs) {
+      const Tile tl = tile_at<K>(p, s, t, rank);
       const bool valid = r < tl.rows_valid;
       __nv_bfloat16 *yrow = y + tl.y_off + static_cast<int64_t>(r) * p.n + c0;
       if (tl.num_k == 0) {
@@ -369,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       tmem_ld_32x32(taddr + 96, v3);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&s.acc_empty);
+      __syncwarp();
+      if (lane == 0) pair::arrive_remote(leader_acc_empty);
       acc_phase ^= 1;
       float sa = 1.0f;
       const float *sb_row = nullptr;
@@ -386,12 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   }
 
+  // Teardown: the pair meets once the leader's MMAs are drained and every
+  // epilogue has read its accumulator; then both CTAs free tensor memory together.
   tc_fence_before();
   __syncthreads();
+  __syncwarp();
+  pair::cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem, kTmemCols);
+    pair::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -403,13 +437,24 @@ static cudaError_t launch_kind(const LaunchGemm &a) {
   if (err != cudaSuccess) return err;
   int64_t bound;
   if (K == GemmKind::kWgradMxfp8)
-    bound = static_cast<int64_t>(a.num_experts) * (a.m / kBM) * (a.n / kBN);
+    bound = static_cast<int64_t>(a.num_experts) * (a.m / kPairM) * (a.n / kBN);
   else
-    bound = (a.m / kBM + a.num_experts) * (a.n / kBN);
-  int grid = a.num_sms;
-  if (bound < grid) grid = static_cast<int>(bound > 0 ? bound : 1);
-  grouped_gemm_kernel<K><<<grid, kThreads, C::kSmemBytes, a.stream>>>(a);
-  return cudaGetLastError();
+    bound = (a.m / kPairM + a.num_experts) * (a.n / kBN);
+  int pairs = a.num_sms / 2;
+  if (bound < pairs) pairs = static_cast<int>(bound > 0 ? bound : 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<K>, a);
 }
 
 cudaError_t launch_grouped_gemm(const LaunchGemm &a) {

@@ -58,29 +58,36 @@ __device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
   return r & 0xFFu;
 }
 
-// E2M1 codes of the correctly rounded quotients fl32(x0/e), fl32(x1/e) (x0 in the
-// low nibble), without dividing unless a quotient sits next to a rounding
+// E2M1 codes of the correctly rounded quotients fl32(x.x/e), fl32(x.y/e) (x.x in
+// the low nibble), without dividing unless a quotient sits next to a rounding
 // boundary of the E2M1 grid.
 //
-// With r = fl32(1/e) (correctly rounded) and e a normal fp32, q = fl32(x r)
-// differs from the exact x/e by less than 2^-22.9 relative, and Q = fl32(x/e) by
-// less than 2^-24, so Q lies strictly between fl32(q (1 - 2^-19)) and
-// fl32(q (1 + 2^-19)).  Rounding to the E2M1 grid is monotone in |v| (same sign
-// throughout), so when both ends round to the same code Q does too.  Otherwise
-// (a quotient within 2^-19 of a grid midpoint, e.g. an exact tie) the code comes
-// from the IEEE quotient itself.  Quotients far below 0.25 round to (signed) zero
-// on every path.  The result is always the code of fl32(x/e).
-__device__ __forceinline__ uint32_t e2m1_codes_of_quotients(float x0, float x1, float e, float r, bool normal_e) {
+// With r an approximate reciprocal of a normal fp32 e (rcp.approx: within 2^-22
+// relative), q = fl32(x r) differs from the exact x/e by less than 2^-21.7
+// relative, and Q = fl32(x/e) by less than 2^-24, so Q lies strictly between
+// fl32(q (1 - 2^-19)) and fl32(q (1 + 2^-19)).  Rounding to the E2M1 grid is
+// monotone in |v| (same sign throughout), so when both ends round to the same
+// code, Q does too.  Otherwise (a quotient within about 2^-19 of a grid midpoint,
+// e.g. an exact tie) the codes come from the IEEE quotients themselves.
+// Quotients far below 0.25 round to (signed) zero on every path.  The result is
+// always the code of fl32(x/e).  Pairs go through the packed f32x2 multiplier.
+__device__ __forceinline__ uint32_t e2m1_codes_of_quotients(float2 x, float e, float r, bool normal_e) {
   constexpr float kBelow = 1.0f - 1.0f / 524288.0f;  // 1 - 2^-19, exact in fp32
   constexpr float kAbove = 1.0f + 1.0f / 524288.0f;  // 1 + 2^-19
   if (normal_e) {
-    const float q0 = __fmul_rn(x0, r);
-    const float q1 = __fmul_rn(x1, r);
-    const uint32_t lo = e2m1_pair(__fmul_rn(q0, kBelow), __fmul_rn(q1, kBelow));
-    const uint32_t hi = e2m1_pair(__fmul_rn(q0, kAbove), __fmul_rn(q1, kAbove));
-    if (lo == hi) return lo;
+    const float2 q = __fmul2_rn(x, make_float2(r, r));
+    const float2 lo = __fmul2_rn(q, make_float2(kBelow, kBelow));
+    const float2 hi = __fmul2_rn(q, make_float2(kAbove, kAbove));
+    const uint32_t clo = e2m1_pair(lo.x, lo.y);
+    if (clo == e2m1_pair(hi.x, hi.y)) return clo;
   }
-  return e2m1_pair(__fdiv_rn(x0, e), __fdiv_rn(x1, e));
+  return e2m1_pair(__fdiv_rn(x.x, e), __fdiv_rn(x.y, e));
+}
+
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 // Row split: WPR warps share one row; warp w of the row takes chunks w, w + WPR,
@@ -163,13 +170,12 @@ __global__ void __launch_bounds__(kNvThreads, 3) nvfp4_pertoken_kernel(const uin
       uint32_t packed = 0;
       if (sb != 0) {
         const float e = __fmul_rn(e4m3_value(sb), s_t);
-        const float r = __frcp_rn(e);
-        const bool normal_e = e >= 1.17549435e-38f;  // 1/e finite
+        const bool normal_e = e >= 1.17549435e-38f;  // reciprocal finite and accurate
+        const float r = rcp_approx(e);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float x0 = __uint_as_float(w[i] << 16);
-          const float x1 = __uint_as_float(w[i] & 0xFFFF0000u);
-          packed |= e2m1_codes_of_quotients(x0, x1, e, r, normal_e) << (8 * i);
+          const float2 xp = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+          packed |= e2m1_codes_of_quotients(xp, e, r, normal_e) << (8 * i);
         }
       }
       if (col < k) *reinterpret_cast<uint32_t *>(codes_row + col / 2) = packed;
