@@ -85,8 +85,8 @@ def test_host_argument_checks(lib):
     assert d(good, good, good, good, 2048, good, 4, 100, 256, 96, good, None, _stream()) == 3
     w = lib.grouped_gemm_wgrad_mxfp8
     assert w(good, good, 128, good, good, 128, good, 4, 100, 256, good, None, _stream()) == 3
-    assert w(good, good, 128, good, good, 128, good, 4, 128, 128, good, None, _stream()) == 3
-    assert w(good, good, 128, good, good, 128, None, 4, 128, 256, good, None, _stream()) == 1
+    assert w(good, good, 128, good, good, 128, good, 4, 128, 256, good, None, _stream()) == 3  # m % 256
+    assert w(good, good, 128, good, good, 128, None, 4, 256, 256, good, None, _stream()) == 1
     assert lib.fme_read_device_status(None, _stream(), None) == 1
 
 
