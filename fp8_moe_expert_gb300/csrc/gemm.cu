@@ -12,15 +12,16 @@
 // 128 rows in each CTA's tensor memory).  Each CTA stages its own 128 rows of A
 // and its half (128 rows) of the tile's 256 B rows, so a pair moves 1.5x fewer
 // operand bytes per flop than a single CTA with a 128 x 256 tile, and each
-// scale copy into tensor memory serves twice the MMA work.  10 warps per CTA:
+// scale copy into tensor memory serves twice the MMA work.  11 warps per CTA:
 //   warp 0      TMA producer (both CTAs): A, B and their scale tiles into a
 //               5-6 stage ring; every copy of the pair completes on the leader
 //               CTA's "full" barrier;
 //   warp 1      allocates 512 tensor-memory columns in both CTAs together; in the
-//               leader, one thread copies each stage's scales into tensor memory
-//               (tcgen05.cp) and issues the block-scaled MMAs (kind::mxf4nvf4 or
-//               kind::mxf8f6f4, M = 256, N = 256); commits free the stage in both
-//               CTAs and, at the end of a tile, fill both CTAs' accumulators;
+//               leader, one thread issues the block-scaled MMAs (kind::mxf4nvf4
+//               or kind::mxf8f6f4, M = 256, N = 256); commits free the stage in
+//               both CTAs and, at the end of a tile, fill both CTAs' accumulators;
+//   warp 10     in the leader, one thread copies each stage's scales into a ring
+//               of 4 tensor-memory buffers (tcgen05.cp) ahead of the MMAs;
 //   warps 2-9   epilogue (both CTAs): tcgen05.ld its own 128 x 256 fp32
 //               accumulator (each warp a 32-lane quarter and half the columns)
 //               into registers, release it to the leader, then apply the
@@ -43,7 +44,9 @@ constexpr int kPairM = 256;        // rows per pair tile
 constexpr int kBN = 256;           // columns per tile
 constexpr int kHalfN = kBN / 2;    // B rows staged by each CTA
 constexpr int kStageKBytes = 128;  // bytes of K per row per stage (one swizzle row)
-constexpr int kThreads = 320;      // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 352;      // producer, MMA, 8 epilogue warps, scale copier
+constexpr int kCopierWarp = 10;
+constexpr int kSfBuffers = 4;      // tensor-memory scale buffers between the copier and the MMA issuer
 constexpr int kMaxStages = 6;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kStageKBytes;
@@ -65,15 +68,18 @@ struct Cfg {
   static constexpr int kStageTx = 2 * kStageBytes;  // both CTAs' copies land on the leader's barrier
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   static_assert(kStages <= kMaxStages, "stage count");
-  static_assert(kBN + 2 * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
+  static_assert(kBN + kSfBuffers * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
 };
 
 struct SharedState {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b
+  uint64_t sf_empty[kSfBuffers];  // the MMAs reading buffer b are done
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
+  uint64_t drain2;
   uint32_t tmem_base;
   int abort_flag;
   int ok_flag;
@@ -264,9 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
+    for (int i = 0; i < kSfBuffers; ++i) {
+      mbar_init(&s.sf_full[i], 1);
+      mbar_init(&s.sf_empty[i], 1);
+    }
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.drain2, 1);
     s.abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -316,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------ MMA issuer (leader)
-    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    uint32_t stage = 0, phase = 0, acc_phase = 0, buf = 0, buf_phase = 0;
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
@@ -325,23 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       if (!mbar_wait(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
       tc_fence_after();
       for (int ks = 0; ks < tl.num_k; ++ks) {
-        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status)) {
+        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
+            !mbar_wait(&s.sf_full[buf], buf_phase, abort_flag, p.status)) {
           stop = true;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa_t = sf_base + (ks & 1) * C::kSfCols;
+        const uint32_t sfa_t = sf_base + buf * C::kSfCols;
         const uint32_t sfb_t = sfa_t + C::kSfaCols;
         const uint32_t a_s = smem_u32(smem_a + stage * kABytes);
         const uint32_t b_s = smem_u32(smem_b + stage * kBBytes);
-        const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
-        const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
-#pragma unroll
-        for (int i = 0; i < C::kAtoms; ++i) {
-          pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
-          pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
-          pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
-        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t ad = desc_sw128_kmajor(a_s + kk * 32);
@@ -353,9 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             pair::mma_mxf8(tmem, ad, bd, pair::idesc_mxf8(kBN, kk), sfa_t, sfb_t, acc);
         }
         pair::commit_both(&s.empty[stage]);
+        pair::commit_local(&s.sf_empty[buf]);
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
+        }
+        if (++buf == kSfBuffers) {
+          buf = 0;
+          buf_phase ^= 1;
         }
       }
       if (stop) break;
@@ -367,7 +376,49 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
-  } else if (warp >= 2) {
+  } else if (warp == kCopierWarp && lane == 0 && rank == 0) {
+    // ---------------------------------------------------- scale copier (leader)
+    // Copies each stage's scale tiles (both CTAs, tcgen05.cp.cta_group::2) into
+    // the next free tensor-memory buffer while the MMA issuer works on earlier
+    // stages, then signals the buffer full.
+    uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
+    bool stop = false;
+    const uint32_t sf_base = tmem + kBN;
+    for (int64_t t = pair_id; t < total && !stop; t += pairs) {
+      const Tile tl = tile_at<K>(p, s, t, 0);
+      for (int ks = 0; ks < tl.num_k; ++ks) {
+        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
+            !mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa_t = sf_base + buf * C::kSfCols;
+        const uint32_t sfb_t = sfa_t + C::kSfaCols;
+        const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
+        const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
+#pragma unroll
+        for (int i = 0; i < C::kAtoms; ++i) {
+          pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
+          pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
+          pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+        }
+        pair::commit_local(&s.sf_full[buf]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++buf == kSfBuffers) {
+          buf = 0;
+          buf_phase ^= 1;
+        }
+      }
+    }
+    pair::commit_local(&s.drain2);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&s.drain2, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
+    }
+  } else if (warp >= 2 && warp < kCopierWarp) {
     // --------------------------------------------------------------- epilogue
     // Warp w reads tensor-memory lane quarter w % 4 (rows 32(w%4) .. +31) and
     // column half (w - 2) / 4.  All 128 accumulator columns of a thread are
