@@ -21,6 +21,13 @@ __device__ __forceinline__ uint32_t mx_code_from_bf16_amax(uint32_t amax_bits) {
 // 2^(127 - code) as an fp32 (code in [0, 246] for bf16 inputs: always normal).
 __device__ __forceinline__ float mx_inv_scale(uint32_t code) { return __uint_as_float((254u - code) << 23); }
 
+// Per-halfword unsigned max of two words of packed bf16 magnitudes.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Two E4M3 codes: `lo` in bits 0..7, `hi` in bits 8..15.
 __device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
   uint16_t r;
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
 // ------------------------------------------------------------- column-wise --
 // Tile = 128 padded positions (one 128-chunk of one group) x 128 columns.  The
 // CTA stages the 128 x 128 bf16 tile in shared memory (rows past the group's end
-// read as zeros), each thread quantizes two 32-blocks of one column, the codes
+// read as zeros), each thread quantizes one 32-block of two adjacent columns, the codes
 // are staged transposed and leave as 128-byte rows, and the 128 x 4 scales of
 // the tile are exactly one 512-byte tile of the scale layout.
 constexpr int kColTilePad = 8;  // bf16 elements of padding per staged row
@@ -173,26 +180,33 @@ __global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restr
     __syncthreads();
     if (t + gridDim.x < total) load_tile(t + gridDim.x, pre);
 
-    const int c = tid & 127;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int b = (tid >> 7) + 2 * h;
+    // thread = (channel pair cp, 32-position block b): both channels' 32 values
+    // come in with one 32-bit shared load per position
+    {
+      const int cp = tid & 63;
+      const int b = tid >> 6;
       uint32_t vals[32];
-      uint32_t bmax = 0;
+      uint32_t m = 0;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        vals[i] = tile[32 * b + i][c];
-        bmax = max(bmax, vals[i] & 0x7FFFu);
+        vals[i] = *reinterpret_cast<const uint32_t *>(&tile[32 * b + i][2 * cp]);
+        m = max_u16x2(m, vals[i] & 0x7FFF7FFFu);
       }
-      const uint32_t code = mx_code_from_bf16_amax(bmax);
-      const float s = mx_inv_scale(code);
-      uint32_t words[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        words[q] = quad_codes(vals[4 * q] | (vals[4 * q + 1] << 16), vals[4 * q + 2] | (vals[4 * q + 3] << 16), s);
-      *reinterpret_cast<uint4 *>(&outq[c][32 * b]) = make_uint4(words[0], words[1], words[2], words[3]);
-      *reinterpret_cast<uint4 *>(&outq[c][32 * b + 16]) = make_uint4(words[4], words[5], words[6], words[7]);
-      sfs[(c & 31) * 16 + (c >> 5) * 4 + b] = static_cast<uint8_t>(code);
+      for (int h = 0; h < 2; ++h) {
+        const int c = 2 * cp + h;
+        const uint32_t code = mx_code_from_bf16_amax(h ? (m >> 16) : (m & 0xFFFFu));
+        const float s = mx_inv_scale(code);
+        const uint32_t sel = h ? 0x7632u : 0x5410u;  // high or low halves of two words
+        uint32_t words[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          words[q] = quad_codes(__byte_perm(vals[4 * q], vals[4 * q + 1], sel),
+                                __byte_perm(vals[4 * q + 2], vals[4 * q + 3], sel), s);
+        *reinterpret_cast<uint4 *>(&outq[c][32 * b]) = make_uint4(words[0], words[1], words[2], words[3]);
+        *reinterpret_cast<uint4 *>(&outq[c][32 * b + 16]) = make_uint4(words[4], words[5], words[6], words[7]);
+        sfs[(c & 31) * 16 + (c >> 5) * 4 + b] = static_cast<uint8_t>(code);
+      }
     }
     __syncthreads();
 

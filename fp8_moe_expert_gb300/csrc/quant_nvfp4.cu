@@ -58,30 +58,46 @@ __device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
   return r & 0xFFu;
 }
 
-// E2M1 codes of the correctly rounded quotients fl32(x.x/e), fl32(x.y/e) (x.x in
-// the low nibble), without dividing unless a quotient sits next to a rounding
-// boundary of the E2M1 grid.
+// E2M1 codes of the correctly rounded quotients fl32(x_i/e) of 8 bf16 values
+// (4 words, element 2i in the low half of word i), packed two per byte with the
+// even element in the low nibble, without dividing unless a quotient sits next
+// to a rounding boundary of the E2M1 grid.
 //
 // With r an approximate reciprocal of a normal fp32 e (rcp.approx: within 2^-22
 // relative), q = fl32(x r) differs from the exact x/e by less than 2^-21.7
 // relative, and Q = fl32(x/e) by less than 2^-24, so Q lies strictly between
 // fl32(q (1 - 2^-19)) and fl32(q (1 + 2^-19)).  Rounding to the E2M1 grid is
 // monotone in |v| (same sign throughout), so when both ends round to the same
-// code, Q does too.  Otherwise (a quotient within about 2^-19 of a grid midpoint,
-// e.g. an exact tie) the codes come from the IEEE quotients themselves.
-// Quotients far below 0.25 round to (signed) zero on every path.  The result is
-// always the code of fl32(x/e).  Pairs go through the packed f32x2 multiplier.
-__device__ __forceinline__ uint32_t e2m1_codes_of_quotients(float2 x, float e, float r, bool normal_e) {
+// code, Q does too.  If that fails for any of the 8 values (a quotient within
+// about 2^-19 of a grid midpoint, e.g. an exact tie), all 8 codes come from the
+// IEEE quotients themselves.  Quotients far below 0.25 round to (signed) zero on
+// every path.  The result is always the codes of fl32(x/e).  Pairs go through
+// the packed f32x2 multiplier.
+__device__ __forceinline__ uint32_t e2m1_codes_of_quotients(const uint32_t (&w)[4], float e, float r,
+                                                            bool normal_e) {
   constexpr float kBelow = 1.0f - 1.0f / 524288.0f;  // 1 - 2^-19, exact in fp32
   constexpr float kAbove = 1.0f + 1.0f / 524288.0f;  // 1 + 2^-19
-  if (normal_e) {
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
     const float2 q = __fmul2_rn(x, make_float2(r, r));
-    const float2 lo = __fmul2_rn(q, make_float2(kBelow, kBelow));
-    const float2 hi = __fmul2_rn(q, make_float2(kAbove, kAbove));
-    const uint32_t clo = e2m1_pair(lo.x, lo.y);
-    if (clo == e2m1_pair(hi.x, hi.y)) return clo;
+    const float2 a = __fmul2_rn(q, make_float2(kBelow, kBelow));
+    const float2 b = __fmul2_rn(q, make_float2(kAbove, kAbove));
+    lo[i] = e2m1_pair(a.x, a.y);
+    hi[i] = e2m1_pair(b.x, b.y);
   }
-  return e2m1_pair(__fdiv_rn(x.x, e), __fdiv_rn(x.y, e));
+  const uint32_t lo4 = __byte_perm(__byte_perm(lo[0], lo[1], 0x0040), __byte_perm(lo[2], lo[3], 0x0040), 0x5410);
+  const uint32_t hi4 = __byte_perm(__byte_perm(hi[0], hi[1], 0x0040), __byte_perm(hi[2], hi[3], 0x0040), 0x5410);
+  if (normal_e && lo4 == hi4) return lo4;
+  uint32_t exact = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float x0 = __uint_as_float(w[i] << 16);
+    const float x1 = __uint_as_float(w[i] & 0xFFFF0000u);
+    exact |= e2m1_pair(__fdiv_rn(x0, e), __fdiv_rn(x1, e)) << (8 * i);
+  }
+  return exact;
 }
 
 __device__ __forceinline__ float rcp_approx(float v) {
@@ -154,10 +170,12 @@ __global__ void __launch_bounds__(kNvThreads, 3) nvfp4_pertoken_kernel(const uin
     const float s_t = (amax_bits == 0) ? 0.0f : __fdiv_rn(amax, 2688.0f);
     const float d = __fmul_rn(6.0f, s_t);
 
-    // padded row of the scale layout
+    // padded row of the scale layout; lanes 0, 8, 16, 24 store the scales of
+    // blocks 16 c + lane/2 .. +3, i.e. tile 4 c + lane/8 of this row
     const int g = find_group(groups.off, num_groups, row);
     const int64_t prow = 128 * static_cast<int64_t>(groups.tiles[g]) + (row - groups.off[g]);
     uint8_t *codes_row = codes + row * (k / 2);
+    uint8_t *sf_lane = sf + sf_offset(prow, 4 * (lane >> 3), c4);
 
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
@@ -171,12 +189,7 @@ __global__ void __launch_bounds__(kNvThreads, 3) nvfp4_pertoken_kernel(const uin
       if (sb != 0) {
         const float e = __fmul_rn(e4m3_value(sb), s_t);
         const bool normal_e = e >= 1.17549435e-38f;  // reciprocal finite and accurate
-        const float r = rcp_approx(e);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 xp = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-          packed |= e2m1_codes_of_quotients(xp, e, r, normal_e) << (8 * i);
-        }
+        packed = e2m1_codes_of_quotients(w, e, rcp_approx(e), normal_e);
       }
       if (col < k) *reinterpret_cast<uint32_t *>(codes_row + col / 2) = packed;
       // scales: block (16 c + lane/2) is held by the even lane of each pair; lanes
@@ -185,9 +198,8 @@ __global__ void __launch_bounds__(kNvThreads, 3) nvfp4_pertoken_kernel(const uin
       const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
       const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
       if ((lane & 7) == 0 && col < k) {
-        const int64_t cb = c * 16 + lane / 2;
         const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
-        *reinterpret_cast<uint32_t *>(sf + sf_offset(prow, cb, c4)) = word;
+        *reinterpret_cast<uint32_t *>(sf_lane + c * 2048) = word;
       }
     }
     if (lane == 0 && wr == 0) row_scale[row] = s_t;
