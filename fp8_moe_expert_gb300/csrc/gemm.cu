@@ -60,13 +60,16 @@ struct Cfg {
   static constexpr int kAtoms = kFp4 ? 4 : 1;          // 512-byte scale tiles per 128 rows per stage
   static constexpr int kSfaBytes = 512 * kAtoms;       // this CTA's 128 rows
   static constexpr int kSfbBytes = 2 * 512 * kAtoms;   // all 256 B rows of the tile
-  static constexpr int kSfaCols = 4 * kAtoms;          // tensor-memory columns per stage
+  // FP4: the four A-scale tiles of a stage are rearranged into one 4 KB block and
+  // moved by a single 128x256b copy into 8 columns (see the copier); FP8: one tile, 4 columns.
+  static constexpr int kSfaCols = kFp4 ? 8 : 4;
+  static constexpr int kArrangedBytes = kFp4 ? 4096 : 0;  // per rearranged A-scale block (two of them)
   static constexpr int kSfbCols = 8 * kAtoms;
   static constexpr int kSfCols = kSfaCols + kSfbCols;
   static constexpr int kStages = kFp4 ? 5 : 6;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageTx = 2 * kStageBytes;  // both CTAs' copies land on the leader's barrier
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kArrangedBytes + 1024;  // + alignment slack
   static_assert(kStages <= kMaxStages, "stage count");
   static_assert(kBN + kSfBuffers * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
 };
@@ -76,6 +79,7 @@ struct SharedState {
   uint64_t empty[kMaxStages];
   uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b
   uint64_t sf_empty[kSfBuffers];  // the MMAs reading buffer b are done
+  uint64_t arranged_free[2];      // the copy out of rearranged block a is done
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -253,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   uint8_t *smem_b = smem_a + C::kStages * kABytes;
   uint8_t *smem_sfa = smem_b + C::kStages * kBBytes;
   uint8_t *smem_sfb = smem_sfa + C::kStages * C::kSfaBytes;
+  uint8_t *smem_arranged = smem_sfb + C::kStages * C::kSfbBytes;  // FP4 only: 2 x 4 KB
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -274,6 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&s.sf_full[i], 1);
       mbar_init(&s.sf_empty[i], 1);
     }
+    mbar_init(&s.arranged_free[0], 1);
+    mbar_init(&s.arranged_free[1], 1);
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const uint64_t bd = desc_sw128_kmajor(b_s + kk * 32);
           const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
           if (C::kFp4)
-            pair::mma_nvf4(tmem, ad, bd, pair::idesc_nvf4(kBN), sfa_t + 4 * kk, sfb_t + 8 * kk, acc);
+            pair::mma_nvf4(tmem, ad, bd, pair::idesc_nvf4(kBN), sfa_t + kk, sfb_t + 8 * kk, acc);
           else
             pair::mma_mxf8(tmem, ad, bd, pair::idesc_mxf8(kBN, kk), sfa_t, sfb_t, acc);
         }
@@ -376,34 +383,83 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
-  } else if (warp == kCopierWarp && lane == 0 && rank == 0) {
+  } else if (warp == kCopierWarp && rank == 0) {
     // ---------------------------------------------------- scale copier (leader)
     // Copies each stage's scale tiles (both CTAs, tcgen05.cp.cta_group::2) into
     // the next free tensor-memory buffer while the MMA issuer works on earlier
     // stages, then signals the buffer full.
-    uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
+    //
+    // FP4 A scales: the block-scaled MMA reads the scale word of accumulator row r
+    // from tensor-memory lane r, column (scale address) + r/32.  Giving MMA kk the
+    // address base + kk, lane L = 32q + i must hold MMA kk's word in column q + kk.
+    // The warp rewrites the stage's four 512-byte tiles (tile kk: row i, word q =
+    // scales of row 32q + i) into a 128-row x 32-byte block whose row L has those
+    // words at word q .. q + 3 (zeros elsewhere), stored as 8-row x 16-byte core
+    // matrices (8-row groups 256 bytes apart, the two 16-byte halves 128 apart),
+    // and one 128x256b copy moves it into 8 columns.  Two such blocks alternate;
+    // a block is rewritten only after the copy out of it has completed.
+    uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0, arr = 0, arr_phase = 0;
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
       const Tile tl = tile_at<K>(p, s, t, 0);
       for (int ks = 0; ks < tl.num_k; ++ks) {
-        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
-            !mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status)) {
+        bool ready = true;
+        if (lane == 0)  // one lane waits; the warp follows its verdict
+          ready = mbar_wait(&s.full[stage], phase, abort_flag, p.status) &&
+                  mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status) &&
+                  (!C::kFp4 || mbar_wait(&s.arranged_free[arr], arr_phase ^ 1, abort_flag, p.status));
+        if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
           stop = true;
           break;
         }
-        tc_fence_after();
+        // every lane observes the completed load itself before reading the tiles
+        if (C::kFp4 && lane != 0) mbar_wait(&s.full[stage], phase, abort_flag, p.status);
         const uint32_t sfa_t = sf_base + buf * C::kSfCols;
         const uint32_t sfb_t = sfa_t + C::kSfaCols;
         const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
         const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
+        if (C::kFp4) {
+          const uint8_t *tiles = smem_sfa + stage * C::kSfaBytes;
+          uint8_t *blk = smem_arranged + arr * C::kArrangedBytes;
+          uint32_t wds[4][4];  // [kk][q]
 #pragma unroll
-        for (int i = 0; i < C::kAtoms; ++i) {
-          pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
-          pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
-          pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(tiles + kk * 512 + lane * 16);
+            wds[kk][0] = v.x;
+            wds[kk][1] = v.y;
+            wds[kk][2] = v.z;
+            wds[kk][3] = v.w;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t row[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) row[q + kk] = wds[kk][q];
+            const int L = 32 * q + lane;
+            uint8_t *dst = blk + (L >> 3) * 256 + (L & 7) * 16;
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
+            *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(row[4], row[5], row[6], row[7]);
+          }
+          fence_proxy_async_shared();  // the block is read by the tensor core's copy
+          __syncwarp();
         }
-        pair::commit_local(&s.sf_full[buf]);
+        if (lane == 0) {
+          tc_fence_after();
+          if (C::kFp4) {
+            pair::copy_scales_128x256(sfa_t, desc_core_blocked(smem_u32(smem_arranged + arr * C::kArrangedBytes)));
+          } else {
+            pair::copy_scales(sfa_t, desc_scale_tile(sfa_s));
+          }
+#pragma unroll
+          for (int i = 0; i < C::kAtoms; ++i) {
+            pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
+            pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+          }
+          pair::commit_local(&s.sf_full[buf]);
+          if (C::kFp4) pair::commit_local(&s.arranged_free[arr]);
+        }
+        __syncwarp();
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
@@ -412,11 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           buf = 0;
           buf_phase ^= 1;
         }
+        if (++arr == 2) {
+          arr = 0;
+          arr_phase ^= 1;
+        }
       }
     }
-    pair::commit_local(&s.drain2);
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&s.drain2, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
+    if (lane == 0) {
+      pair::commit_local(&s.drain2);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&s.drain2, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
+      }
     }
   } else if (warp >= 2 && warp < kCopierWarp) {
     // --------------------------------------------------------------- epilogue
