@@ -60,10 +60,12 @@ struct Cfg {
   static constexpr int kAtoms = kFp4 ? 4 : 1;          // 512-byte scale tiles per 128 rows per stage
   static constexpr int kSfaBytes = 512 * kAtoms;       // this CTA's 128 rows
   static constexpr int kSfbBytes = 2 * 512 * kAtoms;   // all 256 B rows of the tile
-  // FP4: the four A-scale tiles of a stage are rearranged into one 4 KB block and
-  // moved by a single 128x256b copy into 8 columns (see the copier); FP8: one tile, 4 columns.
-  static constexpr int kSfaCols = kFp4 ? 8 : 4;
-  static constexpr int kArrangedBytes = kFp4 ? 4096 : 0;  // per rearranged A-scale block (two of them)
+  // FP4: the four A-scale tiles of a stage are rearranged into two 4 KB blocks,
+  // each moved by one 128x256b copy into 8 columns (see the copier); FP8: one
+  // tile, 4 columns.  Every scale address given to an MMA or a copy stays a
+  // multiple of 4 columns.
+  static constexpr int kSfaCols = kFp4 ? 16 : 4;
+  static constexpr int kArrangedBytes = kFp4 ? 8192 : 0;  // per set of two rearranged blocks (two sets)
   static constexpr int kSfbCols = 8 * kAtoms;
   static constexpr int kSfCols = kSfaCols + kSfbCols;
   static constexpr int kStages = kFp4 ? 5 : 6;
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const uint64_t bd = desc_sw128_kmajor(b_s + kk * 32);
           const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
           if (C::kFp4)
-            pair::mma_nvf4(tmem, ad, bd, pair::idesc_nvf4(kBN), sfa_t + kk, sfb_t + 8 * kk, acc);
+            pair::mma_nvf4(tmem, ad, bd, pair::idesc_nvf4(kBN), sfa_t + 4 * kk, sfb_t + 8 * kk, acc);
           else
             pair::mma_mxf8(tmem, ad, bd, pair::idesc_mxf8(kBN, kk), sfa_t, sfb_t, acc);
         }
@@ -390,14 +392,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // stages, then signals the buffer full.
     //
     // FP4 A scales: the block-scaled MMA reads the scale word of accumulator row r
-    // from tensor-memory lane r, column (scale address) + r/32.  Giving MMA kk the
-    // address base + kk, lane L = 32q + i must hold MMA kk's word in column q + kk.
-    // The warp rewrites the stage's four 512-byte tiles (tile kk: row i, word q =
-    // scales of row 32q + i) into a 128-row x 32-byte block whose row L has those
-    // words at word q .. q + 3 (zeros elsewhere), stored as 8-row x 16-byte core
-    // matrices (8-row groups 256 bytes apart, the two 16-byte halves 128 apart),
-    // and one 128x256b copy moves it into 8 columns.  Two such blocks alternate;
-    // a block is rewritten only after the copy out of it has completed.
+    // from tensor-memory lane r, column (scale address) + r/32.  MMA kk gets the
+    // address base + 4 kk, so lane L = 32q + i must hold MMA kk's word in column
+    // 4 kk + q.  The warp rewrites the stage's four 512-byte tiles (tile kk: row
+    // i, word q = scales of row 32q + i) into two 128-row x 32-byte blocks: block
+    // h row L holds MMA 2h's word at word q and MMA 2h+1's word at word 4 + q
+    // (zeros elsewhere), stored as 8-row x 16-byte core matrices (8-row groups 256
+    // bytes apart, the two 16-byte halves 128 apart).  One 128x256b copy per block
+    // moves it into 8 columns.  Two sets of blocks alternate; a set is rewritten
+    // only after the copies out of it have completed.
     uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0, arr = 0, arr_phase = 0;
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
@@ -432,14 +435,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             wds[kk][3] = v.w;
           }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t row[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) row[q + kk] = wds[kk][q];
-            const int L = 32 * q + lane;
-            uint8_t *dst = blk + (L >> 3) * 256 + (L & 7) * 16;
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
-            *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(row[4], row[5], row[6], row[7]);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t row[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+              row[q] = wds[2 * h][q];
+              row[4 + q] = wds[2 * h + 1][q];
+              const int L = 32 * q + lane;
+              uint8_t *dst = blk + h * 4096 + (L >> 3) * 256 + (L & 7) * 16;
+              *reinterpret_cast<uint4 *>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
+              *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(row[4], row[5], row[6], row[7]);
+            }
           }
           fence_proxy_async_shared();  // the block is read by the tensor core's copy
           __syncwarp();
@@ -447,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (lane == 0) {
           tc_fence_after();
           if (C::kFp4) {
-            pair::copy_scales_128x256(sfa_t, desc_core_blocked(smem_u32(smem_arranged + arr * C::kArrangedBytes)));
+            const uint32_t blk = smem_u32(smem_arranged + arr * C::kArrangedBytes);
+            pair::copy_scales_128x256(sfa_t, desc_core_blocked(blk));
+            pair::copy_scales_128x256(sfa_t + 8, desc_core_blocked(blk + 4096));
           } else {
             pair::copy_scales(sfa_t, desc_scale_tile(sfa_s));
           }
