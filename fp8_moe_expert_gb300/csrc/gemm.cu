@@ -70,7 +70,9 @@ struct Cfg {
   static constexpr int kSfCols = kSfaCols + kSfbCols;
   static constexpr int kStages = kFp4 ? 5 : 6;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStageTx = 2 * kStageBytes;  // both CTAs' copies land on the leader's barrier
+  // Both CTAs' copies land on the leader's barrier, except (FP4) each CTA's A-scale
+  // tiles, which land on its own barrier for its copier warp to rearrange.
+  static constexpr int kStageTx = 2 * (kStageBytes - (kFp4 ? kSfaBytes : 0));
   static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kArrangedBytes + 1024;  // + alignment slack
   static_assert(kStages <= kMaxStages, "stage count");
   static_assert(kBN + kSfBuffers * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
@@ -81,7 +83,9 @@ struct SharedState {
   uint64_t empty[kMaxStages];
   uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b
   uint64_t sf_empty[kSfBuffers];  // the MMAs reading buffer b are done
-  uint64_t arranged_free[2];      // the copy out of rearranged block a is done
+  uint64_t arranged_free[2];      // the copies out of rearranged block set a are done (both CTAs)
+  uint64_t peer_arranged[2];      // leader: the peer CTA has rearranged its block set a
+  uint64_t sfa_full[kMaxStages];  // FP4: this CTA's A-scale tiles of a stage have landed
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -281,8 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&s.sf_full[i], 1);
       mbar_init(&s.sf_empty[i], 1);
     }
-    mbar_init(&s.arranged_free[0], 1);
-    mbar_init(&s.arranged_free[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.arranged_free[i], 1);
+      mbar_init(&s.peer_arranged[i], 1);
+    }
+    for (int i = 0; i < C::kStages; ++i) mbar_init(&s.sfa_full[i], 1);
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
@@ -323,8 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint32_t bar = pair::map_to_rank(&s.full[stage], 0);
         pair::tma_load_2d(smem_a + stage * kABytes, &p.map_a, bar, tl.a_x0 + ks * kStageKBytes, tl.a_y);
         pair::tma_load_2d(smem_b + stage * kBBytes, &p.map_b, bar, tl.b_x0 + ks * kStageKBytes, tl.b_y);
-        pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, bar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
-                          tl.sfa_row);
+        if (C::kFp4) {
+          mbar_arrive_expect_tx(&s.sfa_full[stage], C::kSfaBytes);
+          tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, &s.sfa_full[stage],
+                      (tl.sfa_x0 + ks * C::kAtoms) * 64, tl.sfa_row);
+        } else {
+          pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, bar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
+                            tl.sfa_row);
+        }
         pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
                           tl.sfb_row);
         if (++stage == C::kStages) {
@@ -385,44 +398,51 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
-  } else if (warp == kCopierWarp && rank == 0) {
-    // ---------------------------------------------------- scale copier (leader)
-    // Copies each stage's scale tiles (both CTAs, tcgen05.cp.cta_group::2) into
-    // the next free tensor-memory buffer while the MMA issuer works on earlier
-    // stages, then signals the buffer full.
+  } else if (warp == kCopierWarp && (C::kFp4 || rank == 0)) {
+    // ------------------------------------------------------------ scale copier
+    // The leader's lane 0 copies each stage's scale tiles (both CTAs,
+    // tcgen05.cp.cta_group::2) into the next free tensor-memory buffer while the
+    // MMA issuer works on earlier stages, then signals the buffer full.
     //
     // FP4 A scales: the block-scaled MMA reads the scale word of accumulator row r
     // from tensor-memory lane r, column (scale address) + r/32.  MMA kk gets the
     // address base + 4 kk, so lane L = 32q + i must hold MMA kk's word in column
-    // 4 kk + q.  The warp rewrites the stage's four 512-byte tiles (tile kk: row
-    // i, word q = scales of row 32q + i) into two 128-row x 32-byte blocks: block
-    // h row L holds MMA 2h's word at word q and MMA 2h+1's word at word 4 + q
-    // (zeros elsewhere), stored as 8-row x 16-byte core matrices (8-row groups 256
-    // bytes apart, the two 16-byte halves 128 apart).  One 128x256b copy per block
-    // moves it into 8 columns.  Two sets of blocks alternate; a set is rewritten
-    // only after the copies out of it have completed.
+    // 4 kk + q.  In each CTA the warp rewrites the stage's four 512-byte tiles
+    // (tile kk: row i, word q = scales of row 32q + i) into two 128-row x 32-byte
+    // blocks: block h row L holds MMA 2h's word at word q and MMA 2h+1's word at
+    // word 4 + q (zeros elsewhere), stored as 8-row x 16-byte core matrices (8-row
+    // groups 256 bytes apart, the two 16-byte halves 128 apart).  One 128x256b
+    // copy per block moves it into 8 columns of each CTA.  Two sets of blocks
+    // alternate; the peer tells the leader when its set is ready, and the
+    // leader's commit tells both CTAs when a set may be rewritten.
     uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0, arr = 0, arr_phase = 0;
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
+    const uint32_t leader_peer_arranged0 = pair::map_to_rank(&s.peer_arranged[0], 0);
+    const uint32_t leader_peer_arranged1 = pair::map_to_rank(&s.peer_arranged[1], 0);
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
-      const Tile tl = tile_at<K>(p, s, t, 0);
+      const Tile tl = tile_at<K>(p, s, t, rank);
       for (int ks = 0; ks < tl.num_k; ++ks) {
         bool ready = true;
-        if (lane == 0)  // one lane waits; the warp follows its verdict
-          ready = mbar_wait(&s.full[stage], phase, abort_flag, p.status) &&
-                  mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status) &&
-                  (!C::kFp4 || mbar_wait(&s.arranged_free[arr], arr_phase ^ 1, abort_flag, p.status));
+        if (lane == 0) {  // one lane waits; the warp follows its verdict
+          if (C::kFp4)
+            ready = mbar_wait(&s.sfa_full[stage], phase, abort_flag, p.status) &&
+                    mbar_wait(&s.arranged_free[arr], arr_phase ^ 1, abort_flag, p.status);
+          if (rank == 0)
+            ready = ready && mbar_wait(&s.full[stage], phase, abort_flag, p.status) &&
+                    mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status);
+        }
         if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
           stop = true;
           break;
         }
-        // every lane observes the completed load itself before reading the tiles
-        if (C::kFp4 && lane != 0) mbar_wait(&s.full[stage], phase, abort_flag, p.status);
         const uint32_t sfa_t = sf_base + buf * C::kSfCols;
         const uint32_t sfb_t = sfa_t + C::kSfaCols;
         const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
         const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
         if (C::kFp4) {
+          // every lane observes the completed load itself before reading the tiles
+          if (lane != 0) mbar_wait(&s.sfa_full[stage], phase, abort_flag, p.status);
           const uint8_t *tiles = smem_sfa + stage * C::kSfaBytes;
           uint8_t *blk = smem_arranged + arr * C::kArrangedBytes;
           uint32_t wds[4][4];  // [kk][q]
@@ -447,27 +467,35 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
               *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(row[4], row[5], row[6], row[7]);
             }
           }
-          fence_proxy_async_shared();  // the block is read by the tensor core's copy
+          fence_proxy_async_shared();  // the blocks are read by the tensor core's copy
           __syncwarp();
+          if (rank == 1 && lane == 0) pair::arrive_remote(arr ? leader_peer_arranged1 : leader_peer_arranged0);
         }
-        if (lane == 0) {
-          tc_fence_after();
-          if (C::kFp4) {
-            const uint32_t blk = smem_u32(smem_arranged + arr * C::kArrangedBytes);
-            pair::copy_scales_128x256(sfa_t, desc_core_blocked(blk));
-            pair::copy_scales_128x256(sfa_t + 8, desc_core_blocked(blk + 4096));
-          } else {
-            pair::copy_scales(sfa_t, desc_scale_tile(sfa_s));
-          }
+        if (rank == 0 && lane == 0) {
+          bool ok = !C::kFp4 || mbar_wait(&s.peer_arranged[arr], arr_phase, abort_flag, p.status);
+          if (ok) {
+            tc_fence_after();
+            if (C::kFp4) {
+              const uint32_t blk = smem_u32(smem_arranged + arr * C::kArrangedBytes);
+              pair::copy_scales_128x256(sfa_t, desc_core_blocked(blk));
+              pair::copy_scales_128x256(sfa_t + 8, desc_core_blocked(blk + 4096));
+            } else {
+              pair::copy_scales(sfa_t, desc_scale_tile(sfa_s));
+            }
 #pragma unroll
-          for (int i = 0; i < C::kAtoms; ++i) {
-            pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
-            pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+            for (int i = 0; i < C::kAtoms; ++i) {
+              pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
+              pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+            }
+            pair::commit_local(&s.sf_full[buf]);
+            if (C::kFp4) pair::commit_both(&s.arranged_free[arr]);
           }
-          pair::commit_local(&s.sf_full[buf]);
-          if (C::kFp4) pair::commit_local(&s.arranged_free[arr]);
+          ready = ok;
         }
-        __syncwarp();
+        if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
+          stop = true;
+          break;
+        }
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
@@ -482,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
       }
     }
-    if (lane == 0) {
+    if (rank == 0 && lane == 0) {
       pair::commit_local(&s.drain2);
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(&s.drain2, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
