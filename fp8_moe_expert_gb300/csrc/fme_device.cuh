@@ -207,17 +207,6 @@ __device__ __forceinline__ uint64_t desc_scale_tile(uint32_t saddr) {
   return d;
 }
 
-// Descriptor of a 128-row x 32-byte block stored as 8-row x 16-byte core
-// matrices: 8-row groups 256 bytes apart, the two 16-byte halves 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_core_blocked(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
-  d |= static_cast<uint64_t>(128 >> 4) << 16;
-  d |= static_cast<uint64_t>(256 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  return d;
-}
-
 // Instruction descriptor, kind::mxf8f6f4, E4M3 x E4M3, UE8M0 scales, M = 128.
 // sf_id picks which byte of the 32-bit scale word (which 32-wide K block) is used.
 __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t n, uint32_t sf_id) {
@@ -343,13 +332,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // into four tensor-memory columns of that CTA, replicated over the lane quarters.
 __device__ __forceinline__ void copy_scales(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// Issued by the leader: a 128-row x 32-byte block (core-matrix layout, see
-// desc_core_blocked) of each CTA into eight tensor-memory columns of that CTA,
-// lane L column w <- bytes 4w .. 4w+3 of block row L.
-__device__ __forceinline__ void copy_scales_128x256(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive on the mbarrier at the same shared offset in both CTAs when the

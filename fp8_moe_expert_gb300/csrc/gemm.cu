@@ -60,20 +60,13 @@ struct Cfg {
   static constexpr int kAtoms = kFp4 ? 4 : 1;          // 512-byte scale tiles per 128 rows per stage
   static constexpr int kSfaBytes = 512 * kAtoms;       // this CTA's 128 rows
   static constexpr int kSfbBytes = 2 * 512 * kAtoms;   // all 256 B rows of the tile
-  // FP4: the four A-scale tiles of a stage are rearranged into two 4 KB blocks,
-  // each moved by one 128x256b copy into 8 columns (see the copier); FP8: one
-  // tile, 4 columns.  Every scale address given to an MMA or a copy stays a
-  // multiple of 4 columns.
-  static constexpr int kSfaCols = kFp4 ? 16 : 4;
-  static constexpr int kArrangedBytes = kFp4 ? 8192 : 0;  // per set of two rearranged blocks (two sets)
+  static constexpr int kSfaCols = 4 * kAtoms;          // tensor-memory columns per stage
   static constexpr int kSfbCols = 8 * kAtoms;
   static constexpr int kSfCols = kSfaCols + kSfbCols;
   static constexpr int kStages = kFp4 ? 5 : 6;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  // Both CTAs' copies land on the leader's barrier, except (FP4) each CTA's A-scale
-  // tiles, which land on its own barrier for its copier warp to rearrange.
-  static constexpr int kStageTx = 2 * (kStageBytes - (kFp4 ? kSfaBytes : 0));
-  static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kArrangedBytes + 1024;  // + alignment slack
+  static constexpr int kStageTx = 2 * kStageBytes;  // both CTAs' copies land on the leader's barrier
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   static_assert(kStages <= kMaxStages, "stage count");
   static_assert(kBN + kSfBuffers * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
 };
@@ -83,9 +76,6 @@ struct SharedState {
   uint64_t empty[kMaxStages];
   uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b
   uint64_t sf_empty[kSfBuffers];  // the MMAs reading buffer b are done
-  uint64_t arranged_free[2];      // the copies out of rearranged block set a are done (both CTAs)
-  uint64_t peer_arranged[2];      // leader: the peer CTA has rearranged its block set a
-  uint64_t sfa_full[kMaxStages];  // FP4: this CTA's A-scale tiles of a stage have landed
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -263,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   uint8_t *smem_b = smem_a + C::kStages * kABytes;
   uint8_t *smem_sfa = smem_b + C::kStages * kBBytes;
   uint8_t *smem_sfb = smem_sfa + C::kStages * C::kSfaBytes;
-  uint8_t *smem_arranged = smem_sfb + C::kStages * C::kSfbBytes;  // FP4 only: 2 x 4 KB
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -285,11 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&s.sf_full[i], 1);
       mbar_init(&s.sf_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.arranged_free[i], 1);
-      mbar_init(&s.peer_arranged[i], 1);
-    }
-    for (int i = 0; i < C::kStages; ++i) mbar_init(&s.sfa_full[i], 1);
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
@@ -330,14 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint32_t bar = pair::map_to_rank(&s.full[stage], 0);
         pair::tma_load_2d(smem_a + stage * kABytes, &p.map_a, bar, tl.a_x0 + ks * kStageKBytes, tl.a_y);
         pair::tma_load_2d(smem_b + stage * kBBytes, &p.map_b, bar, tl.b_x0 + ks * kStageKBytes, tl.b_y);
-        if (C::kFp4) {
-          mbar_arrive_expect_tx(&s.sfa_full[stage], C::kSfaBytes);
-          tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, &s.sfa_full[stage],
-                      (tl.sfa_x0 + ks * C::kAtoms) * 64, tl.sfa_row);
-        } else {
-          pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, bar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
-                            tl.sfa_row);
-        }
+        pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, bar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
+                          tl.sfa_row);
         pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
                           tl.sfb_row);
         if (++stage == C::kStages) {
@@ -398,104 +376,34 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
-  } else if (warp == kCopierWarp && (C::kFp4 || rank == 0)) {
-    // ------------------------------------------------------------ scale copier
-    // The leader's lane 0 copies each stage's scale tiles (both CTAs,
-    // tcgen05.cp.cta_group::2) into the next free tensor-memory buffer while the
-    // MMA issuer works on earlier stages, then signals the buffer full.
-    //
-    // FP4 A scales: the block-scaled MMA reads the scale word of accumulator row r
-    // from tensor-memory lane r, column (scale address) + r/32.  MMA kk gets the
-    // address base + 4 kk, so lane L = 32q + i must hold MMA kk's word in column
-    // 4 kk + q.  In each CTA the warp rewrites the stage's four 512-byte tiles
-    // (tile kk: row i, word q = scales of row 32q + i) into two 128-row x 32-byte
-    // blocks: block h row L holds MMA 2h's word at word q and MMA 2h+1's word at
-    // word 4 + q (zeros elsewhere), stored as 8-row x 16-byte core matrices (8-row
-    // groups 256 bytes apart, the two 16-byte halves 128 apart).  One 128x256b
-    // copy per block moves it into 8 columns of each CTA.  Two sets of blocks
-    // alternate; the peer tells the leader when its set is ready, and the
-    // leader's commit tells both CTAs when a set may be rewritten.
-    uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0, arr = 0, arr_phase = 0;
+  } else if (warp == kCopierWarp && lane == 0 && rank == 0) {
+    // ---------------------------------------------------- scale copier (leader)
+    // Copies each stage's scale tiles (both CTAs, tcgen05.cp.cta_group::2) into
+    // the next free tensor-memory buffer while the MMA issuer works on earlier
+    // stages, then signals the buffer full.
+    uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
-    const uint32_t leader_peer_arranged0 = pair::map_to_rank(&s.peer_arranged[0], 0);
-    const uint32_t leader_peer_arranged1 = pair::map_to_rank(&s.peer_arranged[1], 0);
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
-      const Tile tl = tile_at<K>(p, s, t, rank);
+      const Tile tl = tile_at<K>(p, s, t, 0);
       for (int ks = 0; ks < tl.num_k; ++ks) {
-        bool ready = true;
-        if (lane == 0) {  // one lane waits; the warp follows its verdict
-          if (C::kFp4)
-            ready = mbar_wait(&s.sfa_full[stage], phase, abort_flag, p.status) &&
-                    mbar_wait(&s.arranged_free[arr], arr_phase ^ 1, abort_flag, p.status);
-          if (rank == 0)
-            ready = ready && mbar_wait(&s.full[stage], phase, abort_flag, p.status) &&
-                    mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status);
-        }
-        if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
+        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
+            !mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status)) {
           stop = true;
           break;
         }
+        tc_fence_after();
         const uint32_t sfa_t = sf_base + buf * C::kSfCols;
         const uint32_t sfb_t = sfa_t + C::kSfaCols;
         const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
         const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
-        if (C::kFp4) {
-          // every lane observes the completed load itself before reading the tiles
-          if (lane != 0) mbar_wait(&s.sfa_full[stage], phase, abort_flag, p.status);
-          const uint8_t *tiles = smem_sfa + stage * C::kSfaBytes;
-          uint8_t *blk = smem_arranged + arr * C::kArrangedBytes;
-          uint32_t wds[4][4];  // [kk][q]
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(tiles + kk * 512 + lane * 16);
-            wds[kk][0] = v.x;
-            wds[kk][1] = v.y;
-            wds[kk][2] = v.z;
-            wds[kk][3] = v.w;
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t row[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-              row[q] = wds[2 * h][q];
-              row[4 + q] = wds[2 * h + 1][q];
-              const int L = 32 * q + lane;
-              uint8_t *dst = blk + h * 4096 + (L >> 3) * 256 + (L & 7) * 16;
-              *reinterpret_cast<uint4 *>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
-              *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(row[4], row[5], row[6], row[7]);
-            }
-          }
-          fence_proxy_async_shared();  // the blocks are read by the tensor core's copy
-          __syncwarp();
-          if (rank == 1 && lane == 0) pair::arrive_remote(arr ? leader_peer_arranged1 : leader_peer_arranged0);
+        for (int i = 0; i < C::kAtoms; ++i) {
+          pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
+          pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
+          pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
         }
-        if (rank == 0 && lane == 0) {
-          bool ok = !C::kFp4 || mbar_wait(&s.peer_arranged[arr], arr_phase, abort_flag, p.status);
-          if (ok) {
-            tc_fence_after();
-            if (C::kFp4) {
-              const uint32_t blk = smem_u32(smem_arranged + arr * C::kArrangedBytes);
-              pair::copy_scales_128x256(sfa_t, desc_core_blocked(blk));
-              pair::copy_scales_128x256(sfa_t + 8, desc_core_blocked(blk + 4096));
-            } else {
-              pair::copy_scales(sfa_t, desc_scale_tile(sfa_s));
-            }
-#pragma unroll
-            for (int i = 0; i < C::kAtoms; ++i) {
-              pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
-              pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
-            }
-            pair::commit_local(&s.sf_full[buf]);
-            if (C::kFp4) pair::commit_both(&s.arranged_free[arr]);
-          }
-          ready = ok;
-        }
-        if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
-          stop = true;
-          break;
-        }
+        pair::commit_local(&s.sf_full[buf]);
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
@@ -504,17 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           buf = 0;
           buf_phase ^= 1;
         }
-        if (++arr == 2) {
-          arr = 0;
-          arr_phase ^= 1;
-        }
       }
     }
-    if (rank == 0 && lane == 0) {
-      pair::commit_local(&s.drain2);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&s.drain2, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
-      }
+    pair::commit_local(&s.drain2);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&s.drain2, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
   } else if (warp >= 2 && warp < kCopierWarp) {
     // --------------------------------------------------------------- epilogue
