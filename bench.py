@@ -7,10 +7,10 @@ routed rows, Zipf(1.2) loads with 3 empty experts):
 
   forward (NVFP4):  quantize X and W_gate/up -> grouped GEMM gate/up,
                     quantize H and W_down    -> grouped GEMM down
-  backward (MXFP8): quantize dY row-wise and W_down column-wise -> dgrad,
-                    quantize dY and H column-wise              -> wgrad
+  backward (MXFP8): quantize dY row-wise and column-wise in one pass,
+                    W_down column-wise -> dgrad; H column-wise -> wgrad
 
-12 launches of libfme.so per step, inputs resident in HBM (every input is
+11 launches of libfme.so per step, inputs resident in HBM (every input is
 larger than the 129 MB L2).  The headline value is grouped-GEMM TFLOP/s over
 the whole step (GEMM FLOPs / step time, quantizers included); each call's time,
 GB/s or TFLOP/s and roofline fraction are reported in "breakdown".
@@ -128,11 +128,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ the step --
 class MoEStep:
-    """Device buffers of one MoE-layer forward+backward and the 12 calls over them."""
+    """Device buffers of one MoE-layer forward+backward and the 11 calls over them."""
 
     CALLS = ["quant_x_nvfp4", "quant_wgu_nvfp4", "gemm_fwd_gate_up", "quant_h_nvfp4", "quant_wd_nvfp4",
-             "gemm_fwd_down", "quant_dy_rows_mxfp8", "quant_wd_cols_mxfp8", "gemm_dgrad",
-             "quant_dy_cols_mxfp8", "quant_h_cols_mxfp8", "gemm_wgrad"]
+             "gemm_fwd_down", "quant_dy_rowcol_mxfp8", "quant_wd_cols_mxfp8", "gemm_dgrad",
+             "quant_h_cols_mxfp8", "gemm_wgrad"]
 
     def __init__(self, counts, seed, device, inputs_only=False):
         import torch
@@ -187,10 +187,10 @@ class MoEStep:
             "quant_h_nvfp4": ("bytes", nv(R, I)),
             "quant_wd_nvfp4": ("bytes", nv(E * H, I)),
             "gemm_fwd_down": ("flops", 2 * R * H * I),
-            "quant_dy_rows_mxfp8": ("bytes", mx(R, H)),
+            # one read of dY, row-wise and column-wise outputs
+            "quant_dy_rowcol_mxfp8": ("bytes", R * (2 * H + 2 * (H + H // 32))),
             "quant_wd_cols_mxfp8": ("bytes", mx(E * H, I)),
             "gemm_dgrad": ("flops", 2 * R * I * H),
-            "quant_dy_cols_mxfp8": ("bytes", mx(R, H)),
             "quant_h_cols_mxfp8": ("bytes", mx(R, I)),
             "gemm_wgrad": ("flops", 2 * R * H * I),
         }
@@ -211,13 +211,13 @@ class MoEStep:
             lambda: f.quantize_nvfp4_pertoken(self.w_d, codes=self.wdq[0], sf=self.wdq[1], row_scale=self.wdq[2],
                                               status=st),
             lambda: f.grouped_gemm_fwd_nvfp4(*self.hq, *self.wdq, off, H, I, y=self.y_d, status=st),
-            lambda: f.quantize_mxfp8(self.dy, f.ROWWISE, off, codes=self.dyr[0], sf=self.dyr[1], status=st),
+            lambda: f.quantize_mxfp8_rowcol(self.dy, off, row_codes=self.dyr[0], row_sf=self.dyr[1],
+                                            col_codes=self.dyc[0], col_sf=self.dyc[1], padded_offsets=self.dyc[2],
+                                            status=st),
             lambda: f.quantize_mxfp8(self.w_d, f.COLWISE, codes=self.wdc[0], sf=self.wdc[1], padded_offsets=self.wdc[2],
                                      status=st),
             lambda: f.grouped_gemm_dgrad_mxfp8(*self.dyr, self.wdc[0], self.wdc[1], self.ld_w, off, I, H, y=self.dh,
                                                status=st),
-            lambda: f.quantize_mxfp8(self.dy, f.COLWISE, off, codes=self.dyc[0], sf=self.dyc[1],
-                                     padded_offsets=self.dyc[2], status=st),
             lambda: f.quantize_mxfp8(self.h, f.COLWISE, off, codes=self.hc[0], sf=self.hc[1], padded_offsets=self.hc[2],
                                      status=st),
             lambda: f.grouped_gemm_wgrad_mxfp8(self.dyc[0], self.dyc[1], self.ld_r, self.hc[0], self.hc[1], self.ld_r,

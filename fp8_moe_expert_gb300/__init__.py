@@ -61,6 +61,7 @@ SYMBOLS = {
     # name: (restype, argtypes)
     "quantize_nvfp4_pertoken": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8": ("i32", ["p", "i64", "i64", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
+    "quantize_mxfp8_rowcol": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p", "p"]),
     "grouped_gemm_fwd_nvfp4": ("i32", ["p", "p", "p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p",
                                        "p"]),
     "grouped_gemm_dgrad_mxfp8": ("i32", ["p", "p", "p", "p", "i64", "p", "i32", "i64", "i64", "i64", "p", "p",
@@ -184,6 +185,33 @@ def quantize_mxfp8(x, axis=ROWWISE, offsets=None, num_groups=None, *, codes=None
                               _ptr(padded_offsets), _ptr(status), _stream(stream))
     _check(st, "quantize_mxfp8")
     return codes, sf, padded_offsets, ld
+
+
+def quantize_mxfp8_rowcol(x, offsets=None, num_groups=None, *, row_codes=None, row_sf=None, col_codes=None,
+                          col_sf=None, padded_offsets=None, status=None, stream=None):
+    """Row-wise and column-wise MXFP8 of bf16 x [rows, cols] in one pass ->
+    ((row_codes, row_sf), (col_codes, col_sf, padded_offsets, ld))."""
+    import torch
+
+    rows, cols = x.shape
+    offsets, g = _groups(offsets, num_groups)
+    dev = x.device
+    ld = colwise_ld(rows, g)
+    if row_codes is None:
+        row_codes = _empty((rows, cols), torch.uint8, dev)
+    if row_sf is None:
+        row_sf = _empty((max(sf_bytes(rows, cols, 32, g), 16),), torch.uint8, dev)
+    if col_codes is None:
+        col_codes = _empty((cols, ld), torch.uint8, dev)
+    if col_sf is None:
+        col_sf = _empty((max(sf_bytes(cols, ld, 32, 1), 16),), torch.uint8, dev)
+    if padded_offsets is None:
+        padded_offsets = _empty((g + 1,), torch.int32, dev)
+    st = lib().quantize_mxfp8_rowcol(_ptr(x), rows, cols, _ptr(offsets), g, _ptr(row_codes), _ptr(row_sf),
+                                     _ptr(col_codes), _ptr(col_sf), _ptr(padded_offsets), _ptr(status),
+                                     _stream(stream))
+    _check(st, "quantize_mxfp8_rowcol")
+    return (row_codes, row_sf), (col_codes, col_sf, padded_offsets, ld)
 
 
 def grouped_gemm_fwd_nvfp4(a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offsets, n, k, *, y=None,

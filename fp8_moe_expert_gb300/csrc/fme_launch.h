@@ -53,6 +53,7 @@ struct LaunchGemm {
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a);
 cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a);
+cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf);
 cudaError_t launch_grouped_gemm(const LaunchGemm &a);
 
 }  // namespace fme

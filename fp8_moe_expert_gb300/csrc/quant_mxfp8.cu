@@ -118,12 +118,18 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
 constexpr int kColTilePad = 8;  // bf16 elements of padding per staged row
 constexpr int kColTileBytes = 128 * (128 + kColTilePad) * 2;
 constexpr int kColOutBytes = 128 * (128 + 16);
-constexpr int kColSmemBytes = kColTileBytes + kColOutBytes + 512;
+constexpr int kColSmemBytes = kColTileBytes + kColOutBytes + 512 + 512;
 
-__global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
+// kRows: also quantize the same tile row-wise (blocks of 32 along each row), so a
+// tensor needed both ways is read once.  The tile's 128 padded positions are the
+// row-wise scale layout's 128-row block j (both pad each group to 128 rows), so
+// its row-wise scales are one 512-byte tile too.
+template <bool kRows>
+__global__ void __launch_bounds__(256, 3) mxfp8_cols_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
                                                          const int32_t *__restrict__ offsets, int num_groups,
                                                          uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
                                                          int64_t ld, int32_t *__restrict__ padded_offsets,
+                                                         uint8_t *__restrict__ row_codes, uint8_t *__restrict__ row_sf,
                                                          int32_t *status) {
   __shared__ GroupTable groups;
   __shared__ int ok_flag;
@@ -131,6 +137,7 @@ __global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restr
   auto tile = reinterpret_cast<uint16_t(*)[128 + kColTilePad]>(col_smem);
   auto outq = reinterpret_cast<uint8_t(*)[128 + 16]>(col_smem + kColTileBytes);
   uint8_t *sfs = col_smem + kColTileBytes + kColOutBytes;
+  uint8_t *sfr = sfs + 512;  // row-wise scales of the tile (kRows)
 
   if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(status, kDevBadOffsets);
@@ -208,6 +215,44 @@ __global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restr
         sfs[(c & 31) * 16 + (c >> 5) * 4 + b] = static_cast<uint8_t>(code);
       }
     }
+    if (kRows) {
+      // thread = (row r, 32-column block b) for 2 of the tile's 512 pairs; rows past
+      // the group's end are not stored
+      const int64_t g = find_group(groups.tiles, num_groups, j);
+      const int64_t local0 = 128 * (j - groups.tiles[g]);
+      const int64_t n_g = groups.off[g + 1] - groups.off[g];
+      const int valid = static_cast<int>(n_g - local0 < 128 ? n_g - local0 : 128);
+      const int64_t src0 = groups.off[g] + local0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int pr = tid + 256 * h;
+        const int r = pr >> 2;
+        const int b = pr & 3;
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][32 * b + 8 * i]);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = max_u16x2(m, w[i] & 0x7FFF7FFFu);
+        const uint32_t code = mx_code_from_bf16_amax(max(m & 0xFFFFu, m >> 16));
+        const float s = mx_inv_scale(code);
+        uint32_t words[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) words[q] = quad_codes(w[2 * q], w[2 * q + 1], s);
+        if (r < valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(row_codes + (src0 + r) * cols + cb * 128 + 32 * b);
+          dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
+          dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+        }
+        sfr[(r & 31) * 16 + (r >> 5) * 4 + b] = static_cast<uint8_t>(code);
+      }
+    }
     __syncthreads();
 
 #pragma unroll
@@ -220,6 +265,9 @@ __global__ void __launch_bounds__(256) mxfp8_cols_kernel(const uint16_t *__restr
     if (tid < 32) {
       const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
       *reinterpret_cast<uint4 *>(sf_t + (static_cast<int64_t>(cb) * (ld / 128) + j) * 512 + tid * 16) = v;
+    } else if (kRows && tid < 64) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[(tid - 32) * 16]);
+      *reinterpret_cast<uint4 *>(row_sf + (j * cblocks + cb) * 512 + (tid - 32) * 16) = v;
     }
   }
 }
@@ -235,18 +283,25 @@ cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a) {
+template <bool kRows>
+static cudaError_t launch_cols(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
   const int threads = 256;
   const int64_t tiles = (a.ld / 128) * (a.cols / 128);
   const int64_t cap = static_cast<int64_t>(a.num_sms) * 4;
   const int blocks = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
-  cudaError_t err = cudaFuncSetAttribute(mxfp8_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(mxfp8_cols_kernel<kRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kColSmemBytes);
   if (err != cudaSuccess) return err;
-  mxfp8_cols_kernel<<<blocks, threads, kColSmemBytes, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows,
-                                                       static_cast<int>(a.cols), a.offsets, a.num_groups,
-                                                       a.codes, a.sf, a.ld, a.padded_offsets, a.status);
+  mxfp8_cols_kernel<kRows><<<blocks, threads, kColSmemBytes, a.stream>>>(
+      static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.cols), a.offsets, a.num_groups, a.codes, a.sf,
+      a.ld, a.padded_offsets, row_codes, row_sf, a.status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a) { return launch_cols<false>(a, nullptr, nullptr); }
+
+cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
+  return launch_cols<true>(a, row_codes, row_sf);
 }
 
 }  // namespace fme

@@ -1,7 +1,8 @@
 /*
  * fme.h -- C ABI of the GB300 low-precision MoE expert path (libfme.so).
  *
- * Five calls, named after the operations of the MoE expert layer:
+ * Five calls, named after the operations of the MoE expert layer (plus a fused
+ * row-wise + column-wise MXFP8 quantizer for tensors needed both ways):
  *   quantize_nvfp4_pertoken   NVFP4 variant of the forward: E2M1 codes, one E4M3
  *                             scale per 16 values along K, one FP32 scale per token.
  *   quantize_mxfp8            standard MXFP8 of the backward: E4M3 codes, one E8M0
@@ -139,6 +140,20 @@ fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const
 fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axis, const int32_t *offsets,
                           int32_t num_groups, uint8_t *codes, uint8_t *sf, int32_t *padded_offsets,
                           int32_t *dev_status, void *stream);
+
+/*
+ * quantize_mxfp8_rowcol -- quantize_mxfp8 ROWWISE and COLWISE of the same x in one
+ * pass (x is read once), e.g. dY of the backward, which feeds both dgrad
+ * (row-wise) and wgrad (column-wise).  Outputs are identical, byte for byte, to
+ * the two separate calls (cols a multiple of 128):
+ *   row_codes, row_sf   as quantize_mxfp8(ROWWISE) with these offsets
+ *   col_codes, col_sf   as quantize_mxfp8(COLWISE): [cols x ld], tiled scales
+ *   padded_offsets      as quantize_mxfp8(COLWISE)
+ * Row-wise scale bytes of padding rows are written as 0.
+ */
+fme_status quantize_mxfp8_rowcol(const void *x, int64_t rows, int64_t cols, const int32_t *offsets,
+                                 int32_t num_groups, uint8_t *row_codes, uint8_t *row_sf, uint8_t *col_codes,
+                                 uint8_t *col_sf, int32_t *padded_offsets, int32_t *dev_status, void *stream);
 
 /*
  * grouped_gemm_fwd_nvfp4 -- Y[t, :] = S_x[t] * S_w[e, :] * sum_k A'[t,k] B'_e[:,k]

@@ -223,6 +223,24 @@ def test_mxfp8_cols_edges(fme, orc, counts):
     check_mx_cols(fme, orc, x, off)
 
 
+@pytest.mark.parametrize("counts", [[16384], [37, 0, 200, 1, 129], [4000, 3000, 0, 9384]])
+def test_mxfp8_rowcol_fused_matches_oracle(fme, orc, counts):
+    """One-pass row-wise + column-wise quantization equals the oracle both ways."""
+    off = synth.offsets_from_counts(counts)
+    x, _, _ = synth.quantizer_batch(rows=int(off[-1]), cols=1024, seed=5)
+    st = _status()
+    (rc, rs), (cc, cs, poff, ld) = fme.quantize_mxfp8_rowcol(bf16_tensor(x), _dev_offsets(off), status=st)
+    assert fme.read_device_status(st)[0] == 0
+    oc, osf = orc.quant_mxfp8_rows(x)
+    assert np.array_equal(to_np(rc), oc)
+    assert np.array_equal(unswizzle(to_np(rs), x.shape[0], 1024 // 32, off), osf)
+    occ, ocs, opoff = orc.quant_mxfp8_cols(x, off, ld=ld)
+    p = int(opoff[-1])
+    assert np.array_equal(to_np(poff), opoff)
+    assert np.array_equal(to_np(cc)[:, :p], occ[:, :p])
+    assert np.array_equal(unswizzle(to_np(cs), 1024, ld // 32)[:, : p // 32], ocs[:, : p // 32])
+
+
 def test_mxfp8_rows_cols_deterministic(fme):
     x, _, _ = synth.quantizer_batch(rows=512)
     off = synth.offsets_from_counts([100, 0, 412])
