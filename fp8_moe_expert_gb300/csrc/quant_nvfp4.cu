@@ -7,16 +7,18 @@
 // q = E2M1(x / e), all divisions correctly rounded (__fdiv_rn), all conversions
 // round-to-nearest-even with saturation.
 //
-// One to four warps own one row (rows longer than 2048 values are split).  Lane
-// l of a warp holds the 16-value block l of each 512-wide chunk it owns in
-// registers (two 16-byte loads per chunk), so the row is read from HBM once:
-// the row amax is a warp max-reduction (plus a shared-memory exchange between
-// the row's warps), each block's amax, scale, reciprocal and codes stay in one
-// lane, codes leave as one 8-byte store per lane per chunk (256 contiguous bytes
-// per warp) and the four scales of four consecutive blocks leave as one 4-byte
-// store into the tiled scale layout.  The element codes come from the correctly
-// rounded quotient fl32(x/e), found without a division unless the quotient sits
-// next to an E2M1 rounding boundary (see e2m1_block_codes).
+// One CTA quantizes one row at a time, thread t owning the 16-value block t of
+// the row.  Rows stream through a ring of shared-memory stages filled by bulk
+// asynchronous copies (one cp.async.bulk per row, completing on the stage's
+// mbarrier), issued several rows ahead by thread 0, so the HBM reads stay in
+// flight while the CTA computes.  Per row: every thread reads its block once
+// from shared memory, the row amax is a warp max-reduction plus one CTA barrier,
+// then each thread derives its block scale and codes in registers.  Codes leave
+// as one 8-byte store per thread (256 contiguous bytes per warp) and the scales
+// of four consecutive blocks as one 4-byte store into the tiled scale layout.
+// Block scales and element codes come from the correctly rounded quotients, found
+// without a division unless a quotient sits next to a rounding boundary (see
+// e4m3_quotient_code and e2m1_block_codes).
 #include "fme_device.cuh"
 #include "fme_launch.h"
 
@@ -28,12 +30,11 @@ __device__ __forceinline__ uint32_t e4m3_code(float v) {
   return r & 0xFFu;
 }
 
-__device__ __forceinline__ float e4m3_value(uint32_t code) {
-  uint32_t h2;
-  uint16_t in = static_cast<uint16_t>(code);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
-  return __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu)));
-}
+// Value of a non-negative, finite E4M3 code.  The code shifted into the top of an
+// fp32 (exponent field = E4M3 exponent field, mantissa = its 3 bits) is the value
+// times 2^-120, also for the E4M3 subnormals (fp32 subnormals then); the
+// multiply by 2^120 is exact.
+__device__ __forceinline__ float e4m3_value(uint32_t code) { return __uint_as_float(code << 20) * 0x1p120f; }
 
 // max(|a|, |b|) per bf16 half (sign bits hold the xor of the input signs).
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
@@ -106,130 +107,159 @@ __device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float 
   return out;
 }
 
-// Row split: WPR warps share one row; warp w of the row takes chunks w, w + WPR,
-// ... (NCH of them, 512 values each; lane l owns the 16-value block l of a
-// chunk), so every warp keeps at most 4 chunks (64 registers of data) in flight.
-// The row amax is combined through shared memory behind a named barrier of the
-// row's warps (slot parity alternates per row, so one barrier per row suffices).
-constexpr int kNvThreads = 256;
-
-__device__ __forceinline__ void row_barrier(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+// E4M3 code of the correctly rounded quotient fl32(v / d), v >= 0, with rd an
+// approximate reciprocal of d (rcp.approx; d normal).  The same bracket as in
+// e2m1_block_codes: fl32(v rd) is within 2^-21.7 of v/d and fl32(v/d) within
+// 2^-24, so if fl32(q (1 - 2^-19)) and fl32(q (1 + 2^-19)) round to the same E4M3
+// code (one cvt converts both), that is the code of fl32(v/d).  Otherwise, or when
+// d is not normal, the quotient is computed with an IEEE division.
+__device__ __forceinline__ uint32_t e4m3_quotient_code(float v, float d, float rd, bool normal_d) {
+  constexpr float kBelow = 1.0f - 1.0f / 524288.0f;
+  constexpr float kAbove = 1.0f + 1.0f / 524288.0f;
+  const float q = __fmul_rn(v, rd);
+  uint16_t pair;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(__fmul_rn(q, kAbove)), "f"(__fmul_rn(q, kBelow)));
+  const uint32_t lo = pair & 0xFFu;
+  if (normal_d && lo == (static_cast<uint32_t>(pair) >> 8)) return lo;
+  return e4m3_code(__fdiv_rn(v, d));
 }
 
-template <int NCH, int WPR>
-__global__ void __launch_bounds__(kNvThreads, 3) nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows,
-                                                                       int k, const int32_t *__restrict__ offsets,
-                                                                       int num_groups, uint8_t *__restrict__ codes,
-                                                                       uint8_t *__restrict__ sf,
-                                                                       float *__restrict__ row_scale,
-                                                                       int32_t *status) {
-  constexpr int kRowsPerCta = (kNvThreads / 32) / WPR;
+constexpr int kNvMaxThreads = 512;        // k <= 8192: 512 blocks of 16
+constexpr int kNvSmemBudget = 220 * 1024;  // shared memory aimed for per SM
+
+__global__ void __launch_bounds__(kNvMaxThreads, 2)
+    nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
+                          int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
+                          float *__restrict__ row_scale, int32_t *status, int stages) {
   __shared__ GroupTable groups;
   __shared__ int ok_flag;
-  __shared__ uint32_t partial[2][kRowsPerCta][WPR];
+  __shared__ int abort_flag;
+  __shared__ uint32_t part[2][kNvMaxThreads / 32];  // per-warp amax of the row, double-buffered by row parity
+  __shared__ int64_t prow_of[2];                     // the row's padded row in the scale layout
+  extern __shared__ __align__(128) uint8_t nv_smem[];
   if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(status, kDevBadOffsets);
     return;
   }
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int slot = warp / WPR;  // row slot of this CTA
-  const int wr = warp % WPR;    // part of the row
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int nblk = k / 16;
+  const bool active = tid < nblk;
+  const uint32_t row_bytes = static_cast<uint32_t>(k) * 2u;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(nv_smem + static_cast<size_t>(stages) * row_bytes);
+  const int64_t first = blockIdx.x;
+  const int64_t stride = gridDim.x;
   const int64_t c4 = ((k / 16) + 3) & ~3;
-  int parity = 0;
 
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + slot; row < rows;
-       row += static_cast<int64_t>(gridDim.x) * kRowsPerCta, parity ^= 1) {
-    const uint16_t *xr = x + row * k;
-    uint4 v[NCH][2];
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int col = (wr + WPR * j) * 512 + lane * 16;
-      if (col < k) {
-        v[j][0] = __ldcs(reinterpret_cast<const uint4 *>(xr + col));
-        v[j][1] = __ldcs(reinterpret_cast<const uint4 *>(xr + col + 8));
-      } else {
-        v[j][0] = make_uint4(0, 0, 0, 0);
-        v[j][1] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      const int64_t r = first + s * stride;
+      if (r >= rows) break;
+      mbar_arrive_expect_tx(&bars[s], row_bytes);
+      bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + r * k, row_bytes, &bars[s]);
+    }
+  }
+
+  // lanes whose quad index is odd read the second 16 bytes of their block first,
+  // so a quarter-warp's 16-byte reads cover all 32 banks
+  const int swap = (tid >> 2) & 1;
+  int i = 0;
+  int64_t row = first;
+  for (; row < rows; ++i, row += stride) {
+    const int s = i % stages;
+    const uint32_t parity = static_cast<uint32_t>(i / stages) & 1u;
+    const bool ok = mbar_wait(&bars[s], parity, &abort_flag, status);
+    const uint8_t *buf = nv_smem + static_cast<size_t>(s) * row_bytes;
+    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    if (ok && active) {
+      a = *reinterpret_cast<const uint4 *>(buf + tid * 32 + 16 * swap);
+      b = *reinterpret_cast<const uint4 *>(buf + tid * 32 + 16 * (1 - swap));
+    }
+    const uint32_t bmax = amax16_bits(a, b);
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, bmax);
+    if (lane == 0) part[i & 1][warp] = wmax;
+    if (tid == 0) {
+      const int g = find_group(groups.off, num_groups, row);
+      prow_of[i & 1] = 128 * static_cast<int64_t>(groups.tiles[g]) + (row - groups.off[g]);
+    }
+    if (__syncthreads_or(!ok)) break;  // every block of stage s is in registers: refill it
+    if (tid == 0) {
+      const int64_t next = row + stages * stride;
+      if (next < rows) {
+        fence_proxy_async_shared();
+        mbar_arrive_expect_tx(&bars[s], row_bytes);
+        bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + next * k, row_bytes, &bars[s]);
       }
     }
-    // block amax per chunk (|x| as bits: bf16 magnitudes order like integers), then row amax
-    uint32_t bmax[NCH];
-    uint32_t amax_bits = 0;
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      bmax[j] = amax16_bits(v[j][0], v[j][1]);
-      amax_bits = max(amax_bits, bmax[j]);
-    }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, s));
-    if (WPR > 1) {
-      if (lane == 0) partial[parity][slot][wr] = amax_bits;
-      row_barrier(1 + slot, WPR * 32);
-#pragma unroll
-      for (int i = 0; i < WPR; ++i) amax_bits = max(amax_bits, partial[parity][slot][i]);
-    }
+    const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, lane < nwarps ? part[i & 1][lane] : 0u);
+    const int64_t prow = prow_of[i & 1];
     const float amax = bf16_bits_to_float(amax_bits);
     const float s_t = (amax_bits == 0) ? 0.0f : __fdiv_rn(amax, 2688.0f);
     const float d = __fmul_rn(6.0f, s_t);
+    const bool normal_d = d >= 1.17549435e-38f;
 
-    // padded row of the scale layout; lanes 0, 4, .., 28 store the scales of
-    // blocks 32 c + lane .. +3, i.e. tile 8 c + lane/4 of this row
-    const int g = find_group(groups.off, num_groups, row);
-    const int64_t prow = 128 * static_cast<int64_t>(groups.tiles[g]) + (row - groups.off[g]);
-    uint8_t *codes_row = codes + row * (k / 2);
-    uint8_t *sf_lane = sf + sf_offset(prow, 4 * (lane >> 2), c4);
-
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int c = wr + WPR * j;
-      const int col = c * 512 + lane * 16;
-      const uint32_t w[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w,
-                             v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
-      uint32_t sb = 0;
-      if (bmax[j] != 0) sb = e4m3_code(__fdiv_rn(bf16_bits_to_float(bmax[j]), d));
-      uint2 packed = make_uint2(0, 0);
-      if (sb != 0) {
-        const float e = __fmul_rn(e4m3_value(sb), s_t);
-        const bool normal_e = e >= 1.17549435e-38f;  // reciprocal finite and accurate
-        packed = e2m1_block_codes(w, e, rcp_approx(e), normal_e);
-      }
-      if (col < k) *reinterpret_cast<uint2 *>(codes_row + col / 2) = packed;
-      // scales: lanes 4g .. 4g+3 hold blocks 32 c + 4g .. +3; lane 4g stores them as one word
-      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
-      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-      if ((lane & 3) == 0 && col < k) {
-        const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
-        *reinterpret_cast<uint32_t *>(sf_lane + c * 4096) = word;
+    uint32_t sb = 0;
+    if (bmax != 0) sb = e4m3_quotient_code(bf16_bits_to_float(bmax), d, rcp_approx(d), normal_d);
+    uint2 packed = make_uint2(0, 0);
+    if (sb != 0) {
+      const float e = __fmul_rn(e4m3_value(sb), s_t);
+      const bool normal_e = e >= 1.17549435e-38f;  // reciprocal finite and accurate
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      packed = e2m1_block_codes(w, e, rcp_approx(e), normal_e);
+      if (swap) packed = make_uint2(packed.y, packed.x);
+    }
+    if (active) *reinterpret_cast<uint2 *>(codes + row * (k / 2) + tid * 8) = packed;
+    // scales: threads 4g .. 4g+3 hold blocks 4g .. 4g+3; thread 4g stores them as one word
+    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+    if ((lane & 3) == 0 && active)
+      *reinterpret_cast<uint32_t *>(sf + sf_offset(prow, tid, c4)) = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    if (tid == 0) row_scale[row] = s_t;
+  }
+  if (row < rows && tid == 0) {
+    // gave up on a stage: wait (bounded) for the copies still in flight into this
+    // CTA's shared memory before it exits
+    const uint64_t t0 = globaltimer();
+    for (int j = i; j < i + stages && first + static_cast<int64_t>(j) * stride < rows; ++j) {
+      const uint32_t parity = static_cast<uint32_t>(j / stages) & 1u;
+      while (!mbar_try_wait(&bars[j % stages], parity) && globaltimer() - t0 < kWaitLimitNs) {
       }
     }
-    if (lane == 0 && wr == 0) row_scale[row] = s_t;
   }
 }
 
-template <int NCH, int WPR>
-static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
-  constexpr int rows_per_cta = (kNvThreads / 32) / WPR;
-  const int64_t blocks_needed = (a.rows + rows_per_cta - 1) / rows_per_cta;
-  const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
-  const int blocks = static_cast<int>(blocks_needed < cap ? (blocks_needed > 0 ? blocks_needed : 1) : cap);
-  nvfp4_pertoken_kernel<NCH, WPR><<<blocks, kNvThreads, 0, a.stream>>>(
-      static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k), a.offsets, a.num_groups, a.codes, a.sf,
-      a.row_scale, a.status);
-  return cudaGetLastError();
-}
-
-// Chunks of 512 values per row: up to 4 per warp, rows of more than 4 chunks are
-// split over 2 or 4 warps (k <= 8192 = 16 chunks).
+// Threads: one per 16-value block, rounded up to whole warps.  CTAs per SM: as
+// many as 1024 threads and the shared-memory budget allow (at least 4 stages
+// each); stages: the rest of the budget, 2 to 16 rows.
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
-  const int chunks = static_cast<int>((a.k + 511) / 512);
-  if (chunks <= 1) return launch_nvfp4<1, 1>(a);
-  if (chunks <= 2) return launch_nvfp4<2, 1>(a);
-  if (chunks <= 4) return launch_nvfp4<4, 1>(a);
-  if (chunks <= 8) return launch_nvfp4<4, 2>(a);
-  return launch_nvfp4<4, 4>(a);
+  const int threads = static_cast<int>(((a.k / 16) + 31) / 32 * 32);
+  const int64_t row_bytes = a.k * 2;
+  const int64_t fixed = static_cast<int64_t>(sizeof(GroupTable)) + 1024;
+  int per_sm = 1024 / threads;
+  const int64_t by_smem = kNvSmemBudget / (4 * row_bytes + fixed);
+  if (per_sm > by_smem) per_sm = static_cast<int>(by_smem > 1 ? by_smem : 1);
+  if (per_sm > 16) per_sm = 16;
+  int64_t stages = (kNvSmemBudget / per_sm - fixed) / row_bytes;
+  stages = stages < 2 ? 2 : (stages > 16 ? 16 : stages);
+  const size_t smem = static_cast<size_t>(stages * row_bytes + stages * 8);
+  cudaError_t err =
+      cudaFuncSetAttribute(nvfp4_pertoken_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int64_t cap = static_cast<int64_t>(a.num_sms) * per_sm;
+  const int blocks = static_cast<int>(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
+  nvfp4_pertoken_kernel<<<blocks, threads, smem, a.stream>>>(
+      static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k), a.offsets, a.num_groups, a.codes, a.sf,
+      a.row_scale, a.status, static_cast<int>(stages));
+  return cudaGetLastError();
 }
 
 }  // namespace fme

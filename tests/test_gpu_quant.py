@@ -136,6 +136,41 @@ def test_nvfp4_groups_pad_scale_rows(fme, orc):
     check_nvfp4(fme, orc, x, off)
 
 
+def test_nvfp4_every_bf16_amax(fme, orc):
+    """Row r holds the r-th positive finite bf16 value (subnormals included) and a
+    few smaller ones: every per-token scale S = amax/2688, every 6 S and the block
+    scale of the amax block, over the whole bf16 range, bit-exact."""
+    mags = np.arange(1, 0x7F80, dtype=np.uint32)            # +subnormals .. +max finite
+    x = np.zeros((mags.size, 64), np.uint16)
+    x[:, 0] = mags
+    x[:, 1] = 0x8000 | (mags >> 1)                          # negative, about half the magnitude
+    x[:, 17] = mags >> 3                                    # second block
+    x[:, 40] = np.maximum(mags, 1) - 1
+    check_nvfp4(fme, orc, x)
+
+
+def test_nvfp4_exact_ties(fme, orc):
+    """Quotients exactly on rounding midpoints, where round-to-nearest-even decides:
+    amax = 2688 * 2^j makes S = 2^j and 6 S exact; the amax block has scale 448 so
+    x = 448 m 2^j sits on the E2M1 midpoint m; a block with amax 6.375 * 2^j
+    divides to 1.0625, an E4M3 midpoint."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    rows = []
+    for j in range(-20, 21, 3):
+        r = np.zeros(64, np.float32)
+        r[0] = 2688.0 * 2.0 ** j
+        for i, m in enumerate(mids):
+            r[1 + i] = 448.0 * m * 2.0 ** j * (-1 if i % 2 else 1)
+        r[16] = 6.375 * 2.0 ** j
+        r[17:24] = [6.375 * 2.0 ** j * v for v in (0.5, 0.25, 0.75, 0.125, -0.375, 0.0625, -1.0)]
+        r[32] = 3.1875 * 2.0 ** j                      # 3.1875 / 6 = 0.53125: between E4M3 grid points
+        r[33] = -448.0 * 5.0 * 2.0 ** j / 2.0 ** 4
+        rows.append(r)
+    x = synth.bf16_bits(np.stack(rows))
+    assert np.array_equal(synth.bf16_float(x), np.stack(rows)), "the tie values must be exact in bf16"
+    check_nvfp4(fme, orc, x)
+
+
 def test_nvfp4_batch_invariance_and_causality(fme, orc):
     """Per-token scales: shuffling, splitting and appending later rows leave every
     row's codes and scales bit-identical."""
