@@ -233,11 +233,12 @@ struct GroupTable {
   int32_t tiles[kMaxGroups + 1];
 };
 
-// Load and check `offsets` (NULL = one group of `rows`) into `t`; the whole
-// block calls it.  Returns false (same value in every thread) if the offsets do
-// not rise from 0 to rows.
-__device__ inline bool load_groups(GroupTable &t, const int32_t *offsets, int32_t num_groups, int64_t rows,
-                                   int *flag) {
+// Load and check `offsets` (NULL = one group of `rows`) into off[0..G] and the
+// running 128-row tile counts into tiles[0..G]; the whole block calls it.
+// Returns false (same value in every thread) if the offsets do not rise from 0
+// to rows.
+__device__ inline bool load_groups(int32_t *off, int32_t *tiles, const int32_t *offsets, int32_t num_groups,
+                                   int64_t rows, int *flag) {
   if (threadIdx.x == 0) {
     bool ok = true;
     int32_t acc = 0;
@@ -248,18 +249,23 @@ __device__ inline bool load_groups(GroupTable &t, const int32_t *offsets, int32_
       if (g > 0) {
         if (v < prev) ok = false;
         int32_t n = v - prev;
-        t.tiles[g - 1] = acc;
+        tiles[g - 1] = acc;
         acc += (n > 0 ? (n + 127) / 128 : 0);
       }
-      t.off[g] = v;
+      off[g] = v;
       prev = v;
     }
-    t.tiles[num_groups] = acc;
+    tiles[num_groups] = acc;
     if (prev != rows) ok = false;
     *flag = ok ? 1 : 0;
   }
   __syncthreads();
   return *flag != 0;
+}
+
+__device__ inline bool load_groups(GroupTable &t, const int32_t *offsets, int32_t num_groups, int64_t rows,
+                                   int *flag) {
+  return load_groups(t.off, t.tiles, offsets, num_groups, rows, flag);
 }
 
 // Group holding row r: the last g with off[g] <= r (skipping empty groups).

@@ -7,18 +7,18 @@
 // q = E2M1(x / e), all divisions correctly rounded (__fdiv_rn), all conversions
 // round-to-nearest-even with saturation.
 //
-// One CTA quantizes one row at a time, thread t owning the 16-value block t of
-// the row.  Rows stream through a ring of shared-memory stages filled by bulk
-// asynchronous copies (one cp.async.bulk per row, completing on the stage's
-// mbarrier), issued several rows ahead by thread 0, so the HBM reads stay in
-// flight while the CTA computes.  Per row: every thread reads its block once
-// from shared memory, the row amax is a warp max-reduction plus one CTA barrier,
-// then each thread derives its block scale and codes in registers.  Codes leave
-// as one 8-byte store per thread (256 contiguous bytes per warp) and the scales
-// of four consecutive blocks as one 4-byte store into the tiled scale layout.
-// Block scales and element codes come from the correctly rounded quotients, found
-// without a division unless a quotient sits next to a rounding boundary (see
-// e4m3_quotient_code and e2m1_block_codes).
+// One CTA quantizes one row at a time; each thread owns R (1 or 2) of the row's
+// 16-value blocks, t and t + T.  Rows stream through a ring of shared-memory
+// stages filled by bulk asynchronous copies (one cp.async.bulk per row,
+// completing on the stage's mbarrier) issued several rows ahead by thread 0, so
+// the HBM reads stay in flight while the CTA computes.  Per row: every thread
+// reads its blocks once from shared memory, the row amax is a warp max-reduction
+// plus one CTA barrier, then each thread derives its block scales and codes in
+// registers.  Codes leave as 8-byte stores (256 contiguous bytes per warp) and
+// the scales of four consecutive blocks as one 4-byte store into the tiled scale
+// layout.  Block scales and element codes come from the correctly rounded
+// quotients, found without a division unless a quotient sits next to a rounding
+// boundary (see e4m3_quotient_code and e2m1_block_codes).
 #include "fme_device.cuh"
 #include "fme_launch.h"
 
@@ -65,6 +65,16 @@ __device__ __forceinline__ float rcp_approx(float v) {
   return r;
 }
 
+// Two E2M1 codes (one byte) of the IEEE quotients fl32(lo/e), fl32(hi/e).
+__device__ __forceinline__ uint32_t e2m1_pair_exact(uint32_t w, float e) {
+  return e2m1_pair(__fdiv_rn(__uint_as_float(w << 16), e), __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), e));
+}
+
+// Bytes 0..3 of a, b, c, d (each holding two codes in its low byte) as one word.
+__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
 // E2M1 codes of the correctly rounded quotients fl32(x_i/e) of the 16 bf16 values
 // of one block (8 words, element 2i in the low half of word i), packed two per
 // byte with the even element in the low nibble, without dividing unless a
@@ -75,16 +85,15 @@ __device__ __forceinline__ float rcp_approx(float v) {
 // relative, and Q = fl32(x/e) by less than 2^-24, so Q lies strictly between
 // fl32(q (1 - 2^-19)) and fl32(q (1 + 2^-19)).  Rounding to the E2M1 grid is
 // monotone in |v| (same sign throughout), so when both ends round to the same
-// code, Q does too.  If that fails for any of the 16 values (a quotient within
-// about 2^-19 of a grid midpoint, e.g. an exact tie), all 16 codes come from the
-// IEEE quotients themselves.  Quotients far below 0.25 round to (signed) zero on
-// every path.  The result is always the codes of fl32(x/e).  Pairs go through
-// the packed f32x2 multiplier.
+// code, Q does too.  The pairs where they differ (a quotient within about 2^-19
+// of a grid midpoint: with per-token scales x/e lands that close to a midpoint
+// in about one block in a hundred) take their codes from the IEEE quotients, as
+// does the whole block when e is not normal.  Quotients far below 0.25 round to
+// (signed) zero on every path.  Pairs go through the packed f32x2 multiplier.
 __device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float e, float r, bool normal_e) {
   constexpr float kBelow = 1.0f - 1.0f / 524288.0f;  // 1 - 2^-19, exact in fp32
   constexpr float kAbove = 1.0f + 1.0f / 524288.0f;  // 1 + 2^-19
-  uint32_t lo[8];
-  uint32_t diff = 0;
+  uint32_t lo[8], hi[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float2 x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
@@ -92,18 +101,23 @@ __device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float 
     const float2 a = __fmul2_rn(q, make_float2(kBelow, kBelow));
     const float2 b = __fmul2_rn(q, make_float2(kAbove, kAbove));
     lo[i] = e2m1_pair(a.x, a.y);
-    diff |= lo[i] ^ e2m1_pair(b.x, b.y);
+    hi[i] = e2m1_pair(b.x, b.y);
   }
-  uint2 out;
-  out.x = __byte_perm(__byte_perm(lo[0], lo[1], 0x0040), __byte_perm(lo[2], lo[3], 0x0040), 0x5410);
-  out.y = __byte_perm(__byte_perm(lo[4], lo[5], 0x0040), __byte_perm(lo[6], lo[7], 0x0040), 0x5410);
-  if (normal_e && diff == 0) return out;
-  uint32_t ex[8];
+  uint2 out = make_uint2(pack4(lo[0], lo[1], lo[2], lo[3]), pack4(lo[4], lo[5], lo[6], lo[7]));
+  const uint2 amb = make_uint2(out.x ^ pack4(hi[0], hi[1], hi[2], hi[3]), out.y ^ pack4(hi[4], hi[5], hi[6], hi[7]));
+  if (!normal_e) {
+    out.x = pack4(e2m1_pair_exact(w[0], e), e2m1_pair_exact(w[1], e), e2m1_pair_exact(w[2], e),
+                  e2m1_pair_exact(w[3], e));
+    out.y = pack4(e2m1_pair_exact(w[4], e), e2m1_pair_exact(w[5], e), e2m1_pair_exact(w[6], e),
+                  e2m1_pair_exact(w[7], e));
+  } else if ((amb.x | amb.y) != 0) {
+    // byte i of amb.x / amb.y: the two codes of word i / word 4 + i are unsettled
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    ex[i] = e2m1_pair(__fdiv_rn(__uint_as_float(w[i] << 16), e), __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), e));
-  out.x = __byte_perm(__byte_perm(ex[0], ex[1], 0x0040), __byte_perm(ex[2], ex[3], 0x0040), 0x5410);
-  out.y = __byte_perm(__byte_perm(ex[4], ex[5], 0x0040), __byte_perm(ex[6], ex[7], 0x0040), 0x5410);
+    for (int i = 0; i < 4; ++i) {
+      if ((amb.x >> (8 * i)) & 0xFFu) out.x = __byte_perm(out.x, e2m1_pair_exact(w[i], e), (0x3210 & ~(0xF << (4 * i))) | (4 << (4 * i)));
+      if ((amb.y >> (8 * i)) & 0xFFu) out.y = __byte_perm(out.y, e2m1_pair_exact(w[4 + i], e), (0x3210 & ~(0xF << (4 * i))) | (4 << (4 * i)));
+    }
+  }
   return out;
 }
 
@@ -124,20 +138,30 @@ __device__ __forceinline__ uint32_t e4m3_quotient_code(float v, float d, float r
   return e4m3_code(__fdiv_rn(v, d));
 }
 
-constexpr int kNvMaxThreads = 512;        // k <= 8192: 512 blocks of 16
+constexpr int kNvMaxThreads = 256;         // threads per CTA: blocks per row / R, rounded up to warps
 constexpr int kNvSmemBudget = 220 * 1024;  // shared memory aimed for per SM
 
-__global__ void __launch_bounds__(kNvMaxThreads, 2)
+// Shared-memory layout of the dynamic part: [stages x row][stages mbarriers]
+// [G+1 group offsets][G+1 tile counts].
+__host__ __device__ __forceinline__ size_t nv_smem_bytes(int stages, int64_t k, int num_groups) {
+  return static_cast<size_t>(stages) * (2 * k + 8) + 8 * static_cast<size_t>(num_groups + 1);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kNvMaxThreads, 4)
     nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
                           int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
                           float *__restrict__ row_scale, int32_t *status, int stages) {
-  __shared__ GroupTable groups;
   __shared__ int ok_flag;
   __shared__ int abort_flag;
   __shared__ uint32_t part[2][kNvMaxThreads / 32];  // per-warp amax of the row, double-buffered by row parity
-  __shared__ int64_t prow_of[2];                     // the row's padded row in the scale layout
+  __shared__ int64_t sf_row_of[2];                   // byte offset of the row's scales (block 0) in sf
   extern __shared__ __align__(128) uint8_t nv_smem[];
-  if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
+  const uint32_t row_bytes = static_cast<uint32_t>(k) * 2u;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(nv_smem + static_cast<size_t>(stages) * row_bytes);
+  int32_t *g_off = reinterpret_cast<int32_t *>(bars + stages);
+  int32_t *g_tiles = g_off + num_groups + 1;
+  if (!load_groups(g_off, g_tiles, offsets, num_groups, rows, &ok_flag)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(status, kDevBadOffsets);
     return;
   }
@@ -145,13 +169,11 @@ __global__ void __launch_bounds__(kNvMaxThreads, 2)
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
+  const int T = blockDim.x;
   const int nblk = k / 16;
-  const bool active = tid < nblk;
-  const uint32_t row_bytes = static_cast<uint32_t>(k) * 2u;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(nv_smem + static_cast<size_t>(stages) * row_bytes);
   const int64_t first = blockIdx.x;
   const int64_t stride = gridDim.x;
-  const int64_t c4 = ((k / 16) + 3) & ~3;
+  const int64_t c4 = (nblk + 3) & ~3;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -171,24 +193,33 @@ __global__ void __launch_bounds__(kNvMaxThreads, 2)
   // lanes whose quad index is odd read the second 16 bytes of their block first,
   // so a quarter-warp's 16-byte reads cover all 32 banks
   const int swap = (tid >> 2) & 1;
-  int i = 0;
+  int i = 0, s = 0;
+  uint32_t parity = 0;
   int64_t row = first;
   for (; row < rows; ++i, row += stride) {
-    const int s = i % stages;
-    const uint32_t parity = static_cast<uint32_t>(i / stages) & 1u;
     const bool ok = mbar_wait(&bars[s], parity, &abort_flag, status);
     const uint8_t *buf = nv_smem + static_cast<size_t>(s) * row_bytes;
-    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-    if (ok && active) {
-      a = *reinterpret_cast<const uint4 *>(buf + tid * 32 + 16 * swap);
-      b = *reinterpret_cast<const uint4 *>(buf + tid * 32 + 16 * (1 - swap));
+    uint4 a[R], b[R];
+    uint32_t bmax[R];
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int blk = tid + j * T;
+      a[j] = make_uint4(0, 0, 0, 0);
+      b[j] = make_uint4(0, 0, 0, 0);
+      if (ok && blk < nblk) {
+        a[j] = *reinterpret_cast<const uint4 *>(buf + blk * 32 + 16 * swap);
+        b[j] = *reinterpret_cast<const uint4 *>(buf + blk * 32 + 16 * (1 - swap));
+      }
+      bmax[j] = amax16_bits(a[j], b[j]);
+      m = max(m, bmax[j]);
     }
-    const uint32_t bmax = amax16_bits(a, b);
-    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, bmax);
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, m);
     if (lane == 0) part[i & 1][warp] = wmax;
     if (tid == 0) {
-      const int g = find_group(groups.off, num_groups, row);
-      prow_of[i & 1] = 128 * static_cast<int64_t>(groups.tiles[g]) + (row - groups.off[g]);
+      const int g = find_group(g_off, num_groups, row);
+      const int64_t prow = 128 * static_cast<int64_t>(g_tiles[g]) + (row - g_off[g]);
+      sf_row_of[i & 1] = sf_offset(prow, 0, c4);
     }
     if (__syncthreads_or(!ok)) break;  // every block of stage s is in registers: refill it
     if (tid == 0) {
@@ -199,67 +230,85 @@ __global__ void __launch_bounds__(kNvMaxThreads, 2)
         bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + next * k, row_bytes, &bars[s]);
       }
     }
+    if (++s == stages) {
+      s = 0;
+      parity ^= 1u;
+    }
     const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, lane < nwarps ? part[i & 1][lane] : 0u);
-    const int64_t prow = prow_of[i & 1];
+    uint8_t *sf_row = sf + sf_row_of[i & 1];
+    uint8_t *codes_row = codes + row * (k / 2);
     const float amax = bf16_bits_to_float(amax_bits);
     const float s_t = (amax_bits == 0) ? 0.0f : __fdiv_rn(amax, 2688.0f);
     const float d = __fmul_rn(6.0f, s_t);
     const bool normal_d = d >= 1.17549435e-38f;
-
-    uint32_t sb = 0;
-    if (bmax != 0) sb = e4m3_quotient_code(bf16_bits_to_float(bmax), d, rcp_approx(d), normal_d);
-    uint2 packed = make_uint2(0, 0);
-    if (sb != 0) {
-      const float e = __fmul_rn(e4m3_value(sb), s_t);
-      const bool normal_e = e >= 1.17549435e-38f;  // reciprocal finite and accurate
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      packed = e2m1_block_codes(w, e, rcp_approx(e), normal_e);
-      if (swap) packed = make_uint2(packed.y, packed.x);
+    const float rd = rcp_approx(d);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int blk = tid + j * T;
+      uint32_t sb = 0;
+      if (bmax[j] != 0) sb = e4m3_quotient_code(bf16_bits_to_float(bmax[j]), d, rd, normal_d);
+      uint2 packed = make_uint2(0, 0);
+      if (sb != 0) {
+        const float e = __fmul_rn(e4m3_value(sb), s_t);
+        const bool normal_e = e >= 1.17549435e-38f;  // reciprocal finite and accurate
+        const uint32_t w[8] = {a[j].x, a[j].y, a[j].z, a[j].w, b[j].x, b[j].y, b[j].z, b[j].w};
+        packed = e2m1_block_codes(w, e, rcp_approx(e), normal_e);
+        if (swap) packed = make_uint2(packed.y, packed.x);
+      }
+      if (blk < nblk) *reinterpret_cast<uint2 *>(codes_row + blk * 8) = packed;
+      // scales: threads 4g .. 4g+3 hold blocks blk .. blk+3 (blk = 4g + jT); thread 4g
+      // stores them as one word
+      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+      if ((lane & 3) == 0 && blk < nblk)
+        *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
     }
-    if (active) *reinterpret_cast<uint2 *>(codes + row * (k / 2) + tid * 8) = packed;
-    // scales: threads 4g .. 4g+3 hold blocks 4g .. 4g+3; thread 4g stores them as one word
-    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
-    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-    if ((lane & 3) == 0 && active)
-      *reinterpret_cast<uint32_t *>(sf + sf_offset(prow, tid, c4)) = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
     if (tid == 0) row_scale[row] = s_t;
   }
   if (row < rows && tid == 0) {
     // gave up on a stage: wait (bounded) for the copies still in flight into this
     // CTA's shared memory before it exits
     const uint64_t t0 = globaltimer();
-    for (int j = i; j < i + stages && first + static_cast<int64_t>(j) * stride < rows; ++j) {
-      const uint32_t parity = static_cast<uint32_t>(j / stages) & 1u;
-      while (!mbar_try_wait(&bars[j % stages], parity) && globaltimer() - t0 < kWaitLimitNs) {
+    for (int j = 0; j < stages && row + j * stride < rows; ++j) {
+      while (!mbar_try_wait(&bars[s], parity) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+      if (++s == stages) {
+        s = 0;
+        parity ^= 1u;
       }
     }
   }
 }
 
-// Threads: one per 16-value block, rounded up to whole warps.  CTAs per SM: as
-// many as 1024 threads and the shared-memory budget allow (at least 4 stages
-// each); stages: the rest of the budget, 2 to 16 rows.
-cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
-  const int threads = static_cast<int>(((a.k / 16) + 31) / 32 * 32);
-  const int64_t row_bytes = a.k * 2;
-  const int64_t fixed = static_cast<int64_t>(sizeof(GroupTable)) + 1024;
+// R = blocks per thread (2 when a row has more than 256 blocks); threads = blocks
+// / R rounded up to warps.  CTAs per SM: as many as 1024 threads and the
+// shared-memory budget allow with at least 3 stages each; stages: the rest of
+// the budget, 3 to 16 rows.
+template <int R>
+static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
+  const int64_t nblk = a.k / 16;
+  const int threads = static_cast<int>(((nblk + R - 1) / R + 31) / 32 * 32);
+  const int64_t fixed = 1024 + 8 * (a.num_groups + 1);
   int per_sm = 1024 / threads;
-  const int64_t by_smem = kNvSmemBudget / (4 * row_bytes + fixed);
-  if (per_sm > by_smem) per_sm = static_cast<int>(by_smem > 1 ? by_smem : 1);
   if (per_sm > 16) per_sm = 16;
-  int64_t stages = (kNvSmemBudget / per_sm - fixed) / row_bytes;
-  stages = stages < 2 ? 2 : (stages > 16 ? 16 : stages);
-  const size_t smem = static_cast<size_t>(stages * row_bytes + stages * 8);
-  cudaError_t err =
-      cudaFuncSetAttribute(nvfp4_pertoken_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  while (per_sm > 1 && per_sm * (static_cast<int64_t>(nv_smem_bytes(3, a.k, 0)) + fixed) > kNvSmemBudget) --per_sm;
+  int64_t stages = (kNvSmemBudget / per_sm - fixed) / (2 * a.k + 8);
+  stages = stages < 3 ? 3 : (stages > 16 ? 16 : stages);
+  const size_t smem = nv_smem_bytes(static_cast<int>(stages), a.k, a.num_groups);
+  cudaError_t err = cudaFuncSetAttribute(nvfp4_pertoken_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int64_t cap = static_cast<int64_t>(a.num_sms) * per_sm;
   const int blocks = static_cast<int>(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
-  nvfp4_pertoken_kernel<<<blocks, threads, smem, a.stream>>>(
+  nvfp4_pertoken_kernel<R><<<blocks, threads, smem, a.stream>>>(
       static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k), a.offsets, a.num_groups, a.codes, a.sf,
       a.row_scale, a.status, static_cast<int>(stages));
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
+  return (a.k / 16 > kNvMaxThreads) ? launch_nvfp4<2>(a) : launch_nvfp4<1>(a);
 }
 
 }  // namespace fme
