@@ -25,9 +25,11 @@
 //   warps 2-9   epilogue (both CTAs): tcgen05.ld its own 128 x 256 fp32
 //               accumulator (each warp a 32-lane quarter and half the columns)
 //               into registers, release it to the leader, then apply the
-//               per-token and per-column FP32 scales (forward), round to bf16 and
-//               store the rows that belong to the expert, overlapping the next
-//               tile's MMAs.
+//               per-token and per-column FP32 scales (forward), round to bf16,
+//               stage 32-row x 16-column boxes in shared memory (32-byte
+//               swizzle, two per warp) and write them with TMA bulk-tensor stores,
+//               overlapping the next tile's MMAs.  A warp whose 32 rows run past
+//               the expert's last row stores its valid rows directly instead.
 // Both CTAs walk the same tile sequence, derived in shared memory from the
 // per-expert offsets: forward and dgrad go expert by expert, 256-row blocks of
 // each expert's rows, 256-column blocks fastest; wgrad goes expert by expert in
@@ -48,6 +50,8 @@ constexpr int kThreads = 352;      // producer, MMA, 8 epilogue warps, scale cop
 constexpr int kCopierWarp = 10;
 constexpr int kSfBuffers = 4;      // tensor-memory scale buffers between the copier and the MMA issuer
 constexpr int kMaxStages = 6;
+constexpr int kOutBoxBytes = 32 * 16 * 2;            // one 32-row x 16-column bf16 box
+constexpr int kOutBytes = 8 * 2 * kOutBoxBytes;      // two staging boxes per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kStageKBytes;
 constexpr int kBBytes = kHalfN * kStageKBytes;
@@ -63,10 +67,9 @@ struct Cfg {
   static constexpr int kSfaCols = 4 * kAtoms;          // tensor-memory columns per stage
   static constexpr int kSfbCols = 8 * kAtoms;
   static constexpr int kSfCols = kSfaCols + kSfbCols;
-  static constexpr int kStages = kFp4 ? 5 : 6;
+  static constexpr int kStages = kFp4 ? 5 : 6;  // ring depth when the shared memory allows
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageTx = 2 * kStageBytes;  // both CTAs' copies land on the leader's barrier
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   static_assert(kStages <= kMaxStages, "stage count");
   static_assert(kBN + kSfBuffers * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
 };
@@ -83,18 +86,31 @@ struct SharedState {
   uint32_t tmem_base;
   int abort_flag;
   int ok_flag;
-  // fwd, dgrad: groups.off = row offsets, groups.tiles = 128-row tile prefix,
-  //             pair_tiles = 256-row tile prefix.
-  // wgrad:      groups.off = padded offsets, groups.tiles = experts by decreasing work.
-  GroupTable groups;
-  int32_t pair_tiles[kMaxGroups + 1];
 };
+
+// Group tables (G + 1 entries each) in dynamic shared memory, after the operand
+// ring and the output staging boxes.
+struct Groups {
+  int32_t *off;    // fwd, dgrad: row offsets;           wgrad: padded offsets
+  int32_t *tiles;  // fwd, dgrad: 128-row tile prefix;   wgrad: experts by decreasing work
+  int32_t *pair;   // fwd, dgrad: 256-row tile prefix
+};
+
+// Dynamic shared memory: [operand ring][output staging][group tables], with
+// 1024 bytes of slack to align the ring for the 128-byte swizzle.
+__host__ __device__ __forceinline__ int64_t ring_bytes(int stages, int stage_bytes) {
+  return (static_cast<int64_t>(stages) * stage_bytes + 1023) / 1024 * 1024;
+}
+__host__ __device__ __forceinline__ int64_t gemm_smem_bytes(int stages, int stage_bytes, int num_groups) {
+  return 1024 + ring_bytes(stages, stage_bytes) + kOutBytes + 12 * static_cast<int64_t>(num_groups + 1);
+}
 
 struct Tile {
   int32_t e;
   int32_t num_k;           // K stages; 0 = expert without rows (wgrad): output zeros
   int32_t rows_valid;      // rows of this CTA's 128 that belong to the expert (may be <= 0)
   int64_t y_off;           // element offset of this CTA's first output element
+  int32_t y_row;           // output row of this CTA's first row (TMA store coordinate)
   int32_t a_y, b_y;        // TMA row coordinates of this CTA's A rows and B half
   int32_t a_x0, b_x0;      // TMA K coordinates (bytes) of the first stage
   int32_t sfa_row;         // 128-row scale block of this CTA's A rows
@@ -104,14 +120,14 @@ struct Tile {
 };
 
 template <GemmKind K>
-__device__ __forceinline__ int64_t total_tiles(const LaunchGemm &p, const SharedState &s) {
+__device__ __forceinline__ int64_t total_tiles(const LaunchGemm &p, const Groups &g) {
   const int64_t nb = p.n / kBN;
   if (K == GemmKind::kWgradMxfp8) return static_cast<int64_t>(p.num_experts) * (p.m / kPairM) * nb;
-  return static_cast<int64_t>(s.pair_tiles[p.num_experts]) * nb;
+  return static_cast<int64_t>(g.pair[p.num_experts]) * nb;
 }
 
 template <GemmKind K>
-__device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const SharedState &s, int64_t t, int rank) {
+__device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const Groups &s, int64_t t, int rank) {
   using C = Cfg<K>;
   Tile tl;
   const int64_t nb_count = p.n / kBN;
@@ -122,14 +138,15 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const SharedState &
     const int64_t rem = t % per;
     const int64_t mb = rem / nb_count;
     const int64_t nb = rem % nb_count;
-    const int e = s.groups.tiles[order];
-    const int32_t p0 = s.groups.off[e];
+    const int e = s.tiles[order];
+    const int32_t p0 = s.off[e];
     const int64_t row0 = mb * kPairM + rank * kBM;
     tl.e = e;
-    tl.num_k = (s.groups.off[e + 1] - p0) / 128;
+    tl.num_k = (s.off[e + 1] - p0) / 128;
     tl.rows_valid = kBM;
     tl.n0 = static_cast<int32_t>(nb * kBN);
     tl.y_off = (static_cast<int64_t>(e) * p.m + row0) * p.n + nb * kBN;
+    tl.y_row = static_cast<int32_t>(static_cast<int64_t>(e) * p.m + row0);
     tl.a_y = static_cast<int32_t>(row0);
     tl.b_y = static_cast<int32_t>(nb * kBN + rank * kHalfN);
     tl.a_x0 = p0;
@@ -141,19 +158,20 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const SharedState &
   } else {
     const int64_t g = t / nb_count;
     const int64_t nb = t % nb_count;
-    const int e = find_group(s.pair_tiles, p.num_experts, g);
-    const int64_t mb = 2 * (g - s.pair_tiles[e]) + rank;  // this CTA's 128-row block within the expert
-    const int64_t r0 = s.groups.off[e] + mb * kBM;
-    const int64_t n_e = s.groups.off[e + 1] - s.groups.off[e];
+    const int e = find_group(s.pair, p.num_experts, g);
+    const int64_t mb = 2 * (g - s.pair[e]) + rank;  // this CTA's 128-row block within the expert
+    const int64_t r0 = s.off[e] + mb * kBM;
+    const int64_t n_e = s.off[e + 1] - s.off[e];
     const int64_t left = n_e - mb * kBM;
     tl.e = e;
     tl.num_k = static_cast<int32_t>(p.k / C::kKPerStage);
     tl.rows_valid = static_cast<int32_t>(left < kBM ? left : kBM);
     tl.n0 = static_cast<int32_t>(nb * kBN);
     tl.y_off = r0 * p.n + nb * kBN;
+    tl.y_row = static_cast<int32_t>(r0);
     tl.a_y = static_cast<int32_t>(r0);
     tl.a_x0 = 0;
-    tl.sfa_row = s.groups.tiles[e] + static_cast<int32_t>(mb);
+    tl.sfa_row = s.tiles[e] + static_cast<int32_t>(mb);
     tl.sfa_x0 = 0;
     if (K == GemmKind::kFwdNvfp4) {
       const int64_t brow = static_cast<int64_t>(e) * p.n + nb * kBN;
@@ -174,16 +192,16 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const SharedState &
 // Build the tile tables (the same in both CTAs of a pair); returns false in
 // every thread for malformed offsets.
 template <GemmKind K>
-__device__ bool prepare(const LaunchGemm &p, SharedState &s) {
+__device__ bool prepare(const LaunchGemm &p, SharedState &s, const Groups &g) {
   if (K != GemmKind::kWgradMxfp8) {
-    if (!load_groups(s.groups, p.offsets, p.num_experts, p.m, &s.ok_flag)) return false;
+    if (!load_groups(g.off, g.tiles, p.offsets, p.num_experts, p.m, &s.ok_flag)) return false;
     if (threadIdx.x == 0) {
       int32_t acc = 0;
       for (int e = 0; e < p.num_experts; ++e) {
-        s.pair_tiles[e] = acc;
-        acc += (s.groups.off[e + 1] - s.groups.off[e] + kPairM - 1) / kPairM;
+        g.pair[e] = acc;
+        acc += (g.off[e + 1] - g.off[e] + kPairM - 1) / kPairM;
       }
-      s.pair_tiles[p.num_experts] = acc;
+      g.pair[p.num_experts] = acc;
     }
     __syncthreads();
     return true;
@@ -195,7 +213,7 @@ __device__ bool prepare(const LaunchGemm &p, SharedState &s) {
     for (int e = 0; e <= p.num_experts; ++e) {
       const int32_t v = __ldg(p.offsets + e);
       if ((e == 0 && v != 0) || v < prev || (v & 127) != 0) ok = false;
-      s.groups.off[e] = v;
+      g.off[e] = v;
       prev = v;
     }
     if (prev > p.lda || prev > p.ldb) ok = false;
@@ -204,24 +222,23 @@ __device__ bool prepare(const LaunchGemm &p, SharedState &s) {
   __syncthreads();
   if (!s.ok_flag) return false;
   for (int e = threadIdx.x; e < p.num_experts; e += blockDim.x) {
-    const int32_t w = s.groups.off[e + 1] - s.groups.off[e];
+    const int32_t w = g.off[e + 1] - g.off[e];
     int rank = 0;
     for (int f = 0; f < p.num_experts; ++f) {
-      const int32_t wf = s.groups.off[f + 1] - s.groups.off[f];
+      const int32_t wf = g.off[f + 1] - g.off[f];
       rank += (wf > w) || (wf == w && f < e);
     }
-    s.groups.tiles[rank] = e;
+    g.tiles[rank] = e;
   }
   __syncthreads();
   return true;
 }
 
-// Scale (forward: (acc * S_x[t]) * S_w[n], fp32), round to bf16 and store 32
-// consecutive outputs of one row.
+// Scale (forward: (acc * S_x[t]) * S_w[n], fp32) and round to bf16 32
+// consecutive outputs of one row, two per word.
 template <GemmKind K>
-__device__ __forceinline__ void store_chunk(__nv_bfloat16 *dst, const uint32_t (&v)[32], float sa,
-                                            const float *sb) {
-  uint32_t packed[16];
+__device__ __forceinline__ void convert_chunk(uint32_t (&packed)[16], const uint32_t (&v)[32], float sa,
+                                              const float *sb) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     float f[4] = {__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
@@ -238,9 +255,29 @@ __device__ __forceinline__ void store_chunk(__nv_bfloat16 *dst, const uint32_t (
     packed[2 * j] = *reinterpret_cast<const uint32_t *>(&lo);
     packed[2 * j + 1] = *reinterpret_cast<const uint32_t *>(&hi);
   }
+}
+
+// The 32 converted outputs of one row straight to global memory.
+template <GemmKind K>
+__device__ __forceinline__ void store_chunk(__nv_bfloat16 *dst, const uint32_t (&v)[32], float sa,
+                                            const float *sb) {
+  uint32_t packed[16];
+  convert_chunk<K>(packed, v, sa, sb);
   uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
   for (int j = 0; j < 4; ++j) d[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+}
+
+// Row `lane` of a 32-row x 16-column bf16 staging box: words w0 .. w0+7 of
+// `packed`.  32-byte rows with the 32-byte swizzle the TMA store reads: the
+// 16-byte chunk j of row r sits at chunk j ^ ((r >> 2) & 1), so a quarter-warp's
+// stores cover all 32 banks.
+__device__ __forceinline__ void stage_row(uint8_t *box, int lane, const uint32_t (&packed)[16], int w0) {
+  uint8_t *row = box + lane * 32;
+  const int x = (lane >> 2) & 1;
+  *reinterpret_cast<uint4 *>(row + 16 * x) = make_uint4(packed[w0], packed[w0 + 1], packed[w0 + 2], packed[w0 + 3]);
+  *reinterpret_cast<uint4 *>(row + 16 * (1 - x)) =
+      make_uint4(packed[w0 + 4], packed[w0 + 5], packed[w0 + 6], packed[w0 + 7]);
 }
 
 template <GemmKind K>
@@ -248,11 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   using C = Cfg<K>;
   __shared__ SharedState s;
   extern __shared__ uint8_t dyn_smem[];
+  const int S = p.stages;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   uint8_t *smem_a = smem;
-  uint8_t *smem_b = smem_a + C::kStages * kABytes;
-  uint8_t *smem_sfa = smem_b + C::kStages * kBBytes;
-  uint8_t *smem_sfb = smem_sfa + C::kStages * C::kSfaBytes;
+  uint8_t *smem_b = smem_a + S * kABytes;
+  uint8_t *smem_sfa = smem_b + S * kBBytes;
+  uint8_t *smem_sfb = smem_sfa + S * C::kSfaBytes;
+  uint8_t *smem_out = smem + ring_bytes(S, C::kStageBytes);
+  int32_t *gmem = reinterpret_cast<int32_t *>(smem_out + kOutBytes);
+  const Groups grp{gmem, gmem + (p.num_experts + 1), gmem + 2 * (p.num_experts + 1)};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -261,12 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   const int64_t pairs = gridDim.x >> 1;
 
   // Both CTAs of a pair see the same offsets, so both return here or neither does.
-  if (!prepare<K>(p, s)) {
+  if (!prepare<K>(p, s, grp)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(p.status, kDevBadOffsets);
     return;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < S; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
@@ -297,13 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   volatile int *abort_flag = &s.abort_flag;
-  const int64_t total = total_tiles<K>(p, s);
+  const int64_t total = total_tiles<K>(p, grp);
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
     uint32_t stage = 0, phase = 0;
     for (int64_t t = pair_id; t < total; t += pairs) {
-      const Tile tl = tile_at<K>(p, s, t, rank);
+      const Tile tl = tile_at<K>(p, grp, t, rank);
       bool stop = false;
       for (int ks = 0; ks < tl.num_k; ++ks) {
         if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.status)) {
@@ -318,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                           tl.sfa_row);
         pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
                           tl.sfb_row);
-        if (++stage == C::kStages) {
+        if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
@@ -331,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
-      const Tile tl = tile_at<K>(p, s, t, 0);
+      const Tile tl = tile_at<K>(p, grp, t, 0);
       if (tl.num_k == 0) continue;
       if (!mbar_wait(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
       tc_fence_after();
@@ -358,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         pair::commit_both(&s.empty[stage]);
         pair::commit_local(&s.sf_empty[buf]);
-        if (++stage == C::kStages) {
+        if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
@@ -385,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
-      const Tile tl = tile_at<K>(p, s, t, 0);
+      const Tile tl = tile_at<K>(p, grp, t, 0);
       for (int ks = 0; ks < tl.num_k; ++ks) {
         if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
             !mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status)) {
@@ -404,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
         }
         pair::commit_local(&s.sf_full[buf]);
-        if (++stage == C::kStages) {
+        if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
@@ -428,10 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int r = q * 32 + lane;
     const int c0 = half * (kBN / 2);
     const uint32_t leader_acc_empty = pair::map_to_rank(&s.acc_empty, 0);
+    uint8_t *boxes = smem_out + (warp - 2) * 2 * kOutBoxBytes;
+    int box = 0;
     uint32_t acc_phase = 0;
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
     for (int64_t t = pair_id; t < total; t += pairs) {
-      const Tile tl = tile_at<K>(p, s, t, rank);
+      const Tile tl = tile_at<K>(p, grp, t, rank);
       const bool valid = r < tl.rows_valid;
       __nv_bfloat16 *yrow = y + tl.y_off + static_cast<int64_t>(r) * p.n + c0;
       if (tl.num_k == 0) {
@@ -458,13 +501,39 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (valid) sa = __ldg(p.a_scale + tl.a_y + r);
         sb_row = p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0 + c0;
       }
-      if (valid) {
+      if (32 * q + 32 <= tl.rows_valid) {
+        // all 32 rows of this warp are the expert's: stage 32 x 16 boxes, TMA-store them
+        auto emit = [&](const uint32_t(&v)[32], int c) {
+          uint32_t packed[16];
+          convert_chunk<K>(packed, v, sa, sb_row ? sb_row + 32 * c : nullptr);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint8_t *bx = boxes + box * kOutBoxBytes;
+            if (lane == 0) bulk_wait_read<1>();  // the store issued from this box two boxes ago has read it
+            __syncwarp();
+            stage_row(bx, lane, packed, 8 * h);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.map_y, bx, tl.n0 + c0 + 32 * c + 16 * h, tl.y_row + 32 * q);
+              bulk_commit();
+            }
+            box ^= 1;
+          }
+        };
+        emit(v0, 0);
+        emit(v1, 1);
+        emit(v2, 2);
+        emit(v3, 3);
+      } else if (valid) {
         store_chunk<K>(yrow, v0, sa, sb_row);
         store_chunk<K>(yrow + 32, v1, sa, sb_row ? sb_row + 32 : nullptr);
         store_chunk<K>(yrow + 64, v2, sa, sb_row ? sb_row + 64 : nullptr);
         store_chunk<K>(yrow + 96, v3, sa, sb_row ? sb_row + 96 : nullptr);
       }
     }
+    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has written global memory
+    __syncwarp();
   }
 
   // Teardown: the pair meets once the leader's MMAs are drained and every
@@ -480,11 +549,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   }
 }
 
+// Shared memory per CTA for the dynamic part (the static part is small).
+constexpr int64_t kGemmSmemLimit = 227 * 1024 - 1024;
+
 template <GemmKind K>
-static cudaError_t launch_kind(const LaunchGemm &a) {
+static cudaError_t launch_kind(const LaunchGemm &in) {
   using C = Cfg<K>;
+  LaunchGemm a = in;
+  a.stages = C::kStages;
+  while (a.stages > 2 && gemm_smem_bytes(a.stages, C::kStageBytes, a.num_experts) > kGemmSmemLimit) --a.stages;
+  const int smem_bytes = static_cast<int>(gemm_smem_bytes(a.stages, C::kStageBytes, a.num_experts));
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+                                         smem_bytes);
   if (err != cudaSuccess) return err;
   int64_t bound;
   if (K == GemmKind::kWgradMxfp8)
@@ -496,7 +572,7 @@ static cudaError_t launch_kind(const LaunchGemm &a) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
