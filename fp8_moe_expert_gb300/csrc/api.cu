@@ -127,28 +127,6 @@ fme_status encode_scales_2d(CUtensorMap *map, const void *base, uint64_t row_blo
   return FME_OK;
 }
 
-// bf16 output [rows x cols] for the GEMM epilogue's TMA stores: boxes of 16
-// columns (32 bytes) x 32 rows, 32-byte swizzle.
-fme_status encode_out_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows) {
-  EncodeTiledFn fn;
-  fme_status st = get_encoder(&fn);
-  if (st != FME_OK) return st;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {16, 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    char buf[96];
-    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (output) failed (CUresult %d)", static_cast<int>(r));
-    g_last_cuda_error = buf;
-    return FME_ERR_CUDA;
-  }
-  return FME_OK;
-}
-
 int64_t padded_rows_bound(int64_t rows, int32_t groups) {
   if (rows < 0 || groups < 1) return 0;
   return ((rows + 127 * static_cast<int64_t>(groups)) / 128) * 128;
@@ -301,7 +279,6 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * n / 128, (k / 64) * 512, 4, 2)) !=
       FME_OK)
     return st;
-  if ((st = encode_out_bf16(&a.map_y, y, n, m)) != FME_OK) return st;
   a.a_scale = a_scale;
   a.b_scale = b_scale;
   a.offsets = offsets;
@@ -341,7 +318,6 @@ fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
       FME_OK)
     return st;
   if ((st = encode_scales_2d(&a.map_sfb, b_sf, n / 128, (ldb / 128) * 512, 1, 2)) != FME_OK) return st;
-  if ((st = encode_out_bf16(&a.map_y, y, n, m)) != FME_OK) return st;
   a.offsets = offsets;
   a.num_experts = num_experts;
   a.m = m;
@@ -391,7 +367,6 @@ fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
     return st;
   if ((st = encode_scales_2d(&a.map_sfb, sbbase, has_positions ? n / 128 : 2, (ldb_e / 128) * 512, 1, 2)) != FME_OK)
     return st;
-  if ((st = encode_out_bf16(&a.map_y, y, n, static_cast<uint64_t>(num_experts) * m)) != FME_OK) return st;
   a.offsets = padded_offsets;
   a.num_experts = num_experts;
   a.m = m;

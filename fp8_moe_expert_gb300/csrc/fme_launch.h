@@ -39,7 +39,6 @@ struct LaunchGemm {
   GemmKind kind;
   CUtensorMap map_a, map_b;      // operand codes, uint8, 128-byte swizzle
   CUtensorMap map_sfa, map_sfb;  // tiled scales viewed as [128-row blocks x 8-byte words]
-  CUtensorMap map_y;             // bf16 output rows, boxes of 32 rows x 16 columns, 32-byte swizzle (TMA stores)
   const float *a_scale, *b_scale;  // forward only
   const int32_t *offsets;          // row offsets (fwd, dgrad) or padded offsets (wgrad)
   int32_t num_experts;

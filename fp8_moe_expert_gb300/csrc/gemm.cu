@@ -26,10 +26,10 @@
 //               accumulator (each warp a 32-lane quarter and half the columns)
 //               into registers, release it to the leader, then apply the
 //               per-token and per-column FP32 scales (forward), round to bf16,
-//               stage 32-row x 16-column boxes in shared memory (32-byte
-//               swizzle, two per warp) and write them with TMA bulk-tensor stores,
-//               overlapping the next tile's MMAs.  A warp whose 32 rows run past
-//               the expert's last row stores its valid rows directly instead.
+//               and transpose each 32 x 32 block through shared memory so that a
+//               store instruction writes 64 contiguous bytes of each of 8 rows
+//               (rows past the expert's last row are skipped), overlapping the
+//               next tile's MMAs.
 // Both CTAs walk the same tile sequence, derived in shared memory from the
 // per-expert offsets: forward and dgrad go expert by expert, 256-row blocks of
 // each expert's rows, 256-column blocks fastest; wgrad goes expert by expert in
@@ -50,8 +50,9 @@ constexpr int kThreads = 352;      // producer, MMA, 8 epilogue warps, scale cop
 constexpr int kCopierWarp = 10;
 constexpr int kSfBuffers = 4;      // tensor-memory scale buffers between the copier and the MMA issuer
 constexpr int kMaxStages = 6;
-constexpr int kOutBoxBytes = 32 * 16 * 2;            // one 32-row x 16-column bf16 box
-constexpr int kOutBytes = 8 * 2 * kOutBoxBytes;      // two staging boxes per epilogue warp
+constexpr int kOutBoxBytes = 32 * 32 * 2;            // one 32-row x 32-column bf16 block
+constexpr int kSwBytes = 128 * 4;                    // a warp's 128 column scales (forward)
+constexpr int kOutBytes = 8 * (kOutBoxBytes + kSwBytes);  // staging block + column scales per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = kBM * kStageKBytes;
 constexpr int kBBytes = kHalfN * kStageKBytes;
@@ -110,7 +111,6 @@ struct Tile {
   int32_t num_k;           // K stages; 0 = expert without rows (wgrad): output zeros
   int32_t rows_valid;      // rows of this CTA's 128 that belong to the expert (may be <= 0)
   int64_t y_off;           // element offset of this CTA's first output element
-  int32_t y_row;           // output row of this CTA's first row (TMA store coordinate)
   int32_t a_y, b_y;        // TMA row coordinates of this CTA's A rows and B half
   int32_t a_x0, b_x0;      // TMA K coordinates (bytes) of the first stage
   int32_t sfa_row;         // 128-row scale block of this CTA's A rows
@@ -146,7 +146,6 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const Groups &s, in
     tl.rows_valid = kBM;
     tl.n0 = static_cast<int32_t>(nb * kBN);
     tl.y_off = (static_cast<int64_t>(e) * p.m + row0) * p.n + nb * kBN;
-    tl.y_row = static_cast<int32_t>(static_cast<int64_t>(e) * p.m + row0);
     tl.a_y = static_cast<int32_t>(row0);
     tl.b_y = static_cast<int32_t>(nb * kBN + rank * kHalfN);
     tl.a_x0 = p0;
@@ -168,7 +167,6 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const Groups &s, in
     tl.rows_valid = static_cast<int32_t>(left < kBM ? left : kBM);
     tl.n0 = static_cast<int32_t>(nb * kBN);
     tl.y_off = r0 * p.n + nb * kBN;
-    tl.y_row = static_cast<int32_t>(r0);
     tl.a_y = static_cast<int32_t>(r0);
     tl.a_x0 = 0;
     tl.sfa_row = s.tiles[e] + static_cast<int32_t>(mb);
@@ -234,50 +232,54 @@ __device__ bool prepare(const LaunchGemm &p, SharedState &s, const Groups &g) {
   return true;
 }
 
-// Scale (forward: (acc * S_x[t]) * S_w[n], fp32) and round to bf16 32
-// consecutive outputs of one row, two per word.
+// Scale (forward: (acc * S_x[t]) * S_w[n], fp32, two values per packed f32x2
+// multiply) and round to bf16 32 consecutive outputs of one row, two per word.
+// `sw` (forward) points at the 32 column scales in shared memory; every lane
+// reads the same addresses (broadcast).
 template <GemmKind K>
 __device__ __forceinline__ void convert_chunk(uint32_t (&packed)[16], const uint32_t (&v)[32], float sa,
-                                              const float *sb) {
+                                              const float *sw) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    float f[4] = {__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                  __uint_as_float(v[4 * j + 3])};
+    float2 f0 = make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
+    float2 f1 = make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
     if (K == GemmKind::kFwdNvfp4) {
-      const float4 b = __ldg(reinterpret_cast<const float4 *>(sb) + j);
-      f[0] = __fmul_rn(__fmul_rn(f[0], sa), b.x);
-      f[1] = __fmul_rn(__fmul_rn(f[1], sa), b.y);
-      f[2] = __fmul_rn(__fmul_rn(f[2], sa), b.z);
-      f[3] = __fmul_rn(__fmul_rn(f[3], sa), b.w);
+      const float4 b = *reinterpret_cast<const float4 *>(sw + 4 * j);
+      f0 = __fmul2_rn(__fmul2_rn(f0, make_float2(sa, sa)), make_float2(b.x, b.y));
+      f1 = __fmul2_rn(__fmul2_rn(f1, make_float2(sa, sa)), make_float2(b.z, b.w));
     }
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(f0.x, f0.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(f1.x, f1.y);
     packed[2 * j] = *reinterpret_cast<const uint32_t *>(&lo);
     packed[2 * j + 1] = *reinterpret_cast<const uint32_t *>(&hi);
   }
 }
 
-// The 32 converted outputs of one row straight to global memory.
-template <GemmKind K>
-__device__ __forceinline__ void store_chunk(__nv_bfloat16 *dst, const uint32_t (&v)[32], float sa,
-                                            const float *sb) {
-  uint32_t packed[16];
-  convert_chunk<K>(packed, v, sa, sb);
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
+// A 32 x 32 block of bf16 outputs (row `lane` of the warp's 32 rows in
+// `packed`) to global memory through the warp's 2 KB staging block: row r's
+// 16-byte chunk j goes to chunk j ^ ((r >> 1) & 3) of its 64-byte staging row
+// (conflict-free writes and reads), then lane l writes chunk l % 4 of row
+// 8 i + l / 4 for i = 0..3: each store instruction covers 64 contiguous bytes of
+// 8 rows.  Rows at or past `rows_valid` are not written.
+__device__ __forceinline__ void store_block(__nv_bfloat16 *dst, int64_t ld, int rows_valid, uint8_t *stage,
+                                            int lane, const uint32_t (&packed)[16]) {
+  {
+    uint8_t *row = stage + lane * 64;
+    const int x = (lane >> 1) & 3;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) d[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-}
-
-// Row `lane` of a 32-row x 16-column bf16 staging box: words w0 .. w0+7 of
-// `packed`.  32-byte rows with the 32-byte swizzle the TMA store reads: the
-// 16-byte chunk j of row r sits at chunk j ^ ((r >> 2) & 1), so a quarter-warp's
-// stores cover all 32 banks.
-__device__ __forceinline__ void stage_row(uint8_t *box, int lane, const uint32_t (&packed)[16], int w0) {
-  uint8_t *row = box + lane * 32;
-  const int x = (lane >> 2) & 1;
-  *reinterpret_cast<uint4 *>(row + 16 * x) = make_uint4(packed[w0], packed[w0 + 1], packed[w0 + 2], packed[w0 + 3]);
-  *reinterpret_cast<uint4 *>(row + 16 * (1 - x)) =
-      make_uint4(packed[w0 + 4], packed[w0 + 5], packed[w0 + 6], packed[w0 + 7]);
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4 *>(row + 16 * (j ^ x)) =
+          make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+  }
+  __syncwarp();
+  const int j = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const uint4 v = *reinterpret_cast<const uint4 *>(stage + r * 64 + 16 * (j ^ ((r >> 1) & 3)));
+    if (r < rows_valid) *reinterpret_cast<uint4 *>(dst + r * ld + 8 * j) = v;
+  }
+  __syncwarp();
 }
 
 template <GemmKind K>
@@ -469,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int r = q * 32 + lane;
     const int c0 = half * (kBN / 2);
     const uint32_t leader_acc_empty = pair::map_to_rank(&s.acc_empty, 0);
-    uint8_t *boxes = smem_out + (warp - 2) * 2 * kOutBoxBytes;
-    int box = 0;
+    uint8_t *stage_blk = smem_out + (warp - 2) * kOutBoxBytes;
+    float *sw = reinterpret_cast<float *>(smem_out + 8 * kOutBoxBytes + (warp - 2) * kSwBytes);
     uint32_t acc_phase = 0;
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
     for (int64_t t = pair_id; t < total; t += pairs) {
@@ -481,6 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (valid)
           for (int c = 0; c < kBN / 2; c += 8) *reinterpret_cast<uint4 *>(yrow + c) = make_uint4(0, 0, 0, 0);
         continue;
+      }
+      // the forward's scales of this warp's rows and columns, fetched while the MMAs run
+      float sa = 1.0f;
+      float4 swv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (K == GemmKind::kFwdNvfp4) {
+        if (valid) sa = __ldg(p.a_scale + tl.a_y + r);
+        swv = __ldg(reinterpret_cast<const float4 *>(p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0 + c0) +
+                    lane);
       }
       if (!mbar_wait(&s.acc_full, acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
@@ -495,45 +505,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       __syncwarp();
       if (lane == 0) pair::arrive_remote(leader_acc_empty);
       acc_phase ^= 1;
-      float sa = 1.0f;
-      const float *sb_row = nullptr;
       if (K == GemmKind::kFwdNvfp4) {
-        if (valid) sa = __ldg(p.a_scale + tl.a_y + r);
-        sb_row = p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0 + c0;
+        reinterpret_cast<float4 *>(sw)[lane] = swv;
+        __syncwarp();
       }
-      if (32 * q + 32 <= tl.rows_valid) {
-        // all 32 rows of this warp are the expert's: stage 32 x 16 boxes, TMA-store them
+      const int warp_rows = tl.rows_valid - 32 * q;  // rows of this warp's 32 that are the expert's
+      if (warp_rows > 0) {
+        __nv_bfloat16 *ywarp = y + tl.y_off + static_cast<int64_t>(32 * q) * p.n + c0;
         auto emit = [&](const uint32_t(&v)[32], int c) {
           uint32_t packed[16];
-          convert_chunk<K>(packed, v, sa, sb_row ? sb_row + 32 * c : nullptr);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint8_t *bx = boxes + box * kOutBoxBytes;
-            if (lane == 0) bulk_wait_read<1>();  // the store issued from this box two boxes ago has read it
-            __syncwarp();
-            stage_row(bx, lane, packed, 8 * h);
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&p.map_y, bx, tl.n0 + c0 + 32 * c + 16 * h, tl.y_row + 32 * q);
-              bulk_commit();
-            }
-            box ^= 1;
-          }
+          convert_chunk<K>(packed, v, sa, sw + 32 * c);
+          store_block(ywarp + 32 * c, p.n, warp_rows, stage_blk, lane, packed);
         };
         emit(v0, 0);
         emit(v1, 1);
         emit(v2, 2);
         emit(v3, 3);
-      } else if (valid) {
-        store_chunk<K>(yrow, v0, sa, sb_row);
-        store_chunk<K>(yrow + 32, v1, sa, sb_row ? sb_row + 32 : nullptr);
-        store_chunk<K>(yrow + 64, v2, sa, sb_row ? sb_row + 64 : nullptr);
-        store_chunk<K>(yrow + 96, v3, sa, sb_row ? sb_row + 96 : nullptr);
       }
     }
-    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has written global memory
-    __syncwarp();
   }
 
   // Teardown: the pair meets once the leader's MMAs are drained and every
