@@ -21,13 +21,6 @@ __device__ __forceinline__ uint32_t mx_code_from_bf16_amax(uint32_t amax_bits) {
 // 2^(127 - code) as an fp32 (code in [0, 246] for bf16 inputs: always normal).
 __device__ __forceinline__ float mx_inv_scale(uint32_t code) { return __uint_as_float((254u - code) << 23); }
 
-// Per-halfword unsigned max of two words of packed bf16 magnitudes.
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 // Two E4M3 codes: `lo` in bits 0..7, `hi` in bits 8..15.
 __device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
   uint16_t r;
@@ -35,13 +28,24 @@ __device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
   return r;
 }
 
-// Four bf16 (two words) times s -> four E4M3 codes in one word.
-__device__ __forceinline__ uint32_t quad_codes(uint32_t w0, uint32_t w1, float s) {
-  const uint32_t p0 = e4m3_pair(__fmul_rn(bf16_bits_to_float(w0 & 0xFFFFu), s),
-                                __fmul_rn(bf16_bits_to_float(w0 >> 16), s));
-  const uint32_t p1 = e4m3_pair(__fmul_rn(bf16_bits_to_float(w1 & 0xFFFFu), s),
-                                __fmul_rn(bf16_bits_to_float(w1 >> 16), s));
-  return p0 | (p1 << 16);
+// max(|a|, |b|) per bf16 half (sign bits hold the xor of the input signs).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Two values given as fp32 bit patterns (bf16 widened) times s, one packed
+// multiply (exact: s is a power of two) -> two E4M3 codes, `lo` in bits 0..7.
+__device__ __forceinline__ uint32_t e4m3x2_scaled(uint32_t lo, uint32_t hi, float s) {
+  const float2 p = __fmul2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)), make_float2(s, s));
+  return e4m3_pair(p.x, p.y);
+}
+
+// The two bf16 of each of words a, b (elements a.lo, a.hi, b.lo, b.hi) times s
+// -> four E4M3 codes in element order.
+__device__ __forceinline__ uint32_t e4m3x4_words(uint32_t a, uint32_t b, float s) {
+  return __byte_perm(e4m3x2_scaled(a << 16, a & 0xFFFF0000u, s), e4m3x2_scaled(b << 16, b & 0xFFFF0000u, s), 0x5410);
 }
 
 // ---------------------------------------------------------------- row-wise --
@@ -81,20 +85,15 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
 #pragma unroll
       for (int u = 0; u < kRowUnroll; ++u) {
         const int col = base + u * 256 + lane * 8;
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        uint32_t bmax = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          bmax = max(bmax, w[i] & 0x7FFFu);
-          bmax = max(bmax, (w[i] >> 16) & 0x7FFFu);
-        }
+        const uint32_t bm = absmax_bf16x2(absmax_bf16x2(v[u].x, v[u].y), absmax_bf16x2(v[u].z, v[u].w));
+        uint32_t bmax = max(bm & 0x7FFFu, (bm >> 16) & 0x7FFFu);
         bmax = max(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
         bmax = max(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 2));
         const uint32_t code = mx_code_from_bf16_amax(bmax);
         const float s = mx_inv_scale(code);
         uint2 out;
-        out.x = quad_codes(w[0], w[1], s);
-        out.y = quad_codes(w[2], w[3], s);
+        out.x = e4m3x4_words(v[u].x, v[u].y, s);
+        out.y = e4m3x4_words(v[u].z, v[u].w, s);
         if (col < cols) *reinterpret_cast<uint2 *>(cr + col) = out;
         const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 4);
         const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 8);
@@ -112,20 +111,41 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
 // ------------------------------------------------------------- column-wise --
 // Tile = 128 padded positions (one 128-chunk of one group) x 128 columns.  The
 // CTA stages the 128 x 128 bf16 tile in shared memory (rows past the group's end
-// read as zeros), each thread quantizes one 32-block of two adjacent columns, the codes
-// are staged transposed and leave as 128-byte rows, and the 128 x 4 scales of
-// the tile are exactly one 512-byte tile of the scale layout.
+// read as zeros; the next tile is already in registers), each thread quantizes
+// one 32-block of two adjacent columns, the codes are staged transposed and
+// leave as 128-byte rows, and the 128 x 4 scales of the tile are exactly one
+// 512-byte tile of the scale layout.  A CTA walks tiles t = blockIdx.x, +gridDim.x,
+// ... as (chunk, column block) pairs updated incrementally (no division), and
+// the chunk's group only moves forward.
 constexpr int kColTilePad = 8;  // bf16 elements of padding per staged row
 constexpr int kColTileBytes = 128 * (128 + kColTilePad) * 2;
 constexpr int kColOutBytes = 128 * (128 + 16);
 constexpr int kColSmemBytes = kColTileBytes + kColOutBytes + 512 + 512;
+
+// One tile of the walk: chunk j of the padded positions, column block cb, the
+// chunk's group g, its first source row and how many of its 128 rows exist.
+struct ColTile {
+  int64_t j;
+  int cb;
+  int g;
+  int valid;
+  int64_t src0;
+};
+
+__device__ __forceinline__ void col_tile_locate(ColTile &t, const GroupTable &groups, int num_groups) {
+  while (t.g + 1 < num_groups && groups.tiles[t.g + 1] <= t.j) ++t.g;
+  const int64_t local0 = 128 * (t.j - groups.tiles[t.g]);
+  const int64_t n_g = groups.off[t.g + 1] - groups.off[t.g];
+  t.valid = static_cast<int>(n_g - local0 < 128 ? n_g - local0 : 128);
+  t.src0 = groups.off[t.g] + local0;
+}
 
 // kRows: also quantize the same tile row-wise (blocks of 32 along each row), so a
 // tensor needed both ways is read once.  The tile's 128 padded positions are the
 // row-wise scale layout's 128-row block j (both pad each group to 128 rows), so
 // its row-wise scales are one 512-byte tile too.
 template <bool kRows>
-__global__ void __launch_bounds__(256, 3) mxfp8_cols_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
+__global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
                                                          const int32_t *__restrict__ offsets, int num_groups,
                                                          uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
                                                          int64_t ld, int32_t *__restrict__ padded_offsets,
@@ -154,38 +174,48 @@ __global__ void __launch_bounds__(256, 3) mxfp8_cols_kernel(const uint16_t *__re
   }
   const int cblocks = cols / 128;
   const int64_t total = chunks * cblocks;
+  const int64_t dj = gridDim.x / cblocks;
+  const int dcb = gridDim.x % cblocks;
+  auto advance = [&](ColTile &t) {
+    t.j += dj;
+    t.cb += dcb;
+    if (t.cb >= cblocks) {
+      t.cb -= cblocks;
+      ++t.j;
+    }
+  };
 
-  // Tile t -> (chunk j, column block cb); the next tile's 32 KB is loaded into
-  // registers while the current one is quantized and stored.
-  auto load_tile = [&](int64_t t, uint4 (&dst)[8]) {
-    const int64_t j = t / cblocks;
-    const int cb = static_cast<int>(t % cblocks);
-    const int g = find_group(groups.tiles, num_groups, j);
-    const int64_t local0 = 128 * (j - groups.tiles[g]);
-    const int64_t n_g = groups.off[g + 1] - groups.off[g];
-    const int valid = static_cast<int>(n_g - local0 < 128 ? n_g - local0 : 128);
-    const int64_t src0 = groups.off[g] + local0;
+  auto load_tile = [&](const ColTile &t, uint4 (&dst)[8]) {
 #pragma unroll
     for (int pass = 0; pass < 8; ++pass) {
       const int r = pass * 16 + (tid >> 4);
       const int seg = tid & 15;
-      dst[pass] = (r < valid)
-                      ? __ldcs(reinterpret_cast<const uint4 *>(x + (src0 + r) * cols + cb * 128 + seg * 8))
+      dst[pass] = (r < t.valid)
+                      ? __ldcs(reinterpret_cast<const uint4 *>(x + (t.src0 + r) * cols + t.cb * 128 + seg * 8))
                       : make_uint4(0, 0, 0, 0);
     }
   };
+  ColTile cur{static_cast<int64_t>(blockIdx.x) / cblocks, static_cast<int>(blockIdx.x % cblocks), 0, 0, 0};
   uint4 pre[8];
-  if (static_cast<int64_t>(blockIdx.x) < total) load_tile(blockIdx.x, pre);
+  if (cur.j < chunks) {
+    col_tile_locate(cur, groups, num_groups);
+    load_tile(cur, pre);
+  }
+  ColTile nxt = cur;
+  advance(nxt);
 
   for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-    const int64_t j = t / cblocks;
-    const int cb = static_cast<int>(t % cblocks);
+    const int64_t j = cur.j;
+    const int cb = cur.cb;
     __syncthreads();  // the previous tile's shared buffers are free
 #pragma unroll
     for (int pass = 0; pass < 8; ++pass)
       *reinterpret_cast<uint4 *>(&tile[pass * 16 + (tid >> 4)][(tid & 15) * 8]) = pre[pass];
     __syncthreads();
-    if (t + gridDim.x < total) load_tile(t + gridDim.x, pre);
+    if (nxt.j < chunks) {
+      col_tile_locate(nxt, groups, num_groups);
+      load_tile(nxt, pre);
+    }
 
     // thread = (channel pair cp, 32-position block b): both channels' 32 values
     // come in with one 32-bit shared load per position
@@ -197,37 +227,38 @@ __global__ void __launch_bounds__(256, 3) mxfp8_cols_kernel(const uint16_t *__re
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         vals[i] = *reinterpret_cast<const uint32_t *>(&tile[32 * b + i][2 * cp]);
-        m = max_u16x2(m, vals[i] & 0x7FFF7FFFu);
+        m = absmax_bf16x2(m, vals[i]);
       }
+      const uint32_t code_lo = mx_code_from_bf16_amax(m & 0x7FFFu);
+      const uint32_t code_hi = mx_code_from_bf16_amax((m >> 16) & 0x7FFFu);
+      const float s_lo = mx_inv_scale(code_lo);
+      const float s_hi = mx_inv_scale(code_hi);
+      uint32_t wl[8], wh[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = 2 * cp + h;
-        const uint32_t code = mx_code_from_bf16_amax(h ? (m >> 16) : (m & 0xFFFFu));
-        const float s = mx_inv_scale(code);
-        const uint32_t sel = h ? 0x7632u : 0x5410u;  // high or low halves of two words
-        uint32_t words[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          words[q] = quad_codes(__byte_perm(vals[4 * q], vals[4 * q + 1], sel),
-                                __byte_perm(vals[4 * q + 2], vals[4 * q + 3], sel), s);
-        *reinterpret_cast<uint4 *>(&outq[c][32 * b]) = make_uint4(words[0], words[1], words[2], words[3]);
-        *reinterpret_cast<uint4 *>(&outq[c][32 * b + 16]) = make_uint4(words[4], words[5], words[6], words[7]);
-        sfs[(c & 31) * 16 + (c >> 5) * 4 + b] = static_cast<uint8_t>(code);
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t *v = vals + 4 * q;
+        wl[q] = __byte_perm(e4m3x2_scaled(v[0] << 16, v[1] << 16, s_lo), e4m3x2_scaled(v[2] << 16, v[3] << 16, s_lo),
+                            0x5410);
+        wh[q] = __byte_perm(e4m3x2_scaled(v[0] & 0xFFFF0000u, v[1] & 0xFFFF0000u, s_hi),
+                            e4m3x2_scaled(v[2] & 0xFFFF0000u, v[3] & 0xFFFF0000u, s_hi), 0x5410);
       }
+      const int c = 2 * cp;
+      *reinterpret_cast<uint4 *>(&outq[c][32 * b]) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      *reinterpret_cast<uint4 *>(&outq[c][32 * b + 16]) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+      *reinterpret_cast<uint4 *>(&outq[c + 1][32 * b]) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+      *reinterpret_cast<uint4 *>(&outq[c + 1][32 * b + 16]) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+      sfs[(c & 31) * 16 + (c >> 5) * 4 + b] = static_cast<uint8_t>(code_lo);
+      sfs[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + b] = static_cast<uint8_t>(code_hi);
     }
     if (kRows) {
-      // thread = (row r, 32-column block b) for 2 of the tile's 512 pairs; rows past
-      // the group's end are not stored
-      const int64_t g = find_group(groups.tiles, num_groups, j);
-      const int64_t local0 = 128 * (j - groups.tiles[g]);
-      const int64_t n_g = groups.off[g + 1] - groups.off[g];
-      const int valid = static_cast<int>(n_g - local0 < 128 ? n_g - local0 : 128);
-      const int64_t src0 = groups.off[g] + local0;
+      // thread = (row r, 32-column block b) for 2 of the tile's 512 pairs; a
+      // quarter-warp takes 8 consecutive rows of one block (conflict-free 16-byte
+      // reads); rows past the group's end are not stored
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int pr = tid + 256 * h;
-        const int r = pr >> 2;
-        const int b = pr & 3;
+        const int p = tid + 256 * h;
+        const int b = (p >> 3) & 3;
+        const int r = (p & 7) + 8 * (p >> 5);
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -239,14 +270,14 @@ __global__ void __launch_bounds__(256, 3) mxfp8_cols_kernel(const uint16_t *__re
         }
         uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m = max_u16x2(m, w[i] & 0x7FFF7FFFu);
-        const uint32_t code = mx_code_from_bf16_amax(max(m & 0xFFFFu, m >> 16));
+        for (int i = 0; i < 16; i += 2) m = absmax_bf16x2(m, absmax_bf16x2(w[i], w[i + 1]));
+        const uint32_t code = mx_code_from_bf16_amax(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
         const float s = mx_inv_scale(code);
         uint32_t words[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) words[q] = quad_codes(w[2 * q], w[2 * q + 1], s);
-        if (r < valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(row_codes + (src0 + r) * cols + cb * 128 + 32 * b);
+        for (int q = 0; q < 8; ++q) words[q] = e4m3x4_words(w[2 * q], w[2 * q + 1], s);
+        if (r < cur.valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(row_codes + (cur.src0 + r) * cols + cb * 128 + 32 * b);
           dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
           dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
         }
@@ -269,6 +300,8 @@ __global__ void __launch_bounds__(256, 3) mxfp8_cols_kernel(const uint16_t *__re
       const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[(tid - 32) * 16]);
       *reinterpret_cast<uint4 *>(row_sf + (j * cblocks + cb) * 512 + (tid - 32) * 16) = v;
     }
+    cur = nxt;
+    advance(nxt);
   }
 }
 
@@ -287,7 +320,7 @@ template <bool kRows>
 static cudaError_t launch_cols(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
   const int threads = 256;
   const int64_t tiles = (a.ld / 128) * (a.cols / 128);
-  const int64_t cap = static_cast<int64_t>(a.num_sms) * 4;
+  const int64_t cap = static_cast<int64_t>(a.num_sms) * 2;
   const int blocks = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
   cudaError_t err = cudaFuncSetAttribute(mxfp8_cols_kernel<kRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kColSmemBytes);
