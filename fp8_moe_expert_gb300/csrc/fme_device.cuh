@@ -207,6 +207,20 @@ __device__ __forceinline__ uint64_t desc_scale_tile(uint32_t saddr) {
   return d;
 }
 
+// Descriptor of a 4096-byte replicated scale block for the 128 x 256-bit copy:
+// no swizzle, 8-row x 16-byte core matrices; the left 16 bytes of the rows are
+// at 0 .. 2047 (8-row groups 128 bytes apart), the right 16 bytes 2048 further.
+// A block holding [tile0 x 4][tile1 x 4] (two 512-byte scale tiles, each four
+// times) puts tile0 row i % 32 and tile1 row i % 32 into lane i.
+__device__ __forceinline__ uint64_t desc_scale_rep(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(2048 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
 // Instruction descriptor, kind::mxf8f6f4, E4M3 x E4M3, UE8M0 scales, M = 128.
 // sf_id picks which byte of the 32-bit scale word (which 32-wide K block) is used.
 __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t n, uint32_t sf_id) {
@@ -338,6 +352,12 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // into four tensor-memory columns of that CTA, replicated over the lane quarters.
 __device__ __forceinline__ void copy_scales(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Copy 128 rows x 32 bytes (described by `sdesc`) into eight tensor-memory
+// columns of all 128 lanes, row i to lane i, in both CTAs of the pair.
+__device__ __forceinline__ void copy_scales_wide(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive on the mbarrier at the same shared offset in both CTAs when the

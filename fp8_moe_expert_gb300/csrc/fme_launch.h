@@ -18,6 +18,7 @@ struct LaunchNvfp4 {
   int32_t *status;
   int num_sms;
   cudaStream_t stream;
+  bool replicated_sf = false;  // scales in the forward GEMM's B-operand layout (quantize_nvfp4_weights)
 };
 
 struct LaunchMxfp8 {

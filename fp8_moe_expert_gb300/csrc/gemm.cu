@@ -12,7 +12,9 @@
 // 128 rows in each CTA's tensor memory).  Each CTA stages its own 128 rows of A
 // and its half (128 rows) of the tile's 256 B rows, so a pair moves 1.5x fewer
 // operand bytes per flop than a single CTA with a 128 x 256 tile, and each
-// scale copy into tensor memory serves twice the MMA work.  11 warps per CTA:
+// scale copy into tensor memory serves twice the MMA work.  The forward's B
+// scales arrive pre-replicated (quantize_nvfp4_weights), so B needs one wide
+// tensor-memory copy per 64-deep step instead of two narrow ones.  12 warps per CTA:
 //   warp 0      TMA producer (both CTAs): A, B and their scale tiles into a
 //               5-6 stage ring; every copy of the pair completes on the leader
 //               CTA's "full" barrier;
@@ -20,8 +22,10 @@
 //               leader, one thread issues the block-scaled MMAs (kind::mxf4nvf4
 //               or kind::mxf8f6f4, M = 256, N = 256); commits free the stage in
 //               both CTAs and, at the end of a tile, fill both CTAs' accumulators;
-//   warp 10     in the leader, one thread copies each stage's scales into a ring
-//               of 4 tensor-memory buffers (tcgen05.cp) ahead of the MMAs;
+//   warps 10-11 in the leader, one thread of each copies half of each stage's
+//               scale tiles into a ring of 4 tensor-memory buffers (tcgen05.cp)
+//               ahead of the MMAs (one issuing thread cannot keep up with the
+//               FP4 MMAs: each copy occupies it for about 90 cycles);
 //   warps 2-9   epilogue (both CTAs): tcgen05.ld its own 128 x 256 fp32
 //               accumulator (each warp a 32-lane quarter and half the columns)
 //               into registers, release it to the leader, then apply the
@@ -46,8 +50,9 @@ constexpr int kPairM = 256;        // rows per pair tile
 constexpr int kBN = 256;           // columns per tile
 constexpr int kHalfN = kBN / 2;    // B rows staged by each CTA
 constexpr int kStageKBytes = 128;  // bytes of K per row per stage (one swizzle row)
-constexpr int kThreads = 352;      // producer, MMA, 8 epilogue warps, scale copier
-constexpr int kCopierWarp = 10;
+constexpr int kThreads = 384;      // producer, MMA, 8 epilogue warps, 2 scale copiers
+constexpr int kCopierWarp = 10;    // and 11
+constexpr int kCopiers = 2;
 constexpr int kSfBuffers = 4;      // tensor-memory scale buffers between the copier and the MMA issuer
 constexpr int kMaxStages = 6;
 constexpr int kOutBoxBytes = 32 * 32 * 2;            // one 32-row x 32-column bf16 block
@@ -64,7 +69,10 @@ struct Cfg {
   static constexpr int kKPerStage = kFp4 ? 256 : 128;  // elements of K per stage
   static constexpr int kAtoms = kFp4 ? 4 : 1;          // 512-byte scale tiles per 128 rows per stage
   static constexpr int kSfaBytes = 512 * kAtoms;       // this CTA's 128 rows
-  static constexpr int kSfbBytes = 2 * 512 * kAtoms;   // all 256 B rows of the tile
+  // All 256 B rows of the tile.  FP4: the weights' replicated layout, 4096 bytes per
+  // 64-deep step (the two 512-byte tiles four times each, one wide copy); FP8: the
+  // plain tiles (two 512-byte tiles per step).
+  static constexpr int kSfbBytes = kFp4 ? 4096 * kAtoms : 2 * 512 * kAtoms;
   static constexpr int kSfaCols = 4 * kAtoms;          // tensor-memory columns per stage
   static constexpr int kSfbCols = 8 * kAtoms;
   static constexpr int kSfCols = kSfaCols + kSfbCols;
@@ -78,12 +86,12 @@ struct Cfg {
 struct SharedState {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b
+  uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b (one arrival per copier)
   uint64_t sf_empty[kSfBuffers];  // the MMAs reading buffer b are done
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
-  uint64_t drain2;
+  uint64_t drain_cp[kCopiers];
   uint32_t tmem_base;
   int abort_flag;
   int ok_flag;
@@ -114,7 +122,8 @@ struct Tile {
   int32_t a_y, b_y;        // TMA row coordinates of this CTA's A rows and B half
   int32_t a_x0, b_x0;      // TMA K coordinates (bytes) of the first stage
   int32_t sfa_row;         // 128-row scale block of this CTA's A rows
-  int32_t sfb_row;         // first of the two 128-row scale blocks of the tile's B rows
+  int32_t sfb_row;         // FP8: first of the two 128-row scale blocks of the tile's B rows;
+                           // FP4: first 2 KB row of the tile's replicated scale blocks
   int32_t sfa_x0, sfb_x0;  // 512-byte scale tile index of the first stage
   int32_t n0;              // first output column
 };
@@ -175,7 +184,7 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const Groups &s, in
       const int64_t brow = static_cast<int64_t>(e) * p.n + nb * kBN;
       tl.b_y = static_cast<int32_t>(brow + rank * kHalfN);
       tl.b_x0 = 0;
-      tl.sfb_row = static_cast<int32_t>(brow / 128);
+      tl.sfb_row = static_cast<int32_t>((brow / kBN) * (p.k / 64) * 2);
       tl.sfb_x0 = 0;
     } else {
       tl.b_y = static_cast<int32_t>(nb * kBN + rank * kHalfN);
@@ -314,13 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&s.empty[i], 1);
     }
     for (int i = 0; i < kSfBuffers; ++i) {
-      mbar_init(&s.sf_full[i], 1);
+      mbar_init(&s.sf_full[i], kCopiers);
       mbar_init(&s.sf_empty[i], 1);
     }
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
-    mbar_init(&s.drain2, 1);
+    for (int i = 0; i < kCopiers; ++i) mbar_init(&s.drain_cp[i], 1);
     s.abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -359,8 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         pair::tma_load_2d(smem_b + stage * kBBytes, &p.map_b, bar, tl.b_x0 + ks * kStageKBytes, tl.b_y);
         pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, bar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
                           tl.sfa_row);
-        pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
-                          tl.sfb_row);
+        if (C::kFp4)  // four 64-deep steps of replicated blocks: 8 rows of 2 KB
+          pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, 0, tl.sfb_row + 8 * ks);
+        else
+          pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
+                            tl.sfb_row);
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
@@ -419,11 +431,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s.drain, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
-  } else if (warp == kCopierWarp && lane == 0 && rank == 0) {
-    // ---------------------------------------------------- scale copier (leader)
-    // Copies each stage's scale tiles (both CTAs, tcgen05.cp.cta_group::2) into
-    // the next free tensor-memory buffer while the MMA issuer works on earlier
-    // stages, then signals the buffer full.
+  } else if (warp >= kCopierWarp && warp < kCopierWarp + kCopiers && lane == 0 && rank == 0) {
+    // --------------------------------------------------- scale copiers (leader)
+    // Copy each stage's scale tiles (both CTAs, tcgen05.cp.cta_group::2) into the
+    // next free tensor-memory buffer while the MMA issuer works on earlier stages,
+    // then arrive on the buffer's "full" barrier.  FP4: copier 0 takes A (one
+    // 32x128b.warpx4 per 64-deep step), copier 1 takes B (one 128x256b copy of the
+    // replicated block per step: each copy costs the tensor core about the same
+    // whatever its size, so one wide copy beats two narrow ones).  FP8: the stage's
+    // three copies, A, B-low, B-high, alternate between the copiers.
+    const int who = warp - kCopierWarp;
     uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
@@ -440,11 +457,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint32_t sfb_t = sfa_t + C::kSfaCols;
         const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
         const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
+        if (C::kFp4) {
 #pragma unroll
-        for (int i = 0; i < C::kAtoms; ++i) {
-          pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
-          pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
-          pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+          for (int i = 0; i < C::kAtoms; ++i) {
+            if (who == 0)
+              pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
+            else
+              pair::copy_scales_wide(sfb_t + 8 * i, desc_scale_rep(sfb_s + 4096 * i));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::kAtoms; ++i) {
+            if ((3 * i) % kCopiers == who) pair::copy_scales(sfa_t + 4 * i, desc_scale_tile(sfa_s + 512 * i));
+            if ((3 * i + 1) % kCopiers == who) pair::copy_scales(sfb_t + 8 * i, desc_scale_tile(sfb_s + 512 * i));
+            if ((3 * i + 2) % kCopiers == who)
+              pair::copy_scales(sfb_t + 8 * i + 4, desc_scale_tile(sfb_s + C::kSfbBytes / 2 + 512 * i));
+          }
         }
         pair::commit_local(&s.sf_full[buf]);
         if (++stage == S) {
@@ -457,9 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
       }
     }
-    pair::commit_local(&s.drain2);
+    pair::commit_local(&s.drain_cp[who]);
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&s.drain2, 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
+    while (!mbar_try_wait(&s.drain_cp[who], 0) && globaltimer() - t0 < kWaitLimitNs / 4) {
     }
   } else if (warp >= 2 && warp < kCopierWarp) {
     // --------------------------------------------------------------- epilogue

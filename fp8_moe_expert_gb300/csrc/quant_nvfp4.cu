@@ -147,7 +147,11 @@ __host__ __device__ __forceinline__ size_t nv_smem_bytes(int stages, int64_t k, 
   return static_cast<size_t>(stages) * (2 * k + 8) + 8 * static_cast<size_t>(num_groups + 1);
 }
 
-template <int R>
+// kRep: the scales go to the replicated layout of the forward GEMM's B operand
+// (quantize_nvfp4_weights): per 256 rows and 64-deep step a 4096-byte block
+// [tile0 x 4][tile1 x 4], tile0 / tile1 the 512-byte tiles of the block's rows
+// 0..127 / 128..255; each 4-scale word is stored four times.
+template <int R, bool kRep>
 __global__ void __launch_bounds__(kNvMaxThreads, 4)
     nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
                           int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
@@ -217,9 +221,14 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, m);
     if (lane == 0) part[i & 1][warp] = wmax;
     if (tid == 0) {
-      const int g = find_group(g_off, num_groups, row);
-      const int64_t prow = 128 * static_cast<int64_t>(g_tiles[g]) + (row - g_off[g]);
-      sf_row_of[i & 1] = sf_offset(prow, 0, c4);
+      if (kRep) {
+        sf_row_of[i & 1] = (row / 256) * (k / 64) * 4096 + ((row % 256) / 128) * 2048 + (row % 32) * 16 +
+                           ((row % 128) / 32) * 4;
+      } else {
+        const int g = find_group(g_off, num_groups, row);
+        const int64_t prow = 128 * static_cast<int64_t>(g_tiles[g]) + (row - g_off[g]);
+        sf_row_of[i & 1] = sf_offset(prow, 0, c4);
+      }
     }
     if (__syncthreads_or(!ok)) break;  // every block of stage s is in registers: refill it
     if (tid == 0) {
@@ -261,8 +270,16 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
       const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
       const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-      if ((lane & 3) == 0 && blk < nblk)
-        *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      if ((lane & 3) == 0 && blk < nblk) {
+        const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        if (kRep) {
+          uint8_t *dst = sf_row + (blk >> 2) * 4096;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t *>(dst + 512 * r) = word;
+        } else {
+          *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = word;
+        }
+      }
     }
     if (tid == 0) row_scale[row] = s_t;
   }
@@ -285,7 +302,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
 // / R rounded up to warps.  CTAs per SM: as many as 1024 threads and the
 // shared-memory budget allow with at least 3 stages each; stages: the rest of
 // the budget, 3 to 16 rows.
-template <int R>
+template <int R, bool kRep>
 static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   const int64_t nblk = a.k / 16;
   const int threads = static_cast<int>(((nblk + R - 1) / R + 31) / 32 * 32);
@@ -296,19 +313,21 @@ static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   int64_t stages = (kNvSmemBudget / per_sm - fixed) / (2 * a.k + 8);
   stages = stages < 3 ? 3 : (stages > 16 ? 16 : stages);
   const size_t smem = nv_smem_bytes(static_cast<int>(stages), a.k, a.num_groups);
-  cudaError_t err = cudaFuncSetAttribute(nvfp4_pertoken_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(nvfp4_pertoken_kernel<R, kRep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int64_t cap = static_cast<int64_t>(a.num_sms) * per_sm;
   const int blocks = static_cast<int>(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
-  nvfp4_pertoken_kernel<R><<<blocks, threads, smem, a.stream>>>(
+  nvfp4_pertoken_kernel<R, kRep><<<blocks, threads, smem, a.stream>>>(
       static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k), a.offsets, a.num_groups, a.codes, a.sf,
       a.row_scale, a.status, static_cast<int>(stages));
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
-  return (a.k / 16 > kNvMaxThreads) ? launch_nvfp4<2>(a) : launch_nvfp4<1>(a);
+  const bool wide = a.k / 16 > kNvMaxThreads;
+  if (a.replicated_sf) return wide ? launch_nvfp4<2, true>(a) : launch_nvfp4<1, true>(a);
+  return wide ? launch_nvfp4<2, false>(a) : launch_nvfp4<1, false>(a);
 }
 
 }  // namespace fme

@@ -5,6 +5,8 @@
  * row-wise + column-wise MXFP8 quantizer for tensors needed both ways):
  *   quantize_nvfp4_pertoken   NVFP4 variant of the forward: E2M1 codes, one E4M3
  *                             scale per 16 values along K, one FP32 scale per token.
+ *   quantize_nvfp4_weights    the same quantization of the stacked expert weights,
+ *                             scales written in the forward GEMM's B-operand layout.
  *   quantize_mxfp8            standard MXFP8 of the backward: E4M3 codes, one E8M0
  *                             scale per 32 values, row-wise or column-wise.
  *   grouped_gemm_fwd_nvfp4    Y_e = X_e W_e^T per expert, per-token scales applied
@@ -111,6 +113,30 @@ fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const
                                    int32_t *dev_status, void *stream);
 
 /*
+ * quantize_nvfp4_weights -- quantize_nvfp4_pertoken of the stacked expert weights
+ * W [rows x k] (one group), for the B operand of grouped_gemm_fwd_nvfp4.  Codes
+ * and row scales are byte-identical to quantize_nvfp4_pertoken; the E4M3 block
+ * scales go to the B-operand layout instead of the tiled one:
+ *   for each 256-row block rb and each 64-deep step a (4 scales per row), a
+ *   4096-byte block at offset (rb * (k/64) + a) * 4096 holding [T0 T0 T0 T0 T1 T1
+ *   T1 T1], where T0 / T1 are the 512-byte tiles of the tiled layout for rows
+ *   0..127 / 128..255 of the block (row i's 4 scales at (i % 32) * 16 +
+ *   ((i % 128) / 32) * 4).
+ * The four copies are the tensor core's 4x lane replication of B's scales, laid
+ * out so that one 128-lane x 256-bit tensor-memory copy moves a step's scales
+ * (two narrow copies otherwise); the weights' scale bytes grow from k/16 to k/4
+ * per row.
+ *
+ *   x          device bf16 [rows x k]
+ *   rows, k    rows a multiple of 256; k a multiple of 256, 256 <= k <= 8192
+ *   codes      device uint8 [rows x k/2]
+ *   sf         device uint8, fme_sf_bytes_nvfp4_weights(rows, k) bytes
+ *   row_scale  device float [rows]
+ */
+fme_status quantize_nvfp4_weights(const void *x, int64_t rows, int64_t k, uint8_t *codes, uint8_t *sf,
+                                  float *row_scale, int32_t *dev_status, void *stream);
+
+/*
  * quantize_mxfp8 -- standard MXFP8 (OCP MX v1.0 rule) of the MoE backward.
  *
  * Per block of 32: X = 2^(floor(log2 amax) - 8) stored as the E8M0 code
@@ -163,8 +189,8 @@ fme_status quantize_mxfp8_rowcol(const void *x, int64_t rows, int64_t cols, cons
  * No split over K: a row's output does not depend on any other row.
  *
  *   a_codes, a_sf, a_scale  quantize_nvfp4_pertoken of X [m x k] with these offsets
- *   b_codes, b_sf, b_scale  quantize_nvfp4_pertoken of W [num_experts * n x k]
- *                           (expert e's rows are e*n .. e*n+n-1), one group
+ *   b_codes, b_sf, b_scale  quantize_nvfp4_weights of W [num_experts * n x k]
+ *                           (expert e's rows are e*n .. e*n+n-1)
  *   offsets        device int32 [num_experts + 1], rows of X per expert
  *   m, n, k        n a multiple of 256; k a multiple of 256
  *   y              device bf16 [m x n]
@@ -221,6 +247,10 @@ int64_t fme_sf_bytes(int64_t rows, int64_t cols, int32_t block, int32_t num_grou
 
 /* Leading dimension (positions per column) of the column-wise MXFP8 outputs. */
 int64_t fme_colwise_ld(int64_t rows, int32_t num_groups);
+
+/* Bytes of the B-operand scale buffer written by quantize_nvfp4_weights (0 for
+ * rows not a multiple of 256 or k not a multiple of 64). */
+int64_t fme_sf_bytes_nvfp4_weights(int64_t rows, int64_t k);
 
 /* Synchronises `stream`, copies *dev_status to the host and maps it to a status:
  * FME_OK, FME_ERR_DEVICE_BAD_OFFSETS or FME_ERR_DEVICE_TIMEOUT.  `raw` (may be

@@ -44,6 +44,8 @@ def test_helpers_closed_forms(lib):
     assert fme.sf_padded_rows(16384, 32) == 20352
     assert fme.sf_bytes(16384, 7168, 16, 32) == 20352 * 448
     assert fme.sf_bytes(100, 96, 32, 1) == 128 * 4          # 3 scales per row, rounded up to 4
+    assert fme.sf_bytes_nvfp4_weights(32 * 4096, 7168) == 32 * 16 * 112 * 4096   # k/4 bytes per row
+    assert fme.sf_bytes_nvfp4_weights(100, 256) == 0
     assert fme.colwise_ld(65536, 32) == ((65536 + 127 * 32) // 128) * 128
     assert lib.fme_version().startswith(b"fme")
     for code in range(8):
@@ -67,6 +69,14 @@ def test_host_argument_checks(lib):
     assert q(None, 10, 256, None, 1, good, good, good, None, _stream()) == 1
     assert q(odd, 10, 256, None, 1, good, good, good, None, _stream()) == 2
     assert q(good, 0, 256, None, 1, None, None, None, None, _stream()) == 0     # nothing to do
+    qw = lib.quantize_nvfp4_weights
+    assert qw(good, -256, 256, good, good, good, None, _stream()) == 1
+    assert qw(good, 100, 256, good, good, good, None, _stream()) == 3     # rows % 256
+    assert qw(good, 256, 192, good, good, good, None, _stream()) == 3     # k % 256
+    assert qw(good, 256, 8448, good, good, good, None, _stream()) == 3
+    assert qw(None, 256, 256, good, good, good, None, _stream()) == 1
+    assert qw(good, 256, 256, good, odd, good, None, _stream()) == 2
+    assert qw(good, 0, 256, None, None, None, None, _stream()) == 0       # nothing to do
     m = lib.quantize_mxfp8
     assert m(good, 10, 256, 2, None, 1, good, good, None, None, _stream()) == 1
     assert m(good, 10, 256, 0, None, 1, good, good, good, None, _stream()) == 1  # row-wise takes no padded offsets
