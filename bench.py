@@ -346,6 +346,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": n_calls * args.steps,
         "clocks": clocks.summary(),
     }
+    if not args.no_extras:
+        line["extras"] = run_extras(step, args, bf16_sus)
     if not args.no_e2e:
         line["e2e"] = run_e2e(step, calls, args, world)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -353,6 +355,41 @@ def run_ours(args, rank, world, local_rank):
     elif rank == 0 and world > 1:
         line["cpu_baseline"] = None
     return line
+
+
+def run_extras(step, args, bf16_sus):
+    """Calls beyond the step's path, timed on the same workload after it (not part
+    of `value`): the MXFP8 forward grouped GEMMs (gate/up and down) on row-wise
+    MXFP8 operands.  CUDA events on the launching stream, 3 warm-up and
+    `args.steps` timed launches each."""
+    import torch
+
+    f, off, st = step.fme, step.offsets, step.status
+    R, H, I, E = step.R, step.H, step.I, step.E
+    xq = f.quantize_mxfp8(step.x, f.ROWWISE, off, status=st)
+    wq = f.quantize_mxfp8(step.w_gu, f.ROWWISE, status=st)
+    hq = f.quantize_mxfp8(step.h, f.ROWWISE, off, status=st)
+    wdq = f.quantize_mxfp8(step.w_d, f.ROWWISE, status=st)
+    out = {}
+    for name, fn, flops in (
+            ("gemm_fwd_gate_up_mxfp8",
+             lambda: f.grouped_gemm_fwd_mxfp8(*xq, *wq, off, 2 * I, H, y=step.y_gu, status=st), 2 * R * 2 * I * H),
+            ("gemm_fwd_down_mxfp8",
+             lambda: f.grouped_gemm_fwd_mxfp8(*hq, *wdq, off, H, I, y=step.y_d, status=st), 2 * R * H * I)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        ach = flops / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac_fp8": round(ach / (bf16_sus * 2), 3)}
+    del xq, wq, hq, wdq
+    return out
 
 
 INPUT_NAMES = ("x", "w_gu", "h", "w_d", "dy")
@@ -574,6 +611,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip timing the calls outside the step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

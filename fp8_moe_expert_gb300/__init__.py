@@ -65,6 +65,7 @@ SYMBOLS = {
     "quantize_mxfp8_rowcol": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p", "p"]),
     "grouped_gemm_fwd_nvfp4": ("i32", ["p", "p", "p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p",
                                        "p"]),
+    "grouped_gemm_fwd_mxfp8": ("i32", ["p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p", "p"]),
     "grouped_gemm_dgrad_mxfp8": ("i32", ["p", "p", "p", "p", "i64", "p", "i32", "i64", "i64", "i64", "p", "p",
                                          "p"]),
     "grouped_gemm_wgrad_mxfp8": ("i32", ["p", "p", "i64", "p", "p", "i64", "p", "i32", "i64", "i64", "p", "p",
@@ -252,6 +253,21 @@ def grouped_gemm_fwd_nvfp4(a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offse
                                       _ptr(b_scale), _ptr(offsets), e, m, n, k, _ptr(y), _ptr(status),
                                       _stream(stream))
     _check(st, "grouped_gemm_fwd_nvfp4")
+    return y
+
+
+def grouped_gemm_fwd_mxfp8(a_codes, a_sf, b_codes, b_sf, offsets, n, k, *, y=None, status=None, stream=None):
+    """MXFP8 forward: Y [m x n] bf16 from row-wise MXFP8 of X [m x k] and of the
+    stacked weights [E*n x k]."""
+    import torch
+
+    m = a_codes.shape[0]
+    e = offsets.numel() - 1
+    if y is None:
+        y = _empty((m, n), torch.bfloat16, a_codes.device)
+    st = lib().grouped_gemm_fwd_mxfp8(_ptr(a_codes), _ptr(a_sf), _ptr(b_codes), _ptr(b_sf), _ptr(offsets), e, m, n, k,
+                                      _ptr(y), _ptr(status), _stream(stream))
+    _check(st, "grouped_gemm_fwd_mxfp8")
     return y
 
 

@@ -320,6 +320,47 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_fwd_nvfp4 launch");
 }
 
+fme_status grouped_gemm_fwd_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, const uint8_t *b_codes,
+                                  const uint8_t *b_sf, const int32_t *offsets, int32_t num_experts, int64_t m,
+                                  int64_t n, int64_t k, void *y, int32_t *dev_status, void *stream) {
+  if (m < 0 || n < 0 || k < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (n % 256 != 0 || n == 0 || k % 128 != 0 || k == 0 || k > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (m > (int64_t(1) << 31) - 1 || static_cast<int64_t>(num_experts) * n > (int64_t(1) << 31) - 1)
+    return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets) return FME_ERR_INVALID_ARGUMENT;
+  if (m == 0) return FME_OK;
+  if (!a_codes || !a_sf || !b_codes || !b_sf || !y) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a_codes) || !aligned16(a_sf) || !aligned16(b_codes) || !aligned16(b_sf) || !aligned16(y) ||
+      !aligned16(offsets))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchGemm a{};
+  a.kind = fme::GemmKind::kFwdMxfp8;
+  if ((st = encode_u8_2d(&a.map_a, a_codes, k, m, k, 128)) != FME_OK) return st;
+  if ((st = encode_u8_2d(&a.map_b, b_codes, k, static_cast<uint64_t>(num_experts) * n, k, 128)) != FME_OK)
+    return st;
+  // row-wise E8M0 scales: (k / 128) tiles of 512 bytes per 128-row block; a stage takes one
+  if ((st = encode_scales_2d(&a.map_sfa, a_sf, padded_rows_bound(m, num_experts) / 128, (k / 128) * 512, 1, 1)) !=
+      FME_OK)
+    return st;
+  if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * n / 128, (k / 128) * 512, 1,
+                             2)) != FME_OK)
+    return st;
+  a.offsets = offsets;
+  a.num_experts = num_experts;
+  a.m = m;
+  a.n = n;
+  a.k = k;
+  a.y = y;
+  a.status = dev_status;
+  a.num_sms = sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t err = fme::launch_grouped_gemm(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_fwd_mxfp8 launch");
+}
+
 fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, const uint8_t *b_codes,
                                     const uint8_t *b_sf, int64_t ldb, const int32_t *offsets, int32_t num_experts,
                                     int64_t m, int64_t n, int64_t k, void *y, int32_t *dev_status, void *stream) {

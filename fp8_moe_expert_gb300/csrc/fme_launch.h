@@ -34,7 +34,7 @@ struct LaunchMxfp8 {
   cudaStream_t stream;
 };
 
-enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2 };
+enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2, kFwdMxfp8 = 3 };
 
 struct LaunchGemm {
   GemmKind kind;

@@ -34,6 +34,9 @@
 //               store instruction writes 64 contiguous bytes of each of 8 rows
 //               (rows past the expert's last row are skipped), overlapping the
 //               next tile's MMAs.
+// Kinds: the NVFP4 forward (kind::mxf4nvf4, per-token and per-column FP32 scales
+// in the epilogue), the MXFP8 forward (kind::mxf8f6f4, same operand layout), dgrad
+// and wgrad (kind::mxf8f6f4).
 // Both CTAs walk the same tile sequence, derived in shared memory from the
 // per-expert offsets: forward and dgrad go expert by expert, 256-row blocks of
 // each expert's rows, 256-column blocks fastest; wgrad goes expert by expert in
@@ -180,11 +183,13 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const Groups &s, in
     tl.a_x0 = 0;
     tl.sfa_row = s.tiles[e] + static_cast<int32_t>(mb);
     tl.sfa_x0 = 0;
-    if (K == GemmKind::kFwdNvfp4) {
+    if (K == GemmKind::kFwdNvfp4 || K == GemmKind::kFwdMxfp8) {
+      // B = stacked weights, expert e's rows e*n .. e*n+n-1, K contiguous
       const int64_t brow = static_cast<int64_t>(e) * p.n + nb * kBN;
       tl.b_y = static_cast<int32_t>(brow + rank * kHalfN);
       tl.b_x0 = 0;
-      tl.sfb_row = static_cast<int32_t>((brow / kBN) * (p.k / 64) * 2);
+      tl.sfb_row = (K == GemmKind::kFwdNvfp4) ? static_cast<int32_t>((brow / kBN) * (p.k / 64) * 2)
+                                               : static_cast<int32_t>(brow / 128);
       tl.sfb_x0 = 0;
     } else {
       tl.b_y = static_cast<int32_t>(nb * kBN + rank * kHalfN);
@@ -609,6 +614,8 @@ cudaError_t launch_grouped_gemm(const LaunchGemm &a) {
       return launch_kind<GemmKind::kDgradMxfp8>(a);
     case GemmKind::kWgradMxfp8:
       return launch_kind<GemmKind::kWgradMxfp8>(a);
+    case GemmKind::kFwdMxfp8:
+      return launch_kind<GemmKind::kFwdMxfp8>(a);
   }
   return cudaErrorInvalidValue;
 }

@@ -270,15 +270,13 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
       const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
       const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-      if ((lane & 3) == 0 && blk < nblk) {
-        const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
-        if (kRep) {
-          uint8_t *dst = sf_row + (blk >> 2) * 4096;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t *>(dst + 512 * r) = word;
-        } else {
-          *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = word;
-        }
+      const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);  // complete in lanes 4g
+      if (kRep) {
+        // all four lanes of the group store one of the word's four copies
+        const uint32_t w = __shfl_sync(0xFFFFFFFFu, word, lane & ~3);
+        if (blk < nblk) *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 4096 + 512 * (lane & 3)) = w;
+      } else if ((lane & 3) == 0 && blk < nblk) {
+        *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = word;
       }
     }
     if (tid == 0) row_scale[row] = s_t;

@@ -11,6 +11,7 @@
  *                             scale per 32 values, row-wise or column-wise.
  *   grouped_gemm_fwd_nvfp4    Y_e = X_e W_e^T per expert, per-token scales applied
  *                             in the epilogue, bf16 out.
+ *   grouped_gemm_fwd_mxfp8    the same product with MXFP8 operands (no per-token scale).
  *   grouped_gemm_dgrad_mxfp8  dX_e = dY_e W_e per expert, bf16 out.
  *   grouped_gemm_wgrad_mxfp8  dW_e = dY_e^T H_e per expert, bf16 out.
  *
@@ -199,6 +200,24 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
                                   const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
                                   const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n,
                                   int64_t k, void *y, int32_t *dev_status, void *stream);
+
+/*
+ * grouped_gemm_fwd_mxfp8 -- the MXFP8 forward: Y[t, :] = sum_k A'[t,k] B'_e[:,k] for
+ * every row t of expert e, A', B' = E4M3 codes times E8M0 block scales (blocks of
+ * 32 along K), fp32 accumulation on the tensor cores, bf16 out; no per-token scale.
+ * ("Scaling and Optimizing Frontier Model Training", "MXFP8 expert kernels": MXFP8
+ * grouped GEMMs for the forward and backward of the expert layers.)
+ *
+ *   a_codes, a_sf  quantize_mxfp8(ROWWISE) of X [m x k] with these offsets
+ *   b_codes, b_sf  quantize_mxfp8(ROWWISE) of W [num_experts * n x k], one group
+ *                  (expert e's rows are e*n .. e*n+n-1)
+ *   offsets        device int32 [num_experts + 1], rows of X per expert
+ *   m, n, k        n a multiple of 256; k a multiple of 128
+ *   y              device bf16 [m x n]
+ */
+fme_status grouped_gemm_fwd_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, const uint8_t *b_codes,
+                                  const uint8_t *b_sf, const int32_t *offsets, int32_t num_experts, int64_t m,
+                                  int64_t n, int64_t k, void *y, int32_t *dev_status, void *stream);
 
 /*
  * grouped_gemm_dgrad_mxfp8 -- Y[t, :] = sum_j A'[t, j] B'[:, e*k + j] for every

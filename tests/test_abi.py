@@ -24,7 +24,8 @@ def declared_functions():
 
 def test_header_declares_the_five_calls():
     names = declared_functions()
-    for call in ("quantize_nvfp4_pertoken", "quantize_mxfp8", "grouped_gemm_fwd_nvfp4",
+    for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_weights", "quantize_mxfp8", "grouped_gemm_fwd_nvfp4",
+                 "grouped_gemm_fwd_mxfp8",
                  "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8"):
         assert call in names
 
@@ -90,6 +91,12 @@ def test_host_argument_checks(lib):
     assert f(good, good, good, good, good, good, None, 4, 100, 256, 256, good, None, _stream()) == 1
     assert f(good, good, good, good, good, good, good, 0, 100, 256, 256, good, None, _stream()) == 1
     assert f(good, good, good, good, good, good, good, 4, 100, 256, 256, odd, None, _stream()) == 2
+    fm = lib.grouped_gemm_fwd_mxfp8
+    assert fm(good, good, good, good, good, 4, 100, 100, 256, good, None, _stream()) == 3    # n % 256
+    assert fm(good, good, good, good, good, 4, 100, 256, 96, good, None, _stream()) == 3     # k % 128
+    assert fm(good, good, good, good, None, 4, 100, 256, 256, good, None, _stream()) == 1
+    assert fm(good, good, good, good, good, 4, 100, 256, 256, odd, None, _stream()) == 2
+    assert fm(good, good, good, good, good, 4, 0, 256, 256, None, None, _stream()) == 0     # no rows
     d = lib.grouped_gemm_dgrad_mxfp8
     assert d(good, good, good, good, 1024, good, 4, 100, 256, 512, good, None, _stream()) == 1  # ldb < E k
     assert d(good, good, good, good, 2048, good, 4, 100, 256, 96, good, None, _stream()) == 3

@@ -44,6 +44,16 @@ def gpu_fwd(fme, x, w, offsets, n, k):
     return y
 
 
+def gpu_fwd_mxfp8(fme, x, w, offsets, n, k):
+    st = _status()
+    off = _i32(offsets)
+    a = fme.quantize_mxfp8(x, fme.ROWWISE, off, status=st)
+    b = fme.quantize_mxfp8(w, fme.ROWWISE, status=st)
+    y = fme.grouped_gemm_fwd_mxfp8(*a, *b, off, n, k, status=st)
+    _ok(fme, st)
+    return y
+
+
 def gpu_dgrad(fme, dy, w_stacked, offsets, n, k):
     """dX_e = dY_e W_e with W_e = rows [e k, e k + k) of w_stacked [E k x n]."""
     st = _status()
@@ -70,6 +80,12 @@ def gpu_wgrad(fme, dy, h, offsets):
 def ref_fwd_rows(orc, x_bits_rows, w_bits_e):
     a = orc.dequant_nvfp4(*orc.quant_nvfp4(x_bits_rows))
     b = orc.dequant_nvfp4(*orc.quant_nvfp4(w_bits_e))
+    return orc.gemm_abt(a, b)
+
+
+def ref_fwd_mxfp8_rows(orc, x_bits_rows, w_bits_e):
+    a = orc.dequant_mxfp8(*orc.quant_mxfp8_rows(x_bits_rows))
+    b = orc.dequant_mxfp8(*orc.quant_mxfp8_rows(w_bits_e))
     return orc.gemm_abt(a, b)
 
 
@@ -115,6 +131,13 @@ def test_tiny_mxfp8_gemm(fme, orc):
     check_gemm_tolerance(bf16_to_f64(y), orc.gemm_abt(ya, yb), what="tiny mxfp8")
 
 
+def test_tiny_fwd_mxfp8(fme, orc):
+    """The MXFP8 forward on the tiny tensors (one expert, K = 256)."""
+    x_bits, w_bits = synth.tiny(0)
+    y = gpu_fwd_mxfp8(fme, bf16_tensor(x_bits), bf16_tensor(w_bits), [0, 128], 256, 256)
+    check_gemm_tolerance(bf16_to_f64(y), ref_fwd_mxfp8_rows(orc, x_bits, w_bits), what="tiny mxfp8 fwd")
+
+
 # --------------------------------------------------- small ragged, full check --
 COUNTS = [0, 37, 128, 1, 200, 0, 129]
 
@@ -130,6 +153,19 @@ def test_fwd_ragged_experts(fme, orc):
         if COUNTS[g]:
             ref[off[g]:off[g + 1]] = ref_fwd_rows(orc, x_bits[off[g]:off[g + 1]], w_bits[g * n:(g + 1) * n])
     check_gemm_tolerance(y, ref, what="ragged fwd")
+
+
+def test_fwd_mxfp8_ragged_experts(fme, orc):
+    off = synth.offsets_from_counts(COUNTS)
+    e, n, k = len(COUNTS), 512, 640
+    x_bits = synth.normal_bits((int(off[-1]), k), 1.0, seed=13)
+    w_bits = synth.normal_bits((e * n, k), 0.02, seed=14)
+    y = bf16_to_f64(gpu_fwd_mxfp8(fme, bf16_tensor(x_bits), bf16_tensor(w_bits), off, n, k))
+    ref = np.zeros_like(y)
+    for g in range(e):
+        if COUNTS[g]:
+            ref[off[g]:off[g + 1]] = ref_fwd_mxfp8_rows(orc, x_bits[off[g]:off[g + 1]], w_bits[g * n:(g + 1) * n])
+    check_gemm_tolerance(y, ref, what="ragged mxfp8 fwd")
 
 
 def test_dgrad_ragged_experts(fme, orc):
@@ -266,6 +302,31 @@ def _moe_bwd_sampled(fme, orc, counts, seed, label):
 def test_moe_forward_dirichlet(fme, orc):
     """MoE forward, NVFP4: 65536 rows over 32 experts (Dirichlet loads)."""
     _moe_fwd_sampled(fme, orc, synth.dirichlet_counts(), seed=2, label="dirichlet")
+
+
+def test_moe_forward_mxfp8_dirichlet(fme, orc):
+    """MoE forward with MXFP8 operands (the continued-pretraining recipe): gate/up
+    and down over 65536 rows in 32 experts, sampled rows of sampled experts."""
+    import torch
+
+    counts = synth.dirichlet_counts()
+    off = synth.offsets_from_counts(counts)
+    rows, E, H, I = int(off[-1]), len(counts), synth.HIDDEN, synth.INTERMEDIATE
+    x = synth.torch_normal((rows, H), 1.0, seed=51)
+    w_gu = synth.torch_normal((E * 2 * I, H), 0.02, seed=52)
+    h = synth.torch_normal((rows, I), 1.0, seed=53)
+    w_d = synth.torch_normal((E * H, I), 0.02, seed=54)
+    y_gu = gpu_fwd_mxfp8(fme, x, w_gu, off, 2 * I, H)
+    y_d = gpu_fwd_mxfp8(fme, h, w_d, off, H, I)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    for g in _sampled_experts(counts, rng):
+        r = _sample_rows(off, g, rng)
+        ridx = torch.from_numpy(r).cuda()
+        ref = ref_fwd_mxfp8_rows(orc, bf16_bits_np(x[ridx]), bf16_bits_np(w_gu[g * 2 * I:(g + 1) * 2 * I]))
+        check_gemm_tolerance(bf16_to_f64(y_gu[ridx]), ref, what=f"mxfp8 gate/up expert {g}")
+        ref = ref_fwd_mxfp8_rows(orc, bf16_bits_np(h[ridx]), bf16_bits_np(w_d[g * H:(g + 1) * H]))
+        check_gemm_tolerance(bf16_to_f64(y_d[ridx]), ref, what=f"mxfp8 down expert {g}")
 
 
 def test_moe_backward_dirichlet(fme, orc):
