@@ -360,8 +360,9 @@ def run_ours(args, rank, world, local_rank):
 def run_extras(step, args, bf16_sus):
     """Calls beyond the step's path, timed on the same workload after it (not part
     of `value`): the MXFP8 forward grouped GEMMs (gate/up and down) on row-wise
-    MXFP8 operands.  CUDA events on the launching stream, 3 warm-up and
-    `args.steps` timed launches each."""
+    MXFP8 operands, and the fused SwiGLU + NVFP4 quantization of the gate/up
+    output (writing h for the backward).  CUDA events on the launching stream, 3
+    warm-up and `args.steps` timed launches each."""
     import torch
 
     f, off, st = step.fme, step.offsets, step.status
@@ -371,6 +372,24 @@ def run_extras(step, args, bf16_sus):
     hq = f.quantize_mxfp8(step.h, f.ROWWISE, off, status=st)
     wdq = f.quantize_mxfp8(step.w_d, f.ROWWISE, status=st)
     out = {}
+    hbm = float(load_peaks()[0]["hbm_gbs"])
+    h_out = torch.empty_like(step.h)
+    sw_bytes = R * (2 * 2 * I + 2 * I + I // 2 + I // 16 + 4)  # gate/up in; h, codes, scales, row scale out
+    fn = lambda: f.swiglu_quantize_nvfp4(step.y_gu, off, codes=step.hq[0], sf=step.hq[1],  # noqa: E731
+                                         row_scale=step.hq[2], h=h_out, status=st)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    gbs = sw_bytes / (ms * 1e-3) / 1e9
+    out["swiglu_quantize_nvfp4"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    del h_out
     for name, fn, flops in (
             ("gemm_fwd_gate_up_mxfp8",
              lambda: f.grouped_gemm_fwd_mxfp8(*xq, *wq, off, 2 * I, H, y=step.y_gu, status=st), 2 * R * 2 * I * H),

@@ -61,6 +61,7 @@ SYMBOLS = {
     # name: (restype, argtypes)
     "quantize_nvfp4_pertoken": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p"]),
     "quantize_nvfp4_weights": ("i32", ["p", "i64", "i64", "p", "p", "p", "p", "p"]),
+    "swiglu_quantize_nvfp4": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8": ("i32", ["p", "i64", "i64", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8_rowcol": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p", "p"]),
     "grouped_gemm_fwd_nvfp4": ("i32", ["p", "p", "p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p",
@@ -179,6 +180,30 @@ def quantize_nvfp4_weights(w, *, codes=None, sf=None, row_scale=None, status=Non
                                       _stream(stream))
     _check(st, "quantize_nvfp4_weights")
     return codes, sf, row_scale
+
+
+def swiglu_quantize_nvfp4(gate_up, offsets=None, num_groups=None, *, codes=None, sf=None, row_scale=None, h=None,
+                          want_h=True, status=None, stream=None):
+    """h = silu(g) * u of gate_up [rows x 2*inter] (bf16), NVFP4-quantized per
+    token -> (codes, sf, row_scale, h or None)."""
+    import torch
+
+    rows, two_inter = gate_up.shape
+    inter = two_inter // 2
+    offsets, g = _groups(offsets, num_groups)
+    dev = gate_up.device
+    if codes is None:
+        codes = _empty((rows, inter // 2), torch.uint8, dev)
+    if sf is None:
+        sf = _empty((max(sf_bytes(rows, inter, 16, g), 16),), torch.uint8, dev)
+    if row_scale is None:
+        row_scale = _empty((rows,), torch.float32, dev)
+    if h is None and want_h:
+        h = _empty((rows, inter), torch.bfloat16, dev)
+    st = lib().swiglu_quantize_nvfp4(_ptr(gate_up), rows, inter, _ptr(offsets), g, _ptr(codes), _ptr(sf),
+                                     _ptr(row_scale), _ptr(h), _ptr(status), _stream(stream))
+    _check(st, "swiglu_quantize_nvfp4")
+    return codes, sf, row_scale, h
 
 
 def quantize_mxfp8(x, axis=ROWWISE, offsets=None, num_groups=None, *, codes=None, sf=None, padded_offsets=None,

@@ -224,6 +224,28 @@ fme_status quantize_nvfp4_weights(const void *x, int64_t rows, int64_t k, uint8_
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_nvfp4_weights launch");
 }
 
+fme_status swiglu_quantize_nvfp4(const void *gate_up, int64_t rows, int64_t inter, const int32_t *offsets,
+                                 int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale, void *h,
+                                 int32_t *dev_status, void *stream) {
+  if (rows < 0 || check_groups(num_groups) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (offsets == nullptr && num_groups != 1) return FME_ERR_INVALID_ARGUMENT;
+  if (inter % 64 != 0 || inter < 64 || inter > 8192) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (rows > (int64_t(1) << 31) - 1) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return FME_OK;
+  if (!gate_up || !codes || !sf || !row_scale) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(gate_up) || !aligned16(codes) || !aligned16(sf) || !aligned16(row_scale) || !aligned16(h))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchNvfp4 a{gate_up, rows, inter, offsets, num_groups, codes, sf, row_scale, dev_status, sms,
+                     static_cast<cudaStream_t>(stream)};
+  a.swiglu = true;
+  a.h_out = h;
+  cudaError_t err = fme::launch_quantize_nvfp4(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "swiglu_quantize_nvfp4 launch");
+}
+
 fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axis, const int32_t *offsets,
                           int32_t num_groups, uint8_t *codes, uint8_t *sf, int32_t *padded_offsets,
                           int32_t *dev_status, void *stream) {

@@ -143,25 +143,54 @@ constexpr int kNvSmemBudget = 220 * 1024;  // shared memory aimed for per SM
 
 // Shared-memory layout of the dynamic part: [stages x row][stages mbarriers]
 // [G+1 group offsets][G+1 tile counts].
-__host__ __device__ __forceinline__ size_t nv_smem_bytes(int stages, int64_t k, int num_groups) {
-  return static_cast<size_t>(stages) * (2 * k + 8) + 8 * static_cast<size_t>(num_groups + 1);
+__host__ __device__ __forceinline__ size_t nv_smem_bytes(int stages, int64_t row_bytes, int num_groups) {
+  return static_cast<size_t>(stages) * (row_bytes + 8) + 8 * static_cast<size_t>(num_groups + 1);
+}
+
+// silu(g) * u in fp32, sigma in the form that cannot overflow: t = e^-|g| (the
+// square of e^(-|g|/2), so that it rounds into the subnormal range instead of
+// flushing while g e^g is still representable), sigma = (g >= 0 ? 1 : t) / (1 + t).
+// Relative error a few 2^-17 at most (the fast exponential), far below bf16's.
+__device__ __forceinline__ float silu_times(float g, float u) {
+  const float s = __expf(-0.5f * fabsf(g));
+  const float t = s * s;
+  const float sig = (g >= 0.0f ? 1.0f : t) * rcp_approx(1.0f + t);
+  return g * sig * u;
+}
+
+// SwiGLU of two bf16 words: gate (g.lo, g.hi) and up (u.lo, u.hi) -> the bf16 word
+// (h.lo, h.hi), h = silu(g) * u rounded to bf16 (nearest even).
+__device__ __forceinline__ uint32_t swiglu_word(uint32_t g, uint32_t u) {
+  const float h0 = silu_times(__uint_as_float(g << 16), __uint_as_float(u << 16));
+  const float h1 = silu_times(__uint_as_float(g & 0xFFFF0000u), __uint_as_float(u & 0xFFFF0000u));
+  const __nv_bfloat162 h = __floats2bfloat162_rn(h0, h1);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 swiglu_uint4(const uint4 &g, const uint4 &u) {
+  return make_uint4(swiglu_word(g.x, u.x), swiglu_word(g.y, u.y), swiglu_word(g.z, u.z), swiglu_word(g.w, u.w));
 }
 
 // kRep: the scales go to the replicated layout of the forward GEMM's B operand
 // (quantize_nvfp4_weights): per 256 rows and 64-deep step a 4096-byte block
 // [tile0 x 4][tile1 x 4], tile0 / tile1 the 512-byte tiles of the block's rows
 // 0..127 / 128..255; each 4-scale word is stored four times.
-template <int R, bool kRep>
+// kSwiGLU: the row is produced from a gate/up row [g (k values) | u (k values)]
+// staged whole in shared memory: h = silu(g) * u rounded to bf16, optionally
+// written to h_out, then quantized exactly as a bf16 input row would be.
+template <int R, bool kRep, bool kSwiGLU>
 __global__ void __launch_bounds__(kNvMaxThreads, 4)
     nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
                           int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
-                          float *__restrict__ row_scale, int32_t *status, int stages) {
+                          float *__restrict__ row_scale, uint16_t *__restrict__ h_out, int32_t *status,
+                          int stages) {
   __shared__ int ok_flag;
   __shared__ int abort_flag;
   __shared__ uint32_t part[2][kNvMaxThreads / 32];  // per-warp amax of the row, double-buffered by row parity
   __shared__ int64_t sf_row_of[2];                   // byte offset of the row's scales (block 0) in sf
   extern __shared__ __align__(128) uint8_t nv_smem[];
-  const uint32_t row_bytes = static_cast<uint32_t>(k) * 2u;
+  const uint32_t row_bytes = static_cast<uint32_t>(k) * (kSwiGLU ? 4u : 2u);  // staged input row
+  const int64_t row_elems = kSwiGLU ? 2 * static_cast<int64_t>(k) : k;
   uint64_t *bars = reinterpret_cast<uint64_t *>(nv_smem + static_cast<size_t>(stages) * row_bytes);
   int32_t *g_off = reinterpret_cast<int32_t *>(bars + stages);
   int32_t *g_tiles = g_off + num_groups + 1;
@@ -190,7 +219,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       const int64_t r = first + s * stride;
       if (r >= rows) break;
       mbar_arrive_expect_tx(&bars[s], row_bytes);
-      bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + r * k, row_bytes, &bars[s]);
+      bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + r * row_elems, row_bytes, &bars[s]);
     }
   }
 
@@ -214,6 +243,16 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       if (ok && blk < nblk) {
         a[j] = *reinterpret_cast<const uint4 *>(buf + blk * 32 + 16 * swap);
         b[j] = *reinterpret_cast<const uint4 *>(buf + blk * 32 + 16 * (1 - swap));
+        if (kSwiGLU) {
+          const uint8_t *up = buf + 2 * static_cast<size_t>(k);
+          a[j] = swiglu_uint4(a[j], *reinterpret_cast<const uint4 *>(up + blk * 32 + 16 * swap));
+          b[j] = swiglu_uint4(b[j], *reinterpret_cast<const uint4 *>(up + blk * 32 + 16 * (1 - swap)));
+          if (h_out != nullptr) {
+            uint16_t *hb = h_out + row * k + blk * 16;
+            *reinterpret_cast<uint4 *>(hb + 8 * swap) = a[j];
+            *reinterpret_cast<uint4 *>(hb + 8 * (1 - swap)) = b[j];
+          }
+        }
       }
       bmax[j] = amax16_bits(a[j], b[j]);
       m = max(m, bmax[j]);
@@ -236,7 +275,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       if (next < rows) {
         fence_proxy_async_shared();
         mbar_arrive_expect_tx(&bars[s], row_bytes);
-        bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + next * k, row_bytes, &bars[s]);
+        bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + next * row_elems, row_bytes, &bars[s]);
       }
     }
     if (++s == stages) {
@@ -300,32 +339,35 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
 // / R rounded up to warps.  CTAs per SM: as many as 1024 threads and the
 // shared-memory budget allow with at least 3 stages each; stages: the rest of
 // the budget, 3 to 16 rows.
-template <int R, bool kRep>
+template <int R, bool kRep, bool kSwiGLU>
 static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   const int64_t nblk = a.k / 16;
+  const int64_t row_bytes = a.k * (kSwiGLU ? 4 : 2);
   const int threads = static_cast<int>(((nblk + R - 1) / R + 31) / 32 * 32);
   const int64_t fixed = 1024 + 8 * (a.num_groups + 1);
   int per_sm = 1024 / threads;
   if (per_sm > 16) per_sm = 16;
-  while (per_sm > 1 && per_sm * (static_cast<int64_t>(nv_smem_bytes(3, a.k, 0)) + fixed) > kNvSmemBudget) --per_sm;
-  int64_t stages = (kNvSmemBudget / per_sm - fixed) / (2 * a.k + 8);
+  while (per_sm > 1 && per_sm * (static_cast<int64_t>(nv_smem_bytes(3, row_bytes, 0)) + fixed) > kNvSmemBudget)
+    --per_sm;
+  int64_t stages = (kNvSmemBudget / per_sm - fixed) / (row_bytes + 8);
   stages = stages < 3 ? 3 : (stages > 16 ? 16 : stages);
-  const size_t smem = nv_smem_bytes(static_cast<int>(stages), a.k, a.num_groups);
-  cudaError_t err = cudaFuncSetAttribute(nvfp4_pertoken_kernel<R, kRep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  const size_t smem = nv_smem_bytes(static_cast<int>(stages), row_bytes, a.num_groups);
+  auto kernel = nvfp4_pertoken_kernel<R, kRep, kSwiGLU>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int64_t cap = static_cast<int64_t>(a.num_sms) * per_sm;
   const int blocks = static_cast<int>(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
-  nvfp4_pertoken_kernel<R, kRep><<<blocks, threads, smem, a.stream>>>(
-      static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k), a.offsets, a.num_groups, a.codes, a.sf,
-      a.row_scale, a.status, static_cast<int>(stages));
+  kernel<<<blocks, threads, smem, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k),
+                                              a.offsets, a.num_groups, a.codes, a.sf, a.row_scale,
+                                              static_cast<uint16_t *>(a.h_out), a.status, static_cast<int>(stages));
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
   const bool wide = a.k / 16 > kNvMaxThreads;
-  if (a.replicated_sf) return wide ? launch_nvfp4<2, true>(a) : launch_nvfp4<1, true>(a);
-  return wide ? launch_nvfp4<2, false>(a) : launch_nvfp4<1, false>(a);
+  if (a.swiglu) return wide ? launch_nvfp4<2, false, true>(a) : launch_nvfp4<1, false, true>(a);
+  if (a.replicated_sf) return wide ? launch_nvfp4<2, true, false>(a) : launch_nvfp4<1, true, false>(a);
+  return wide ? launch_nvfp4<2, false, false>(a) : launch_nvfp4<1, false, false>(a);
 }
 
 }  // namespace fme

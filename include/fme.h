@@ -7,6 +7,7 @@
  *                             scale per 16 values along K, one FP32 scale per token.
  *   quantize_nvfp4_weights    the same quantization of the stacked expert weights,
  *                             scales written in the forward GEMM's B-operand layout.
+ *   swiglu_quantize_nvfp4     silu(gate) * up of the gate/up output, quantized as above.
  *   quantize_mxfp8            standard MXFP8 of the backward: E4M3 codes, one E8M0
  *                             scale per 32 values, row-wise or column-wise.
  *   grouped_gemm_fwd_nvfp4    Y_e = X_e W_e^T per expert, per-token scales applied
@@ -136,6 +137,28 @@ fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const
  */
 fme_status quantize_nvfp4_weights(const void *x, int64_t rows, int64_t k, uint8_t *codes, uint8_t *sf,
                                   float *row_scale, int32_t *dev_status, void *stream);
+
+/*
+ * swiglu_quantize_nvfp4 -- the activation between the forward GEMMs fused with
+ * the NVFP4 per-token quantization of its output.  Row t of gate_up [rows x
+ * 2*inter] (bf16, the gate/up GEMM output) is [g (inter values) | u (inter
+ * values)]; h = silu(g) * u, silu(v) = v / (1 + e^-v), evaluated in fp32 and
+ * rounded to bf16 (nearest even), is quantized exactly as
+ * quantize_nvfp4_pertoken quantizes a bf16 row (same codes, scale layout and row
+ * scale for the same h).  The pages give DeepSeek-V3-class experts ("Scaling
+ * and Optimizing Frontier Model Training", "MXFP8 expert kernels"); the gated
+ * activation is their SwiGLU.
+ *
+ *   gate_up    device bf16 [rows x 2*inter]
+ *   rows, inter  inter a multiple of 64, 64 <= inter <= 8192
+ *   offsets, num_groups  as quantize_nvfp4_pertoken
+ *   codes, sf, row_scale as quantize_nvfp4_pertoken with k = inter
+ *   h          device bf16 [rows x inter] receiving the activation (needed by
+ *              the backward), or NULL
+ */
+fme_status swiglu_quantize_nvfp4(const void *gate_up, int64_t rows, int64_t inter, const int32_t *offsets,
+                                 int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale, void *h,
+                                 int32_t *dev_status, void *stream);
 
 /*
  * quantize_mxfp8 -- standard MXFP8 (OCP MX v1.0 rule) of the MoE backward.

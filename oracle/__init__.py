@@ -81,6 +81,7 @@ def _declare(lib):
     lib.fme_orc_quant_mxfp8_cols.argtypes = [P, I64, I64, P, I32, I64, P, P, P]
     lib.fme_orc_dequant_mxfp8.argtypes = [P, P, I64, I64, P]
     lib.fme_orc_gemm_abt.argtypes = [P, P, I64, I64, I64, P]
+    lib.fme_orc_swiglu.argtypes = [P, I64, I64, P]
     for name in ("fme_orc_e2m1_encode_array", "fme_orc_e4m3_encode_array", "fme_orc_quant_nvfp4",
                  "fme_orc_dequant_nvfp4", "fme_orc_quant_mxfp8_rows", "fme_orc_quant_mxfp8_cols",
                  "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt"):
@@ -192,6 +193,16 @@ class Oracle:
         out = np.empty((rows, cols), np.float64)
         self.lib.fme_orc_dequant_mxfp8(_p(codes), _p(sf), rows, cols, _p(out))
         return out
+
+    # SwiGLU --------------------------------------------------------------
+    def swiglu(self, y_gu_bits) -> np.ndarray:
+        """h = silu(g) * u in fp64 for bf16 rows [g | u] (bit patterns)."""
+        y = _bits(y_gu_bits)
+        rows, two_inter = y.shape
+        inter = two_inter // 2
+        h = np.empty((rows, inter), np.float64)
+        self.lib.fme_orc_swiglu(_p(y), rows, inter, _p(h))
+        return h
 
     # GEMM ----------------------------------------------------------------
     def gemm_abt(self, a, b) -> np.ndarray:

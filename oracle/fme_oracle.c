@@ -24,6 +24,11 @@
  *     core dequantizes inside the multiply.  The oracle computes that result
  *     from its plain definition: dequantize both operands exactly, multiply
  *     and sum in fp64.
+ *   - Same page, same section: the experts are DeepSeek-V3-class (hidden 7168,
+ *     intermediate 2048; the gate/up projection is twice the intermediate
+ *     width).  The activation between the two projections is read as SwiGLU,
+ *     h = silu(g) * u with silu(v) = v / (1 + e^-v), g and u the two halves of
+ *     the gate/up output; the oracle evaluates it in fp64.
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *   - per-token decode scale S_t = amax_t / (6 * 448), fp32, IEEE division;
@@ -350,6 +355,21 @@ void fme_orc_gemm_abt(const double *a, const double *b, int64_t m, int64_t n, in
             for (int64_t q = 0; q < k; ++q)
                 acc += a[i * k + q] * b[j * k + q];
             y[i * n + j] = acc;
+        }
+    }
+}
+
+/* -------------------------------------------------------------- SwiGLU -- */
+
+/* h [rows x inter] = silu(g) * u in fp64, where row t of y_gu [rows x 2 inter]
+ * (bf16) is [g_t (inter values) | u_t (inter values)] and silu(v) = v / (1 + e^-v). */
+void fme_orc_swiglu(const uint16_t *y_gu, int64_t rows, int64_t inter, double *h) {
+    for (int64_t t = 0; t < rows; ++t) {
+        const uint16_t *row = y_gu + t * 2 * inter;
+        for (int64_t j = 0; j < inter; ++j) {
+            const double g = (double)bf16_value(row[j]);
+            const double u = (double)bf16_value(row[inter + j]);
+            h[t * inter + j] = g / (1.0 + exp(-g)) * u;
         }
     }
 }

@@ -392,4 +392,38 @@ def check_quantized_gemm_end_to_end(orc):
     assert np.allclose(y, want, rtol=1e-14, atol=0), (y, want)
 
 
+def _swiglu_rows(g, u):
+    return synth.bf16_bits(np.concatenate([np.asarray(g, np.float32), np.asarray(u, np.float32)], axis=1))
+
+
+def check_swiglu_closed_forms(orc):
+    """silu(0) = 0; silu(v) - silu(-v) = v (sigma(v) + sigma(-v) = 1), so
+    h(g, u) - h(-g, u) = g u; silu(v) -> v for large v and -> 0 for very negative
+    v; the bf16 gate and up halves are read from the right half of the row."""
+    g = np.array([[0.0, 0.5, -1.25, 3.0, -7.0, 20.0, -30.0, 100.0]], np.float32)
+    u = np.array([[1.0, -2.0, 0.75, 1.5, -0.5, 2.0, 4.0, -1.0]], np.float32)
+    hp = orc.swiglu(_swiglu_rows(g, u))
+    hn = orc.swiglu(_swiglu_rows(-g, u))
+    gd, ud = g.astype(np.float64), u.astype(np.float64)
+    assert hp[0, 0] == 0.0
+    assert np.allclose(hp - hn, gd * ud, rtol=1e-14, atol=1e-300)
+    assert abs(hp[0, 7] - gd[0, 7] * ud[0, 7]) < 1e-30 * abs(gd[0, 7])
+    assert abs(hp[0, 6]) < 1e-10
+    big = orc.swiglu(_swiglu_rows(np.full((1, 4), 88.0), np.full((1, 4), 1.0)))
+    assert np.allclose(big, 88.0, rtol=1e-30, atol=1e-30)
+
+
+def check_swiglu_vs_scipy(orc):
+    """fp64 silu(g) * u against scipy's logistic function (another implementation
+    of e^-v), on bf16 inputs spanning the range that matters."""
+    from scipy.special import expit
+
+    rng = np.random.default_rng(17)
+    g = synth.bf16_float(synth.bf16_bits(rng.standard_normal((8, 96)) * 4.0))
+    u = synth.bf16_float(synth.bf16_bits(rng.standard_normal((8, 96))))
+    h = orc.swiglu(_swiglu_rows(g, u))
+    want = g.astype(np.float64) * expit(g.astype(np.float64)) * u.astype(np.float64)
+    assert np.allclose(h, want, rtol=4e-16, atol=1e-300)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

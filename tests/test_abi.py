@@ -24,7 +24,8 @@ def declared_functions():
 
 def test_header_declares_the_five_calls():
     names = declared_functions()
-    for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_weights", "quantize_mxfp8", "grouped_gemm_fwd_nvfp4",
+    for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_weights", "swiglu_quantize_nvfp4", "quantize_mxfp8",
+                 "grouped_gemm_fwd_nvfp4",
                  "grouped_gemm_fwd_mxfp8",
                  "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8"):
         assert call in names
@@ -78,6 +79,13 @@ def test_host_argument_checks(lib):
     assert qw(None, 256, 256, good, good, good, None, _stream()) == 1
     assert qw(good, 256, 256, good, odd, good, None, _stream()) == 2
     assert qw(good, 0, 256, None, None, None, None, _stream()) == 0       # nothing to do
+    sq = lib.swiglu_quantize_nvfp4
+    assert sq(good, 10, 96, None, 1, good, good, good, None, None, _stream()) == 3      # inter % 64
+    assert sq(good, 10, 8256, None, 1, good, good, good, None, None, _stream()) == 3
+    assert sq(good, 10, 256, None, 2, good, good, good, None, None, _stream()) == 1     # groups without offsets
+    assert sq(None, 10, 256, None, 1, good, good, good, None, None, _stream()) == 1
+    assert sq(good, 10, 256, None, 1, good, good, good, odd, None, _stream()) == 2      # h misaligned
+    assert sq(good, 0, 256, None, 1, None, None, None, None, None, _stream()) == 0
     m = lib.quantize_mxfp8
     assert m(good, 10, 256, 2, None, 1, good, good, None, None, _stream()) == 1
     assert m(good, 10, 256, 0, None, 1, good, good, good, None, _stream()) == 1  # row-wise takes no padded offsets

@@ -44,6 +44,11 @@ MUTANTS = {
                                     "double q = ldexp((double)v[j], 128 - (int)sc);"),
     "colwise_pads_to_32": ("int64_t padded = ((n_g + 127) / 128) * 128;", "int64_t padded = ((n_g + 31) / 32) * 32;"),
     # GEMM
+    "swiglu_sigmoid_of_minus_g": ("h[t * inter + j] = g / (1.0 + exp(-g)) * u;",
+                                  "h[t * inter + j] = g / (1.0 + exp(g)) * u;"),
+    "swiglu_gate_up_halves_swapped": ("const double g = (double)bf16_value(row[j]);\n            const double u = (double)bf16_value(row[inter + j]);",
+                                      "const double u = (double)bf16_value(row[j]);\n            const double g = (double)bf16_value(row[inter + j]);"),
+    "swiglu_drops_up": ("h[t * inter + j] = g / (1.0 + exp(-g)) * u;", "h[t * inter + j] = g / (1.0 + exp(-g));"),
     "gemm_transposed_operand": ("acc += a[i * k + q] * b[j * k + q];", "acc += a[i * k + q] * b[q * n + j];"),
     "gemm_drops_last_term": ("for (int64_t q = 0; q < k; ++q)\n                acc +=",
                              "for (int64_t q = 0; q < k - 1; ++q)\n                acc +="),
