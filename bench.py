@@ -408,6 +408,71 @@ def run_extras(step, args, bf16_sus):
         ach = flops / (ms * 1e-3) / 1e12
         out[name] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac_fp8": round(ach / (bf16_sus * 2), 3)}
     del xq, wq, hq, wdq
+    out.update(run_routing_extras(step, args, hbm))
+    return out
+
+
+def _time_call(fn, steps):
+    import torch
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_routing_extras(step, args, hbm):
+    """Routing around the expert GEMMs on the same rows: R = tokens x top-8 routed
+    rows of 32768 tokens over the 32 experts (synthetic Zipf-popular choices).
+    Grouping (3 launches), the grouped NVFP4 and MXFP8 quantizations that gather
+    the tokens' rows, and the weighted combine of the down projection's output.
+    GB/s counts every grouped row read once (the gather reads each token top_k
+    times; L2 may serve some of those) and every output written once."""
+    import torch
+
+    from fp8_moe_expert_gb300 import synth
+
+    f, st = step.fme, step.status
+    R, H, E = step.R, step.H, step.E
+    top_k = 8
+    tokens = R // top_k
+    ids_np, w_np = synth.topk_routing(tokens=tokens, top_k=top_k, experts=E)
+    ids = torch.from_numpy(ids_np).to(step.dev)
+    weights = torch.from_numpy(w_np).to(step.dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=step.dev)
+    row_of = torch.empty((tokens, top_k), dtype=torch.int32, device=step.dev)
+    src = torch.empty(R, dtype=torch.int32, device=step.dev)
+    ws = torch.empty(f.route_workspace_bytes(tokens, top_k, E), dtype=torch.uint8, device=step.dev)
+    x_tok = step.x[:tokens]
+    out_tok = torch.empty((tokens, H), dtype=torch.bfloat16, device=step.dev)
+    out = {}
+    ms = _time_call(lambda: f.moe_route(ids, E, offsets=off, row_of=row_of, src_row=src, workspace=ws, status=st),
+                    args.steps)
+    out["moe_route"] = {"ms": round(ms, 4), "tokens": tokens, "top_k": top_k}
+    q_bytes = R * (2 * H + H // 2 + H // 16 + 4)
+    ms = _time_call(lambda: f.permute_quantize_nvfp4(x_tok, src, top_k, off, codes=step.xq[0], sf=step.xq[1],
+                                                     row_scale=step.xq[2], status=st), args.steps)
+    gbs = q_bytes / (ms * 1e-3) / 1e9
+    out["permute_quantize_nvfp4"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    m_bytes = R * (2 * H + H + H // 32)
+    ms = _time_call(lambda: f.permute_quantize_mxfp8(x_tok, src, top_k, off, codes=step.dyr[0], sf=step.dyr[1],
+                                                     status=st), args.steps)
+    gbs = m_bytes / (ms * 1e-3) / 1e9
+    out["permute_quantize_mxfp8"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    c_bytes = R * (2 * H + 8) + tokens * 2 * H
+    ms = _time_call(lambda: f.moe_combine(step.y_d, row_of, weights, out=out_tok, status=st), args.steps)
+    gbs = c_bytes / (ms * 1e-3) / 1e9
+    out["moe_combine"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    code, raw = f.read_device_status(st)
+    if code != 0:
+        raise RuntimeError(f"routing extras: device status {code} ({raw:#x})")
+    del ids, weights, off, row_of, src, ws, out_tok
     return out
 
 

@@ -20,6 +20,7 @@ COLWISE = 1
 MAX_GROUPS = 1024
 DEV_TIMEOUT = 0x1
 DEV_BAD_OFFSETS = 0x2
+DEV_BAD_INDEX = 0x4
 
 _lib = None
 _lock = threading.Lock()
@@ -71,6 +72,11 @@ SYMBOLS = {
                                          "p"]),
     "grouped_gemm_wgrad_mxfp8": ("i32", ["p", "p", "i64", "p", "p", "i64", "p", "i32", "i64", "i64", "p", "p",
                                          "p"]),
+    "moe_route": ("i32", ["p", "i64", "i32", "i32", "p", "p", "p", "p", "i64", "p", "p"]),
+    "permute_quantize_nvfp4": ("i32", ["p", "i64", "i64", "p", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
+    "permute_quantize_mxfp8": ("i32", ["p", "i64", "i64", "p", "i32", "p", "i32", "p", "p", "p", "p"]),
+    "moe_combine": ("i32", ["p", "i64", "p", "p", "i64", "i32", "i64", "p", "p", "p"]),
+    "fme_route_workspace_bytes": ("i64", ["i64", "i32", "i32"]),
     "fme_sf_padded_rows": ("i64", ["i64", "i32"]),
     "fme_sf_bytes": ("i64", ["i64", "i64", "i32", "i32"]),
     "fme_colwise_ld": ("i64", ["i64", "i32"]),
@@ -107,6 +113,10 @@ def colwise_ld(rows: int, num_groups: int = 1) -> int:
 
 def sf_bytes_nvfp4_weights(rows: int, k: int) -> int:
     return int(lib().fme_sf_bytes_nvfp4_weights(rows, k))
+
+
+def route_workspace_bytes(tokens: int, top_k: int, num_experts: int) -> int:
+    return int(lib().fme_route_workspace_bytes(tokens, top_k, num_experts))
 
 
 def _ptr(t):
@@ -321,6 +331,88 @@ def grouped_gemm_wgrad_mxfp8(a_codes, a_sf, lda, b_codes, b_sf, ldb, padded_offs
                                         _ptr(padded_offsets), e, m, n, _ptr(y), _ptr(status), _stream(stream))
     _check(st, "grouped_gemm_wgrad_mxfp8")
     return y
+
+
+# ------------------------------------------------------------------ routing --
+def moe_route(topk_ids, num_experts, *, offsets=None, row_of=None, src_row=None, workspace=None, status=None,
+              stream=None):
+    """Group the assignments of topk_ids [tokens, top_k] (int32 expert ids) by
+    expert, stably -> (offsets [E+1], row_of [tokens, top_k], src_row [tokens*top_k]),
+    all int32."""
+    import torch
+
+    tokens, top_k = topk_ids.shape
+    dev = topk_ids.device
+    if offsets is None:
+        offsets = _empty((num_experts + 1,), torch.int32, dev)
+    if row_of is None:
+        row_of = _empty((tokens, top_k), torch.int32, dev)
+    if src_row is None:
+        src_row = _empty((tokens * top_k,), torch.int32, dev)
+    need = route_workspace_bytes(tokens, top_k, num_experts)
+    if workspace is None:
+        workspace = _empty((need,), torch.uint8, dev)
+    st = lib().moe_route(_ptr(topk_ids), tokens, top_k, num_experts, _ptr(offsets), _ptr(row_of), _ptr(src_row),
+                         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+                         _stream(stream))
+    _check(st, "moe_route")
+    return offsets, row_of, src_row
+
+
+def permute_quantize_nvfp4(x, src_row, top_k, offsets, *, codes=None, sf=None, row_scale=None, status=None,
+                           stream=None):
+    """NVFP4 per-token quantization of the grouped rows x[src_row // top_k] ->
+    (codes [tokens*top_k, k/2], sf, row_scale [tokens*top_k])."""
+    import torch
+
+    tokens, k = x.shape
+    rows = tokens * top_k
+    g = offsets.numel() - 1
+    dev = x.device
+    if codes is None:
+        codes = _empty((rows, k // 2), torch.uint8, dev)
+    if sf is None:
+        sf = _empty((max(sf_bytes(rows, k, 16, g), 16),), torch.uint8, dev)
+    if row_scale is None:
+        row_scale = _empty((rows,), torch.float32, dev)
+    st = lib().permute_quantize_nvfp4(_ptr(x), tokens, k, _ptr(src_row), top_k, _ptr(offsets), g, _ptr(codes),
+                                      _ptr(sf), _ptr(row_scale), _ptr(status), _stream(stream))
+    _check(st, "permute_quantize_nvfp4")
+    return codes, sf, row_scale
+
+
+def permute_quantize_mxfp8(x, src_row, top_k, offsets, *, codes=None, sf=None, status=None, stream=None):
+    """MXFP8 row-wise quantization of the grouped rows x[src_row // top_k] ->
+    (codes [tokens*top_k, k], sf)."""
+    import torch
+
+    tokens, k = x.shape
+    rows = tokens * top_k
+    g = offsets.numel() - 1
+    dev = x.device
+    if codes is None:
+        codes = _empty((rows, k), torch.uint8, dev)
+    if sf is None:
+        sf = _empty((max(sf_bytes(rows, k, 32, g), 16),), torch.uint8, dev)
+    st = lib().permute_quantize_mxfp8(_ptr(x), tokens, k, _ptr(src_row), top_k, _ptr(offsets), g, _ptr(codes),
+                                      _ptr(sf), _ptr(status), _stream(stream))
+    _check(st, "permute_quantize_mxfp8")
+    return codes, sf
+
+
+def moe_combine(y, row_of, weights, *, out=None, status=None, stream=None):
+    """out[t] = bf16(sum_k weights[t, k] * y[row_of[t, k]]) (fp32, k in order) for
+    grouped expert outputs y [rows_y, n] bf16 -> out [tokens, n] bf16."""
+    import torch
+
+    rows_y, n = y.shape
+    tokens, top_k = row_of.shape
+    if out is None:
+        out = _empty((tokens, n), torch.bfloat16, y.device)
+    st = lib().moe_combine(_ptr(y), rows_y, _ptr(row_of), _ptr(weights), tokens, top_k, n, _ptr(out), _ptr(status),
+                           _stream(stream))
+    _check(st, "moe_combine")
+    return out
 
 
 def read_device_status(status, stream=None) -> tuple[int, int]:

@@ -18,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIBRARY = os.path.join(HERE, "libfme.so")
-SOURCES = ["api.cu", "quant_nvfp4.cu", "quant_mxfp8.cu", "gemm.cu"]
+SOURCES = ["api.cu", "quant_nvfp4.cu", "quant_mxfp8.cu", "gemm.cu", "route.cu"]
 HEADERS = ["fme_device.cuh", "fme_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

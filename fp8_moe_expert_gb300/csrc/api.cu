@@ -150,6 +150,13 @@ int64_t fme_sf_bytes(int64_t rows, int64_t cols, int32_t block, int32_t num_grou
 
 int64_t fme_colwise_ld(int64_t rows, int32_t num_groups) { return padded_rows_bound(rows, num_groups); }
 
+int64_t fme_route_workspace_bytes(int64_t tokens, int32_t top_k, int32_t num_experts) {
+  if (tokens < 0 || top_k < 1 || num_experts < 1) return 0;
+  const int64_t chunks = (tokens * top_k + fme::kRouteChunkHost - 1) / fme::kRouteChunkHost;
+  const int64_t b = chunks * num_experts * 4;
+  return b < 16 ? 16 : b;
+}
+
 int64_t fme_sf_bytes_nvfp4_weights(int64_t rows, int64_t k) {
   if (rows < 0 || k < 0 || rows % 256 != 0 || k % 64 != 0) return 0;
   return (rows / 256) * (k / 64) * 4096;
@@ -169,6 +176,7 @@ const char *fme_error_string(fme_status status) {
     case FME_ERR_CUDA: return "CUDA error";
     case FME_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
     case FME_ERR_DEVICE_BAD_OFFSETS: return "offsets do not rise from 0 to rows";
+    case FME_ERR_DEVICE_BAD_INDEX: return "an expert id or a row index out of range";
     default: return "unknown status";
   }
 }
@@ -183,6 +191,7 @@ fme_status fme_read_device_status(const int32_t *dev_status, void *stream, int32
   if (err != cudaSuccess) return cuda_fail(err, "cudaStreamSynchronize");
   if (raw) *raw = host;
   if (host & FME_DEV_BAD_OFFSETS) return FME_ERR_DEVICE_BAD_OFFSETS;
+  if (host & FME_DEV_BAD_INDEX) return FME_ERR_DEVICE_BAD_INDEX;
   if (host & FME_DEV_TIMEOUT) return FME_ERR_DEVICE_TIMEOUT;
   return FME_OK;
 }
@@ -244,6 +253,91 @@ fme_status swiglu_quantize_nvfp4(const void *gate_up, int64_t rows, int64_t inte
   a.h_out = h;
   cudaError_t err = fme::launch_quantize_nvfp4(a);
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "swiglu_quantize_nvfp4 launch");
+}
+
+fme_status moe_route(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int32_t num_experts, int32_t *offsets,
+                     int32_t *row_of, int32_t *src_row, void *workspace, int64_t workspace_bytes,
+                     int32_t *dev_status, void *stream) {
+  if (tokens < 0 || top_k < 1 || top_k > 64 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (tokens * top_k > (int64_t(1) << 31) - 1) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets || !workspace) return FME_ERR_INVALID_ARGUMENT;
+  if (tokens > 0 && (!topk_ids || !row_of || !src_row)) return FME_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < fme_route_workspace_bytes(tokens, top_k, num_experts)) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(topk_ids) || !aligned16(offsets) || !aligned16(row_of) || !aligned16(src_row) ||
+      !aligned16(workspace))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchRoute r{topk_ids, tokens, top_k, num_experts, offsets, row_of, src_row,
+                     static_cast<int32_t *>(workspace), dev_status, static_cast<cudaStream_t>(stream)};
+  cudaError_t err = fme::launch_route(r);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "moe_route launch");
+}
+
+fme_status permute_quantize_nvfp4(const void *x, int64_t tokens, int64_t k, const int32_t *src_row, int32_t top_k,
+                                  const int32_t *offsets, int32_t num_experts, uint8_t *codes, uint8_t *sf,
+                                  float *row_scale, int32_t *dev_status, void *stream) {
+  if (tokens < 0 || top_k < 1 || top_k > 64 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0 || k < 64 || k > 8192) return FME_ERR_UNSUPPORTED_SHAPE;
+  const int64_t rows = tokens * top_k;
+  if (rows > (int64_t(1) << 31) - 1) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets) return FME_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return FME_OK;
+  if (!x || !src_row || !codes || !sf || !row_scale) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(src_row) || !aligned16(codes) || !aligned16(sf) || !aligned16(row_scale) ||
+      !aligned16(offsets))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchNvfp4 a{x, rows, k, offsets, num_experts, codes, sf, row_scale, dev_status, sms,
+                     static_cast<cudaStream_t>(stream)};
+  a.gather = src_row;
+  a.gather_div = top_k;
+  a.gather_limit = tokens;
+  cudaError_t err = fme::launch_quantize_nvfp4(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "permute_quantize_nvfp4 launch");
+}
+
+fme_status permute_quantize_mxfp8(const void *x, int64_t tokens, int64_t k, const int32_t *src_row, int32_t top_k,
+                                  const int32_t *offsets, int32_t num_experts, uint8_t *codes, uint8_t *sf,
+                                  int32_t *dev_status, void *stream) {
+  if (tokens < 0 || top_k < 1 || top_k > 64 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (k % 32 != 0 || k < 32 || k > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
+  const int64_t rows = tokens * top_k;
+  if (rows > (int64_t(1) << 31) - 1 - 128 * static_cast<int64_t>(num_experts)) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets) return FME_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return FME_OK;
+  if (!x || !src_row || !codes || !sf) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(src_row) || !aligned16(codes) || !aligned16(sf)) return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchMxfp8 a{x, rows, k, offsets, num_experts, codes, sf, nullptr, 0, dev_status, sms,
+                     static_cast<cudaStream_t>(stream)};
+  a.gather = src_row;
+  a.gather_div = top_k;
+  a.gather_limit = tokens;
+  cudaError_t err = fme::launch_quantize_mxfp8_rows(a);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "permute_quantize_mxfp8 launch");
+}
+
+fme_status moe_combine(const void *y, int64_t rows_y, const int32_t *row_of, const float *weights, int64_t tokens,
+                       int32_t top_k, int64_t n, void *out, int32_t *dev_status, void *stream) {
+  if (tokens < 0 || rows_y < 0 || top_k < 1 || top_k > 64 || n < 0) return FME_ERR_INVALID_ARGUMENT;
+  if (n % 8 != 0 || n == 0) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (tokens * top_k > (int64_t(1) << 31) - 1) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (tokens == 0) return FME_OK;
+  if (!row_of || !weights || !out || (rows_y > 0 && !y)) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(y) || !aligned16(row_of) || !aligned16(weights) || !aligned16(out)) return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchCombine c{y, row_of, weights, tokens, top_k, n, rows_y, out, dev_status, sms,
+                       static_cast<cudaStream_t>(stream)};
+  cudaError_t err = fme::launch_combine(c);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "moe_combine launch");
 }
 
 fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axis, const int32_t *offsets,

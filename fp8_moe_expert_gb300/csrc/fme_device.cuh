@@ -14,6 +14,7 @@ namespace fme {
 // Bits OR-ed into the caller's device status word (mirror FME_DEV_* in fme.h).
 constexpr int kDevTimeout = 0x1;
 constexpr int kDevBadOffsets = 0x2;
+constexpr int kDevBadIndex = 0x4;
 constexpr int kMaxGroups = 1024;
 
 // A bounded wait gives up after this long (ns of %globaltimer); real waits in

@@ -21,6 +21,32 @@ struct LaunchNvfp4 {
   bool replicated_sf = false;  // scales in the forward GEMM's B-operand layout (quantize_nvfp4_weights)
   bool swiglu = false;         // x is a gate/up output [rows x 2k]; quantize silu(gate) * up
   void *h_out = nullptr;       // swiglu: the bf16 activation [rows x k], or NULL
+  const int32_t *gather = nullptr;  // row r reads input row gather[r] / gather_div (permuted tokens)
+  int32_t gather_div = 1;
+  int64_t gather_limit = 0;         // input rows; gathered rows outside [0, limit) are reported
+};
+
+struct LaunchRoute {
+  const int32_t *ids;
+  int64_t tokens;
+  int32_t top_k, num_experts;
+  int32_t *offsets, *row_of, *src_row;
+  int32_t *ws;  // [chunks x num_experts]
+  int32_t *status;
+  cudaStream_t stream;
+};
+
+struct LaunchCombine {
+  const void *y;
+  const int32_t *row_of;
+  const float *weights;
+  int64_t tokens;
+  int32_t top_k;
+  int64_t n, rows_y;
+  void *out;
+  int32_t *status;
+  int num_sms;
+  cudaStream_t stream;
 };
 
 struct LaunchMxfp8 {
@@ -34,6 +60,11 @@ struct LaunchMxfp8 {
   int32_t *status;
   int num_sms;
   cudaStream_t stream;
+  // Row-wise only: row r reads source row gather[r] / gather_div, which must lie
+  // in [0, gather_limit).
+  const int32_t *gather = nullptr;
+  int32_t gather_div = 1;
+  int64_t gather_limit = 0;
 };
 
 enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2, kFwdMxfp8 = 3 };
@@ -59,5 +90,8 @@ cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf);
 cudaError_t launch_grouped_gemm(const LaunchGemm &a);
+cudaError_t launch_route(const LaunchRoute &r);
+cudaError_t launch_combine(const LaunchCombine &c);
+constexpr int64_t kRouteChunkHost = 1024;  // assignments per routing chunk (route.cu)
 
 }  // namespace fme

@@ -52,13 +52,16 @@ __device__ __forceinline__ uint32_t e4m3x4_words(uint32_t a, uint32_t b, float s
 // One warp per row; lane l handles 8 consecutive values of every 256-wide
 // chunk, four lanes form a 32-block (two shuffles for its amax).  Codes leave as
 // 8-byte stores (256 contiguous bytes per warp); lanes 0 and 16 each store four
-// consecutive scales as one word of the tiled layout.
+// consecutive scales as one word of the tiled layout.  With `gather`, row r reads
+// source row gather[r] / gather_div (grouped rows of routed tokens); an index
+// outside [0, gather_limit) is reported and reads source row 0.
 constexpr int kRowUnroll = 4;
 
 __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
                                                          const int32_t *__restrict__ offsets, int num_groups,
                                                          uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
-                                                         int32_t *status) {
+                                                         int32_t *status, const int32_t *__restrict__ gather,
+                                                         int gather_div, int64_t gather_limit) {
   __shared__ GroupTable groups;
   __shared__ int ok_flag;
   if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
@@ -73,7 +76,15 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
        row += static_cast<int64_t>(gridDim.x) * warps) {
     const int g = find_group(groups.off, num_groups, row);
     const int64_t prow = 128 * static_cast<int64_t>(groups.tiles[g]) + (row - groups.off[g]);
-    const uint16_t *xr = x + row * cols;
+    int64_t src = row;
+    if (gather) {
+      src = __ldg(gather + row) / gather_div;
+      if (src < 0 || src >= gather_limit) {
+        if (lane == 0) report(status, kDevBadIndex);
+        src = 0;
+      }
+    }
+    const uint16_t *xr = x + src * cols;
     uint8_t *cr = codes + row * cols;
     for (int base = 0; base < cols; base += 256 * kRowUnroll) {
       uint4 v[kRowUnroll];
@@ -312,7 +323,8 @@ cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a) {
   const int blocks = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
   mxfp8_rows_kernel<<<blocks, threads, 0, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows,
                                                        static_cast<int>(a.cols), a.offsets, a.num_groups,
-                                                       a.codes, a.sf, a.status);
+                                                       a.codes, a.sf, a.status, a.gather, a.gather_div,
+                                                       a.gather_limit);
   return cudaGetLastError();
 }
 

@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
                           int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
                           float *__restrict__ row_scale, uint16_t *__restrict__ h_out, int32_t *status,
-                          int stages) {
+                          int stages, const int32_t *__restrict__ gather, int gather_div, int64_t gather_limit) {
   __shared__ int ok_flag;
   __shared__ int abort_flag;
   __shared__ uint32_t part[2][kNvMaxThreads / 32];  // per-warp amax of the row, double-buffered by row parity
@@ -214,12 +214,22 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     fence_barrier_init();
   }
   __syncthreads();
+  // input row of output row r: r itself, or the gathered token (checked)
+  auto src_of = [&](int64_t r) -> int64_t {
+    if (gather == nullptr) return r;
+    const int64_t g = __ldg(gather + r) / gather_div;
+    if (g < 0 || g >= gather_limit) {
+      report(status, kDevBadIndex);
+      return 0;
+    }
+    return g;
+  };
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       const int64_t r = first + s * stride;
       if (r >= rows) break;
       mbar_arrive_expect_tx(&bars[s], row_bytes);
-      bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + r * row_elems, row_bytes, &bars[s]);
+      bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + src_of(r) * row_elems, row_bytes, &bars[s]);
     }
   }
 
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       if (next < rows) {
         fence_proxy_async_shared();
         mbar_arrive_expect_tx(&bars[s], row_bytes);
-        bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + next * row_elems, row_bytes, &bars[s]);
+        bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + src_of(next) * row_elems, row_bytes, &bars[s]);
       }
     }
     if (++s == stages) {
@@ -359,7 +369,8 @@ static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   const int blocks = static_cast<int>(a.rows < cap ? (a.rows > 0 ? a.rows : 1) : cap);
   kernel<<<blocks, threads, smem, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k),
                                               a.offsets, a.num_groups, a.codes, a.sf, a.row_scale,
-                                              static_cast<uint16_t *>(a.h_out), a.status, static_cast<int>(stages));
+                                              static_cast<uint16_t *>(a.h_out), a.status, static_cast<int>(stages),
+                                              a.gather, a.gather_div, a.gather_limit);
   return cudaGetLastError();
 }
 

@@ -87,6 +87,28 @@ def zipf_counts(rows: int = 262144, experts: int = EXPERTS, s: float = 1.2, empt
     return counts
 
 
+def topk_routing(tokens: int = 32768, top_k: int = 8, experts: int = EXPERTS, s: float = 1.2, seed: int = 6):
+    """Per-token expert choices in the router-replay form: ``top_k`` distinct expert
+    ids per token, experts drawn with Zipf(s) popularity over a seeded order
+    (Gumbel top-k sampling without replacement), and positive routing weights
+    normalised to sum 1 per token.
+
+    Returns (ids int32 [tokens, top_k], weights float32 [tokens, top_k])."""
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(experts)
+    logp = np.empty(experts)
+    logp[order] = -s * np.log(np.arange(1, experts + 1, dtype=np.float64))
+    ids = np.empty((tokens, top_k), np.int32)
+    step = 8192
+    for t0 in range(0, tokens, step):
+        t1 = min(tokens, t0 + step)
+        keys = logp[None, :] + rng.gumbel(size=(t1 - t0, experts))
+        ids[t0:t1] = np.argsort(-keys, axis=1, kind="stable")[:, :top_k]
+    w = rng.uniform(0.05, 1.0, size=(tokens, top_k))
+    weights = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    return ids, weights
+
+
 # -------------------------------------------------------------- numpy inputs --
 def tiny(seed: int = 0):
     """One expert: X [128 x 256] ~ N(0,1) with 1% of entries x30; W [256 x 256] ~ N(0, 0.02^2).

@@ -8,6 +8,10 @@
  *   quantize_nvfp4_weights    the same quantization of the stacked expert weights,
  *                             scales written in the forward GEMM's B-operand layout.
  *   swiglu_quantize_nvfp4     silu(gate) * up of the gate/up output, quantized as above.
+ *   moe_route, permute_quantize_nvfp4, permute_quantize_mxfp8, moe_combine
+ *                             grouping the routed tokens by expert (quantizing
+ *                             them in grouped order) and combining the experts'
+ *                             outputs per token.
  *   quantize_mxfp8            standard MXFP8 of the backward: E4M3 codes, one E8M0
  *                             scale per 32 values, row-wise or column-wise.
  *   grouped_gemm_fwd_nvfp4    Y_e = X_e W_e^T per expert, per-token scales applied
@@ -79,10 +83,12 @@ typedef int32_t fme_status;
 #define FME_ERR_CUDA 5               /* a CUDA runtime or driver call failed; see fme_last_cuda_error() */
 #define FME_ERR_DEVICE_TIMEOUT 6     /* reported by fme_read_device_status() */
 #define FME_ERR_DEVICE_BAD_OFFSETS 7 /* reported by fme_read_device_status() */
+#define FME_ERR_DEVICE_BAD_INDEX 8   /* reported by fme_read_device_status() */
 
 /* Bits a kernel ORs into *dev_status. */
 #define FME_DEV_TIMEOUT 0x1     /* a bounded wait inside a GEMM ran out; the kernel gave up */
 #define FME_DEV_BAD_OFFSETS 0x2 /* offsets not rising from 0 to rows (or padded offsets invalid) */
+#define FME_DEV_BAD_INDEX 0x4   /* an expert id or a gathered row index out of range */
 
 #define FME_ROWWISE 0
 #define FME_COLWISE 1
@@ -159,6 +165,70 @@ fme_status quantize_nvfp4_weights(const void *x, int64_t rows, int64_t k, uint8_
 fme_status swiglu_quantize_nvfp4(const void *gate_up, int64_t rows, int64_t inter, const int32_t *offsets,
                                  int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale, void *h,
                                  int32_t *dev_status, void *stream);
+
+/*
+ * Routing: grouping the routed tokens by expert, and combining back.
+ *
+ * "Cursor Composer 2 report deep dive", section 2, and "Composer 2 Technical
+ * Report" (papercache.org summary), section 6.1: tokens are quantized before they
+ * are dispatched to their experts, and the experts' outputs are combined per token
+ * in BF16.  Section 6.2 of the report: the expert choices per token are replayed
+ * from the inference engine, so the grouping is a function of those ids alone.
+ * Assignment a = t * top_k + k is token t's k-th expert, topk_ids[a].
+ *
+ * moe_route -- stable counting sort of the assignments by expert: offsets[E+1]
+ * (rows per expert, prefix sums), row_of[a] = the grouped row of assignment a,
+ * src_row[r] = the assignment of grouped row r.  Within an expert, rows follow a:
+ * the grouping depends on the ids alone.  Ids outside [0, num_experts) get
+ * row_of = -1, no grouped row, and FME_DEV_BAD_INDEX.
+ *   topk_ids   device int32 [tokens x top_k]
+ *   top_k      1 .. 64; num_experts 1 .. FME_MAX_GROUPS
+ *   offsets    device int32 [num_experts + 1]
+ *   row_of, src_row  device int32 [tokens x top_k]
+ *   workspace  device scratch, fme_route_workspace_bytes(tokens, top_k, num_experts)
+ *              bytes (16-byte aligned), contents irrelevant before and after
+ */
+fme_status moe_route(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int32_t num_experts, int32_t *offsets,
+                     int32_t *row_of, int32_t *src_row, void *workspace, int64_t workspace_bytes,
+                     int32_t *dev_status, void *stream);
+
+/*
+ * permute_quantize_nvfp4 -- quantize_nvfp4_pertoken of the grouped token rows
+ * X_g[r] = x[src_row[r] / top_k] without materialising X_g: codes, tiled scales
+ * (padded per expert with these offsets) and row scales of the tokens in grouped
+ * order, ready for grouped_gemm_fwd_nvfp4.  Gathered indices outside [0, tokens)
+ * are reported (FME_DEV_BAD_INDEX).
+ *   x          device bf16 [tokens x k]; k as quantize_nvfp4_pertoken
+ *   src_row, offsets  from moe_route; the grouped rows are tokens * top_k
+ */
+fme_status permute_quantize_nvfp4(const void *x, int64_t tokens, int64_t k, const int32_t *src_row, int32_t top_k,
+                                  const int32_t *offsets, int32_t num_experts, uint8_t *codes, uint8_t *sf,
+                                  float *row_scale, int32_t *dev_status, void *stream);
+
+/*
+ * permute_quantize_mxfp8 -- quantize_mxfp8 row-wise of the grouped token rows
+ * X_g[r] = x[src_row[r] / top_k]: MXFP8 codes [tokens*top_k x k] in grouped order
+ * and their tiled scales (each expert padded to 128 rows), the quantize-before-
+ * dispatch form of the grouped tokens.  Gathered indices outside [0, tokens) are
+ * reported (FME_DEV_BAD_INDEX).
+ *   x          device bf16 [tokens x k]; k a multiple of 32
+ *   src_row, offsets  from moe_route
+ */
+fme_status permute_quantize_mxfp8(const void *x, int64_t tokens, int64_t k, const int32_t *src_row, int32_t top_k,
+                                  const int32_t *offsets, int32_t num_experts, uint8_t *codes, uint8_t *sf,
+                                  int32_t *dev_status, void *stream);
+
+/*
+ * moe_combine -- out[t, :] = bf16( sum_k weights[t, k] * y[row_of[t, k], :] ), the
+ * sum over k in order in fp32, every product and every sum rounded to nearest
+ * even (no fused multiply-add); assignments with row_of < 0 contribute nothing.
+ *   y          device bf16 [rows_y x n], the grouped expert outputs
+ *   row_of     from moe_route; weights device float [tokens x top_k]
+ *   n          a multiple of 8
+ *   out        device bf16 [tokens x n]
+ */
+fme_status moe_combine(const void *y, int64_t rows_y, const int32_t *row_of, const float *weights, int64_t tokens,
+                       int32_t top_k, int64_t n, void *out, int32_t *dev_status, void *stream);
 
 /*
  * quantize_mxfp8 -- standard MXFP8 (OCP MX v1.0 rule) of the MoE backward.
@@ -289,6 +359,9 @@ int64_t fme_sf_bytes(int64_t rows, int64_t cols, int32_t block, int32_t num_grou
 
 /* Leading dimension (positions per column) of the column-wise MXFP8 outputs. */
 int64_t fme_colwise_ld(int64_t rows, int32_t num_groups);
+
+/* Bytes of moe_route's workspace (at least 16). */
+int64_t fme_route_workspace_bytes(int64_t tokens, int32_t top_k, int32_t num_experts);
 
 /* Bytes of the B-operand scale buffer written by quantize_nvfp4_weights (0 for
  * rows not a multiple of 256 or k not a multiple of 64). */

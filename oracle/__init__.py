@@ -82,9 +82,12 @@ def _declare(lib):
     lib.fme_orc_dequant_mxfp8.argtypes = [P, P, I64, I64, P]
     lib.fme_orc_gemm_abt.argtypes = [P, P, I64, I64, I64, P]
     lib.fme_orc_swiglu.argtypes = [P, I64, I64, P]
+    lib.fme_orc_route.argtypes = [P, I64, I32, P, P, P]
+    lib.fme_orc_combine.argtypes = [P, P, P, I64, I32, I64, P]
     for name in ("fme_orc_e2m1_encode_array", "fme_orc_e4m3_encode_array", "fme_orc_quant_nvfp4",
                  "fme_orc_dequant_nvfp4", "fme_orc_quant_mxfp8_rows", "fme_orc_quant_mxfp8_cols",
-                 "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt"):
+                 "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt", "fme_orc_swiglu", "fme_orc_route",
+                 "fme_orc_combine"):
         getattr(lib, name).restype = None
     return lib
 
@@ -203,6 +206,33 @@ class Oracle:
         h = np.empty((rows, inter), np.float64)
         self.lib.fme_orc_swiglu(_p(y), rows, inter, _p(h))
         return h
+
+    # routing -------------------------------------------------------------
+    def route(self, ids, num_experts: int):
+        """Stable grouping of assignments a (row-major over [tokens, top_k]) by
+        expert -> offsets [E+1], row_of (shape of ids), src_row [ids.size], int32."""
+        ids = np.ascontiguousarray(ids, np.int32)
+        n = ids.size
+        offsets = np.zeros(num_experts + 1, np.int32)
+        row_of = np.zeros(ids.shape, np.int32)
+        src_row = np.zeros(n, np.int32)
+        self.lib.fme_orc_route(_p(ids), n, num_experts, _p(offsets), _p(row_of), _p(src_row))
+        valid = int(offsets[-1])
+        return offsets, row_of, src_row[:valid] if valid < n else src_row
+
+    def combine(self, y_bits, row_of, weights):
+        """out [tokens, n] bf16 bits = fp32 in-order weighted sum of the rows of
+        y (bf16 bits) picked by row_of [tokens, top_k], rounded once to bf16."""
+        y = _bits(y_bits)
+        row_of = np.ascontiguousarray(row_of, np.int32)
+        w = np.ascontiguousarray(weights, np.float32)
+        tokens, top_k = row_of.shape
+        n = y.shape[1]
+        if np.any(row_of >= y.shape[0]):
+            raise ValueError("row_of points past y")
+        out = np.zeros((tokens, n), np.uint16)
+        self.lib.fme_orc_combine(_p(y), _p(row_of), _p(w), tokens, top_k, n, _p(out))
+        return out
 
     # GEMM ----------------------------------------------------------------
     def gemm_abt(self, a, b) -> np.ndarray:

@@ -29,6 +29,14 @@
  *     width).  The activation between the two projections is read as SwiGLU,
  *     h = silu(g) * u with silu(v) = v / (1 + e^-v), g and u the two halves of
  *     the gate/up output; the oracle evaluates it in fp64.
+ *   - "Cursor Composer 2 report deep dive", section 2, and the report's
+ *     section 6.1: tokens are quantized before dispatch to their experts and
+ *     the experts' outputs are combined per token in BF16; section 6.2: the
+ *     per-token expert choices are replayed.  The oracle groups assignment
+ *     a = t * top_k + k (token t's k-th expert) by expert keeping the order of
+ *     a (a stable counting sort), and combines out[t] = sum over k in order of
+ *     weight * y[row], each product and sum one fp32 operation, rounded once to
+ *     bf16 at the end.
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *   - per-token decode scale S_t = amax_t / (6 * 448), fp32, IEEE division;
@@ -370,6 +378,68 @@ void fme_orc_swiglu(const uint16_t *y_gu, int64_t rows, int64_t inter, double *h
             const double g = (double)bf16_value(row[j]);
             const double u = (double)bf16_value(row[inter + j]);
             h[t * inter + j] = g / (1.0 + exp(-g)) * u;
+        }
+    }
+}
+
+/* ------------------------------------------------------------- routing -- */
+
+/* Stable grouping of the n assignments by expert id: offsets[e] is the number of
+ * assignments to experts below e, and the assignments to expert e take grouped
+ * rows offsets[e], offsets[e] + 1, ... in increasing order of a.  row_of[a] is
+ * the grouped row of assignment a (-1 for an id outside [0, E)), src_row[r] the
+ * assignment at grouped row r. */
+void fme_orc_route(const int32_t *ids, int64_t n, int32_t num_experts, int32_t *offsets, int32_t *row_of,
+                   int32_t *src_row) {
+    for (int32_t e = 0; e <= num_experts; ++e)
+        offsets[e] = 0;
+    for (int64_t a = 0; a < n; ++a)
+        if (ids[a] >= 0 && ids[a] < num_experts)
+            offsets[ids[a] + 1] += 1;
+    for (int32_t e = 0; e < num_experts; ++e)
+        offsets[e + 1] += offsets[e];
+    for (int32_t e = 0; e < num_experts; ++e) {
+        int32_t next = offsets[e];
+        for (int64_t a = 0; a < n; ++a) {
+            if (ids[a] == e) {
+                row_of[a] = next;
+                src_row[next] = (int32_t)a;
+                next += 1;
+            }
+        }
+    }
+    for (int64_t a = 0; a < n; ++a)
+        if (ids[a] < 0 || ids[a] >= num_experts)
+            row_of[a] = -1;
+}
+
+/* binary32 -> bf16 bits, round to nearest even (finite inputs). */
+static uint16_t bf16_round(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint32_t lower = u & 0xFFFFu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1;
+    return (uint16_t)upper;
+}
+
+/* out[t, j] = bf16(acc), acc = 0 then acc = acc + w[t, k] * y[row_of[t, k], j]
+ * for k = 0 .. top_k-1 in order, each * and + one binary32 operation; entries
+ * with row_of < 0 are skipped. */
+void fme_orc_combine(const uint16_t *y, const int32_t *row_of, const float *w, int64_t tokens, int32_t top_k,
+                     int64_t n, uint16_t *out) {
+    for (int64_t t = 0; t < tokens; ++t) {
+        for (int64_t j = 0; j < n; ++j) {
+            float acc = 0.0f;
+            for (int32_t k = 0; k < top_k; ++k) {
+                const int32_t r = row_of[t * top_k + k];
+                if (r < 0)
+                    continue;
+                const float prod = w[t * top_k + k] * bf16_value(y[(int64_t)r * n + j]);
+                acc = acc + prod;
+            }
+            out[t * n + j] = bf16_round(acc);
         }
     }
 }

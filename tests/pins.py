@@ -426,4 +426,96 @@ def check_swiglu_vs_scipy(orc):
     assert np.allclose(h, want, rtol=4e-16, atol=1e-300)
 
 
+# --------------------------------------------------------------- routing ----
+def check_route_vs_stable_argsort(orc):
+    """Grouping = numpy's stable argsort of the ids (another sort algorithm);
+    offsets = the prefix sums of numpy's bincount; row_of inverts src_row."""
+    ids, _ = synth.topk_routing(tokens=3000, top_k=6, experts=40, seed=21)
+    offsets, row_of, src_row = orc.route(ids, 40)
+    flat = ids.ravel()
+    want_src = np.argsort(flat, kind="stable")
+    assert np.array_equal(src_row, want_src)
+    want_off = np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=40))])
+    assert np.array_equal(offsets, want_off)
+    assert np.array_equal(row_of.ravel()[src_row], np.arange(flat.size))
+    assert np.all(flat[src_row][:-1] <= flat[src_row][1:])
+
+
+def check_route_brute_force(orc):
+    """Every id pattern of 2 tokens x top-2 over 3 experts (81 cases): grouped
+    row r holds the r-th assignment in the order of the pairs (id, a), found by
+    Python's sorted."""
+    import itertools
+
+    for pat in itertools.product(range(3), repeat=4):
+        ids = np.array(pat, np.int32).reshape(2, 2)
+        offsets, row_of, src_row = orc.route(ids, 3)
+        want = [a for _, a in sorted((e, a) for a, e in enumerate(pat))]
+        assert list(src_row) == want, pat
+        assert list(offsets) == [0, pat.count(0), pat.count(0) + pat.count(1), 4]
+        for r, a in enumerate(want):
+            assert row_of.ravel()[a] == r
+
+
+def check_route_invalid_and_empty(orc):
+    """Ids outside [0, E) take no grouped row and get row_of = -1; experts with no
+    assignment have empty ranges; zero tokens give zero offsets."""
+    ids = np.array([[3, -1], [0, 7], [3, 0]], np.int32)
+    offsets, row_of, src_row = orc.route(ids, 5)
+    assert list(offsets) == [0, 2, 2, 2, 4, 4]
+    assert row_of.tolist() == [[2, -1], [0, -1], [3, 1]]
+    assert list(src_row[:4]) == [2, 5, 0, 4]
+    off0, _, _ = orc.route(np.zeros((0, 4), np.int32), 3)
+    assert list(off0) == [0, 0, 0, 0]
+
+
+def _combine(orc, y_vals, row_of, w):
+    y = synth.bf16_bits(np.asarray(y_vals, np.float32))
+    return synth.bf16_float(orc.combine(y, np.asarray(row_of, np.int32), np.asarray(w, np.float32)))
+
+
+def check_combine_closed_forms(orc):
+    """Hand-worked fp32 cases, one column each, rounded once to bf16 at the end:
+    one-hot weight returns the row; the sum is taken in fp32 (exact sum
+    1 + 2^-8 + 2^-30 rounds up in bf16, the fp32 running sum sits on the tie and
+    goes to even); in k order (1 - 1 + 2^-30 is 2^-30, 1 + 2^-30 - 1 is 0); each
+    product rounded before the add ((1 + 2^-23)(1 + 2^-7) loses its 2^-30);
+    skipped entries (row_of < 0); the bf16 rounding ties to even."""
+    t = 2.0 ** -30
+    cases = [
+        # (y rows [r x 1], row_of [1 x k], weights [1 x k], expected)
+        ([[5.0], [-3.25]], [[1, 0]], [[1.0, 0.0]], -3.25),
+        ([[1.0], [2.0 ** -8], [t]], [[0, 1, 2]], [[1.0, 1.0, 1.0]], 1.0),
+        ([[1.0], [-1.0], [t]], [[0, 1, 2]], [[1.0, 1.0, 1.0]], t),
+        ([[1.0], [t], [-1.0]], [[0, 1, 2]], [[1.0, 1.0, 1.0]], 0.0),
+        ([[-(1.0 + 2.0 ** -7)], [1.0 + 2.0 ** -7]], [[0, 1]], [[1.0, 1.0 + 2.0 ** -23]], 2.0 ** -23),
+        ([[2.0], [7.0]], [[-1, 1]], [[9.0, 0.5]], 3.5),
+        ([[1.0], [3.0 * 2.0 ** -8]], [[0, 1]], [[1.0, 1.0]], 1.0 + 2.0 ** -6),
+        ([[1.0], [2.0 ** -8]], [[0, 1]], [[1.0, 1.0]], 1.0),
+        ([[1.0 + 2.0 ** -7], [2.0 ** -8]], [[0, 1]], [[1.0, 1.0]], 1.0 + 2.0 ** -6),
+    ]
+    for y, ro, w, want in cases:
+        got = _combine(orc, y, ro, w)
+        assert got.shape == (1, 1) and got[0, 0] == np.float32(want), (y, ro, w, got, want)
+
+
+def check_combine_error_bound(orc):
+    """Random routed outputs: the result is within half a bf16 ulp of the fp32
+    sum, which is within top_k * 2^-24 * sum |w y| of the exact (fp64) sum."""
+    ids, w = synth.topk_routing(tokens=200, top_k=8, experts=16, seed=23)
+    offsets, row_of, _ = orc.route(ids, 16)
+    y = synth.normal_bits((int(offsets[-1]), 64), 1.0, seed=24)
+    out = synth.bf16_float(orc.combine(y, row_of, w)).astype(np.float64)
+    yv = synth.bf16_float(y).astype(np.float64)
+    gathered = yv[row_of]  # [tokens, top_k, n]
+    exact = np.einsum("tk,tkn->tn", w.astype(np.float64), gathered)
+    mag = np.einsum("tk,tkn->tn", np.abs(w.astype(np.float64)), np.abs(gathered))
+    fp32_err = 8 * 2.0 ** -24 * mag
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact) + fp32_err, 1e-30))) - 8)
+    assert np.all(np.abs(out - exact) <= half_ulp + fp32_err * 1.01 + 1e-30)
+    y_rows = yv[row_of[5, 3]]
+    single = synth.bf16_float(orc.combine(y, row_of[5:6, 3:4], np.ones((1, 1), np.float32)))
+    assert np.array_equal(single[0], y_rows.astype(np.float32))
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

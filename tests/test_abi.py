@@ -27,7 +27,8 @@ def test_header_declares_the_five_calls():
     for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_weights", "swiglu_quantize_nvfp4", "quantize_mxfp8",
                  "grouped_gemm_fwd_nvfp4",
                  "grouped_gemm_fwd_mxfp8",
-                 "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8"):
+                 "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8", "moe_route", "permute_quantize_nvfp4",
+                 "permute_quantize_mxfp8", "moe_combine"):
         assert call in names
 
 
@@ -50,7 +51,14 @@ def test_helpers_closed_forms(lib):
     assert fme.sf_bytes_nvfp4_weights(100, 256) == 0
     assert fme.colwise_ld(65536, 32) == ((65536 + 127 * 32) // 128) * 128
     assert lib.fme_version().startswith(b"fme")
-    for code in range(8):
+    # route workspace: ceil(tokens * top_k / 1024) chunks x E counters, at least 16 bytes
+    assert fme.route_workspace_bytes(32768, 8, 32) == 256 * 32 * 4
+    assert fme.route_workspace_bytes(1, 1, 1) == 16
+    assert fme.route_workspace_bytes(1025, 1, 3) == 24
+    assert fme.route_workspace_bytes(1024, 1, 3) == 16
+    assert fme.route_workspace_bytes(0, 8, 32) == 16
+    assert fme.route_workspace_bytes(-1, 8, 32) == 0
+    for code in range(9):
         assert lib.fme_error_string(code)
 
 
@@ -112,6 +120,34 @@ def test_host_argument_checks(lib):
     assert w(good, good, 128, good, good, 128, good, 4, 100, 256, good, None, _stream()) == 3
     assert w(good, good, 128, good, good, 128, good, 4, 128, 256, good, None, _stream()) == 3  # m % 256
     assert w(good, good, 128, good, good, 128, None, 4, 256, 256, good, None, _stream()) == 1
+    r = lib.moe_route
+    ws = 1 << 20
+    assert r(good, 10, 8, 0, good, good, good, good, ws, None, _stream()) == 1       # no experts
+    assert r(good, 10, 8, 1025, good, good, good, good, ws, None, _stream()) == 1    # too many
+    assert r(good, 10, 65, 32, good, good, good, good, ws, None, _stream()) == 1     # top_k
+    assert r(good, -1, 8, 32, good, good, good, good, ws, None, _stream()) == 1
+    assert r(good, 1 << 29, 8, 32, good, good, good, good, ws, None, _stream()) == 3  # > 2^31 - 1 rows
+    assert r(good, 10, 8, 32, good, good, good, good, 8, None, _stream()) == 1       # workspace too small
+    assert r(None, 10, 8, 32, good, good, good, good, ws, None, _stream()) == 1
+    assert r(good, 10, 8, 32, good, odd, good, good, ws, None, _stream()) == 2
+    pn = lib.permute_quantize_nvfp4
+    assert pn(good, 10, 96, good, 8, good, 32, good, good, good, None, _stream()) == 3    # k % 64
+    assert pn(good, 10, 256, good, 0, good, 32, good, good, good, None, _stream()) == 1   # top_k
+    assert pn(good, 10, 256, good, 8, None, 32, good, good, good, None, _stream()) == 1   # offsets
+    assert pn(good, 10, 256, None, 8, good, 32, good, good, good, None, _stream()) == 1   # src_row
+    assert pn(good, 10, 256, odd, 8, good, 32, good, good, good, None, _stream()) == 2
+    assert pn(good, 0, 256, None, 8, good, 32, None, None, None, None, _stream()) == 0    # no rows
+    pm = lib.permute_quantize_mxfp8
+    assert pm(good, 10, 48, good, 8, good, 32, good, good, None, _stream()) == 3          # k % 32
+    assert pm(good, 10, 256, good, 8, good, 0, good, good, None, _stream()) == 1
+    assert pm(good, 10, 256, good, 8, good, 32, good, odd, None, _stream()) == 2
+    assert pm(good, 0, 256, None, 8, good, 32, None, None, None, _stream()) == 0
+    c = lib.moe_combine
+    assert c(good, 80, good, good, 10, 8, 100, good, None, _stream()) == 3               # n % 8
+    assert c(good, 80, good, good, 10, 0, 256, good, None, _stream()) == 1               # top_k
+    assert c(good, 80, None, good, 10, 8, 256, good, None, _stream()) == 1
+    assert c(good, 80, good, good, 10, 8, 256, odd, None, _stream()) == 2
+    assert c(None, 0, None, None, 0, 8, 256, None, None, _stream()) == 0                  # no tokens
     assert lib.fme_read_device_status(None, _stream(), None) == 1
 
 

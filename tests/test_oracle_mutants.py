@@ -49,6 +49,17 @@ MUTANTS = {
     "swiglu_gate_up_halves_swapped": ("const double g = (double)bf16_value(row[j]);\n            const double u = (double)bf16_value(row[inter + j]);",
                                       "const double u = (double)bf16_value(row[j]);\n            const double g = (double)bf16_value(row[inter + j]);"),
     "swiglu_drops_up": ("h[t * inter + j] = g / (1.0 + exp(-g)) * u;", "h[t * inter + j] = g / (1.0 + exp(-g));"),
+    "route_unstable": ("        for (int64_t a = 0; a < n; ++a) {\n            if (ids[a] == e) {",
+                       "        for (int64_t a = n - 1; a >= 0; --a) {\n            if (ids[a] == e) {"),
+    "route_offsets_not_summed": ("offsets[e + 1] += offsets[e];", "offsets[e + 1] += 0;"),
+    "route_invalid_kept_as_last": ("            row_of[a] = -1;", "            row_of[a] = n - 1;"),
+    "combine_fp64_sum": ("            float acc = 0.0f;\n", "            double acc = 0.0;\n"),
+    "combine_reversed_k": ("for (int32_t k = 0; k < top_k; ++k) {\n                const int32_t r",
+                           "for (int32_t k = top_k - 1; k >= 0; --k) {\n                const int32_t r"),
+    "combine_fused_multiply_add": ("                acc = acc + prod;",
+                                   "                acc = fmaf(w[t * top_k + k], bf16_value(y[(int64_t)r * n + j]), acc);"),
+    "combine_ties_away": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (lower >= 0x8000u)"),
+    "combine_truncates": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (0)"),
     "gemm_transposed_operand": ("acc += a[i * k + q] * b[j * k + q];", "acc += a[i * k + q] * b[q * n + j];"),
     "gemm_drops_last_term": ("for (int64_t q = 0; q < k; ++q)\n                acc +=",
                              "for (int64_t q = 0; q < k - 1; ++q)\n                acc +="),
