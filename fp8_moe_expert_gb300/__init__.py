@@ -73,6 +73,7 @@ SYMBOLS = {
     "grouped_gemm_wgrad_mxfp8": ("i32", ["p", "p", "i64", "p", "p", "i64", "p", "i32", "i64", "i64", "p", "p",
                                          "p"]),
     "moe_route": ("i32", ["p", "i64", "i32", "i32", "p", "p", "p", "p", "i64", "p", "p"]),
+    "moe_route_noalloc": ("i32", ["p", "i64", "i32", "i32", "p", "p", "p", "p", "p"]),
     "permute_quantize_nvfp4": ("i32", ["p", "i64", "i64", "p", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
     "permute_quantize_mxfp8": ("i32", ["p", "i64", "i64", "p", "i32", "p", "i32", "p", "p", "p", "p"]),
     "moe_combine": ("i32", ["p", "i64", "p", "p", "i64", "i32", "i64", "p", "p", "p"]),
@@ -356,6 +357,16 @@ def moe_route(topk_ids, num_experts, *, offsets=None, row_of=None, src_row=None,
                          _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
                          _stream(stream))
     _check(st, "moe_route")
+    return offsets, row_of, src_row
+
+
+def moe_route_noalloc(topk_ids, num_experts, offsets, row_of, src_row, *, status=None, stream=None):
+    """moe_route into caller-owned outputs, with the library's static counters as
+    the workspace: neither this call nor the library allocates memory."""
+    tokens, top_k = topk_ids.shape
+    st = lib().moe_route_noalloc(_ptr(topk_ids), tokens, top_k, num_experts, _ptr(offsets), _ptr(row_of),
+                                 _ptr(src_row), _ptr(status), _stream(stream))
+    _check(st, "moe_route_noalloc")
     return offsets, row_of, src_row
 
 

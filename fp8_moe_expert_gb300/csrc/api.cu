@@ -275,6 +275,26 @@ fme_status moe_route(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "moe_route launch");
 }
 
+fme_status moe_route_noalloc(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int32_t num_experts,
+                             int32_t *offsets, int32_t *row_of, int32_t *src_row, int32_t *dev_status,
+                             void *stream) {
+  if (tokens < 0 || top_k < 1 || top_k > 64 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (tokens * top_k > (int64_t(1) << 31) - 1) return FME_ERR_UNSUPPORTED_SHAPE;
+  const int64_t chunks = (tokens * top_k + fme::kRouteChunkHost - 1) / fme::kRouteChunkHost;
+  if (chunks * num_experts > fme::kRouteStaticWords) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets) return FME_ERR_INVALID_ARGUMENT;
+  if (tokens > 0 && (!topk_ids || !row_of || !src_row)) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(topk_ids) || !aligned16(offsets) || !aligned16(row_of) || !aligned16(src_row))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchRoute r{topk_ids, tokens, top_k, num_experts, offsets, row_of, src_row, nullptr, dev_status,
+                     static_cast<cudaStream_t>(stream)};
+  cudaError_t err = fme::launch_route_static(r);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "moe_route_noalloc launch");
+}
+
 fme_status permute_quantize_nvfp4(const void *x, int64_t tokens, int64_t k, const int32_t *src_row, int32_t top_k,
                                   const int32_t *offsets, int32_t num_experts, uint8_t *codes, uint8_t *sf,
                                   float *row_scale, int32_t *dev_status, void *stream) {

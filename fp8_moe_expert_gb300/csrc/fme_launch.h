@@ -91,6 +91,10 @@ cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf);
 cudaError_t launch_grouped_gemm(const LaunchGemm &a);
 cudaError_t launch_route(const LaunchRoute &r);
+// launch_route with the module's static device counters as the workspace (r.ws
+// is ignored); needs chunks * num_experts <= kRouteStaticWords.
+constexpr int64_t kRouteStaticWords = int64_t(1) << 20;
+cudaError_t launch_route_static(LaunchRoute r);
 cudaError_t launch_combine(const LaunchCombine &c);
 constexpr int64_t kRouteChunkHost = 1024;  // assignments per routing chunk (route.cu)
 

@@ -150,6 +150,19 @@ __global__ void __launch_bounds__(kRouteChunk) route_scatter_kernel(const int32_
   if (a < n && e < 0) row_of[a] = -1;
 }
 
+// Per-(chunk, expert) counters for routing calls that bring no workspace: 4 MB
+// of device memory that exists for the module's lifetime, so such a call makes
+// no allocation.  Calls that use it must be ordered (one stream, or events).
+__device__ int32_t g_route_counters[kRouteStaticWords];
+
+cudaError_t launch_route_static(LaunchRoute r) {
+  void *p = nullptr;
+  cudaError_t err = cudaGetSymbolAddress(&p, g_route_counters);
+  if (err != cudaSuccess) return err;
+  r.ws = static_cast<int32_t *>(p);
+  return launch_route(r);
+}
+
 cudaError_t launch_route(const LaunchRoute &r) {
   const int64_t n = r.tokens * r.top_k;
   const int64_t chunks = (n + kRouteChunk - 1) / kRouteChunk;

@@ -193,6 +193,20 @@ fme_status moe_route(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int
                      int32_t *dev_status, void *stream);
 
 /*
+ * moe_route_noalloc -- moe_route without a workspace argument and without any
+ * allocation: the per-(chunk, expert) counters live in a static device array of
+ * FME_ROUTE_STATIC_WORDS int32 inside the library, so
+ * ceil(tokens * top_k / 1024) * num_experts must not exceed it
+ * (FME_ERR_UNSUPPORTED_SHAPE otherwise).  Same outputs, bit for bit, as
+ * moe_route.  Calls share that array: they must be ordered on the device (one
+ * stream, or streams joined by events), never concurrent.
+ */
+#define FME_ROUTE_STATIC_WORDS (1 << 20)
+fme_status moe_route_noalloc(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int32_t num_experts,
+                             int32_t *offsets, int32_t *row_of, int32_t *src_row, int32_t *dev_status,
+                             void *stream);
+
+/*
  * permute_quantize_nvfp4 -- quantize_nvfp4_pertoken of the grouped token rows
  * X_g[r] = x[src_row[r] / top_k] without materialising X_g: codes, tiled scales
  * (padded per expert with these offsets) and row scales of the tokens in grouped
