@@ -409,6 +409,48 @@ def run_extras(step, args, bf16_sus):
         out[name] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac_fp8": round(ach / (bf16_sus * 2), 3)}
     del xq, wq, hq, wdq
     out.update(run_routing_extras(step, args, hbm))
+    out.update(run_gate_up_bwd_extras(step, args, hbm, bf16_sus))
+    return out
+
+
+def run_gate_up_bwd_extras(step, args, hbm, bf16_sus):
+    """The gate/up half of the backward on the same rows: the fused SwiGLU backward
+    + MXFP8 row/column quantization of d(gate/up) [R x 2I] from the forward's
+    gate/up output and dh, the column-wise quantization of X and of W_gu, and the
+    gate/up dgrad (contraction over 2I = 4096) and wgrad (dW_gu [E x 2I x H])."""
+    import torch
+
+    f, off, st = step.fme, step.offsets, step.status
+    R, H, I, E = step.R, step.H, step.I, step.E
+    out = {}
+    sb = f.swiglu_backward_quantize_mxfp8(step.y_gu, step.dh, off, status=st)
+    rc, rs, cc, cs, poff, ld = sb[:6]
+    sb_bytes = R * (2 * 2 * I + 2 * I + 2 * I + 2 * I + 2 * (2 * I // 32))
+    ms = _time_call(lambda: f.swiglu_backward_quantize_mxfp8(step.y_gu, step.dh, off, row_codes=rc, row_sf=rs,
+                                                             col_codes=cc, col_sf=cs, padded_offsets=poff,
+                                                             status=st), args.steps)
+    gbs = sb_bytes / (ms * 1e-3) / 1e9
+    out["swiglu_backward_quantize_mxfp8"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                             "frac_hbm": round(gbs / hbm, 3)}
+    xc = f.quantize_mxfp8(step.x, f.COLWISE, off, codes=step.dyc[0], sf=step.dyc[1], padded_offsets=step.dyc[2],
+                          status=st)
+    ld_w = f.colwise_ld(E * 2 * I, 1)
+    wc = f.quantize_mxfp8(step.w_gu, f.COLWISE, status=st)
+    dx = torch.empty((R, H), dtype=torch.bfloat16, device=step.dev)
+    dw = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=step.dev)
+    flops = 2 * R * 2 * I * H
+    for name, fn in (
+            ("gemm_dgrad_gate_up",
+             lambda: f.grouped_gemm_dgrad_mxfp8(rc, rs, wc[0], wc[1], ld_w, off, H, 2 * I, y=dx, status=st)),
+            ("gemm_wgrad_gate_up",
+             lambda: f.grouped_gemm_wgrad_mxfp8(cc, cs, ld, xc[0], xc[1], xc[3], poff, 2 * I, H, y=dw, status=st))):
+        ms = _time_call(fn, args.steps)
+        ach = flops / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac_fp8": round(ach / (bf16_sus * 2), 3)}
+    code, raw = f.read_device_status(st)
+    if code != 0:
+        raise RuntimeError(f"gate/up backward extras: device status {code} ({raw:#x})")
+    del sb, rc, rs, cc, cs, xc, wc, dx, dw
     return out
 
 
@@ -487,8 +529,9 @@ def run_e2e(step, calls, args, world):
     and outputs, copies in on one stream, the 11 calls on another, copies out on a
     third, ordered by events (step i's uploads overlap step i-1's calls and
     downloads).  The 19.3 GB of copies per step, not the kernels, set the pace:
-    splitting each direction over two streams measured the same.  The clock covers all three streams from the first upload to the
-    last download."""
+    splitting each direction over two streams measured the same.  At least 3
+    (and at least `args.warmup`) pipelined warm-up steps run first; the clock
+    covers all three streams from the first timed upload to the last download."""
     import torch
 
     sets = [{n: getattr(step, n) for n in INPUT_NAMES + OUTPUT_NAMES}]
@@ -530,8 +573,9 @@ def run_e2e(step, calls, args, world):
         started[k] = True
 
     steps = max(2, min(args.steps, 8))
-    one(0)
-    one(1)
+    warm = max(3, args.warmup)
+    for i in range(warm):
+        one(i)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -540,7 +584,7 @@ def run_e2e(step, calls, args, world):
     start.record(cur)
     for s_ in (s_in, s_run, s_out):
         s_.wait_event(start)
-    for i in range(2, 2 + steps):
+    for i in range(warm, warm + steps):
         one(i)
     for s_ in (s_in, s_run, s_out):
         cur.wait_stream(s_)

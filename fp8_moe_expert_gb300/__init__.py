@@ -65,6 +65,8 @@ SYMBOLS = {
     "swiglu_quantize_nvfp4": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8": ("i32", ["p", "i64", "i64", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8_rowcol": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p", "p"]),
+    "swiglu_backward_quantize_mxfp8": ("i32", ["p", "p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p",
+                                               "p", "p"]),
     "grouped_gemm_fwd_nvfp4": ("i32", ["p", "p", "p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p",
                                        "p"]),
     "grouped_gemm_fwd_mxfp8": ("i32", ["p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p", "p"]),
@@ -275,6 +277,38 @@ def quantize_mxfp8_rowcol(x, offsets=None, num_groups=None, *, row_codes=None, r
                                      _stream(stream))
     _check(st, "quantize_mxfp8_rowcol")
     return (row_codes, row_sf), (col_codes, col_sf, padded_offsets, ld)
+
+
+def swiglu_backward_quantize_mxfp8(gate_up, dh, offsets=None, num_groups=None, *, row_codes=None, row_sf=None,
+                                   col_codes=None, col_sf=None, padded_offsets=None, d_gate_up=None,
+                                   want_d=False, status=None, stream=None):
+    """d(gate/up) of h = silu(g) * u given dh, quantized to MXFP8 row-wise and
+    column-wise -> (row_codes, row_sf, col_codes, col_sf, padded_offsets, ld,
+    d_gate_up or None)."""
+    import torch
+
+    rows, two_inter = gate_up.shape
+    inter = two_inter // 2
+    offsets, g = _groups(offsets, num_groups)
+    dev = gate_up.device
+    ld = colwise_ld(rows, g)
+    if row_codes is None:
+        row_codes = _empty((rows, two_inter), torch.uint8, dev)
+    if row_sf is None:
+        row_sf = _empty((max(sf_bytes(rows, two_inter, 32, g), 16),), torch.uint8, dev)
+    if col_codes is None:
+        col_codes = _empty((two_inter, ld), torch.uint8, dev)
+    if col_sf is None:
+        col_sf = _empty((max(sf_bytes(two_inter, ld, 32, 1), 16),), torch.uint8, dev)
+    if padded_offsets is None:
+        padded_offsets = _empty((g + 1,), torch.int32, dev)
+    if d_gate_up is None and want_d:
+        d_gate_up = _empty((rows, two_inter), torch.bfloat16, dev)
+    st = lib().swiglu_backward_quantize_mxfp8(_ptr(gate_up), _ptr(dh), rows, inter, _ptr(offsets), g,
+                                              _ptr(row_codes), _ptr(row_sf), _ptr(col_codes), _ptr(col_sf),
+                                              _ptr(padded_offsets), _ptr(d_gate_up), _ptr(status), _stream(stream))
+    _check(st, "swiglu_backward_quantize_mxfp8")
+    return row_codes, row_sf, col_codes, col_sf, padded_offsets, ld, d_gate_up
 
 
 def grouped_gemm_fwd_nvfp4(a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offsets, n, k, *, y=None,

@@ -409,6 +409,31 @@ fme_status quantize_mxfp8_rowcol(const void *x, int64_t rows, int64_t cols, cons
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_mxfp8_rowcol launch");
 }
 
+fme_status swiglu_backward_quantize_mxfp8(const void *gate_up, const void *dh, int64_t rows, int64_t inter,
+                                          const int32_t *offsets, int32_t num_groups, uint8_t *row_codes,
+                                          uint8_t *row_sf, uint8_t *col_codes, uint8_t *col_sf,
+                                          int32_t *padded_offsets, void *d_gate_up, int32_t *dev_status,
+                                          void *stream) {
+  if (rows < 0 || check_groups(num_groups) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (offsets == nullptr && num_groups != 1) return FME_ERR_INVALID_ARGUMENT;
+  if (rows > (int64_t(1) << 31) - 1 - 128 * static_cast<int64_t>(num_groups)) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (inter % 128 != 0 || inter < 128 || inter > 32768) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!padded_offsets || !col_codes || !col_sf || !row_sf || (rows > 0 && (!gate_up || !dh || !row_codes)))
+    return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(gate_up) || !aligned16(dh) || !aligned16(row_codes) || !aligned16(row_sf) ||
+      !aligned16(col_codes) || !aligned16(col_sf) || !aligned16(padded_offsets) || !aligned16(d_gate_up))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchMxfp8 a{gate_up, rows, 2 * inter, offsets, num_groups, col_codes, col_sf, padded_offsets,
+                     fme_colwise_ld(rows, num_groups), dev_status, sms, static_cast<cudaStream_t>(stream)};
+  a.dh = dh;
+  a.d_out = d_gate_up;
+  cudaError_t err = fme::launch_swiglu_bwd_mxfp8(a, row_codes, row_sf);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "swiglu_backward_quantize_mxfp8 launch");
+}
+
 fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
                                   const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
                                   const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n, int64_t k,

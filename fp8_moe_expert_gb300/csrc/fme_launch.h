@@ -65,6 +65,10 @@ struct LaunchMxfp8 {
   const int32_t *gather = nullptr;
   int32_t gather_div = 1;
   int64_t gather_limit = 0;
+  // SwiGLU backward (launch_swiglu_bwd_mxfp8): x = gate/up [rows x cols], dh
+  // [rows x cols/2], optional bf16 d(gate/up) out [rows x cols].
+  const void *dh = nullptr;
+  void *d_out = nullptr;
 };
 
 enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2, kFwdMxfp8 = 3 };
@@ -89,6 +93,9 @@ cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a);
 cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf);
+// Fused SwiGLU backward + row-wise and column-wise MXFP8 of d(gate/up); a.codes /
+// a.sf are the column-wise outputs (as launch_quantize_mxfp8_rowcol).
+cudaError_t launch_swiglu_bwd_mxfp8(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf);
 cudaError_t launch_grouped_gemm(const LaunchGemm &a);
 cudaError_t launch_route(const LaunchRoute &r);
 // launch_route with the module's static device counters as the workspace (r.ws

@@ -8,6 +8,13 @@
 // bits; x / X is then one exact fp32 multiply by 2^(127 - code), so the fast
 // division the pages allow for MXFP8 and a correctly rounded one give the same
 // codes.  Elements convert with cvt.rn.satfinite (nearest even, saturating at 448).
+//
+// The SwiGLU backward of the gate/up projection (h = silu(g) * u, the activation
+// between the two expert projections) is fused with the row-wise and column-wise
+// quantization of its result d(gate_up) = [dg | du], the A operands of the gate/up
+// data and weight gradients: dg = dh * u * sigma(g) * (1 + g * sigma(-g)),
+// du = dh * g * sigma(g), each evaluated in fp32 and rounded to bf16 before it is
+// quantized exactly as a bf16 input would be.
 #include "fme_device.cuh"
 #include "fme_launch.h"
 
@@ -16,6 +23,46 @@ namespace fme {
 __device__ __forceinline__ uint32_t mx_code_from_bf16_amax(uint32_t amax_bits) {
   const int e = static_cast<int>((amax_bits >> 7) & 0xFF);
   return static_cast<uint32_t>(e > 8 ? e - 8 : 0);
+}
+
+__device__ __forceinline__ float rcp_fast(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// (dg, du) of one element: gate g, up u, upstream gradient dh.  sigma(g) and
+// sigma(-g) come from t = e^(-|g|) as (1 or t) / (1 + t), so neither is formed as
+// 1 - sigma (no cancellation for large |g|) and e^(-|g|) never overflows.
+__device__ __forceinline__ void swiglu_bwd_one(float g, float u, float dh, float &dg, float &du) {
+  const float s = __expf(-0.5f * fabsf(g));
+  const float t = s * s;
+  const float r = rcp_fast(1.0f + t);
+  const float sig = (g >= 0.0f ? 1.0f : t) * r;
+  const float sig_neg = (g >= 0.0f ? t : 1.0f) * r;
+  du = dh * (g * sig);
+  dg = (dh * u) * (sig * (1.0f + g * sig_neg));
+}
+
+// Eight elements (one 16-byte word of g, u and dh each) -> the bf16 words of dg
+// and du (nearest even).
+__device__ __forceinline__ void swiglu_bwd_uint4(const uint4 &g, const uint4 &u, const uint4 &dh, uint4 &dg,
+                                                 uint4 &du) {
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w}, hw[4] = {dh.x, dh.y, dh.z, dh.w};
+  uint32_t ow_g[4], ow_u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float g0, u0, g1, u1;
+    swiglu_bwd_one(__uint_as_float(gw[i] << 16), __uint_as_float(uw[i] << 16), __uint_as_float(hw[i] << 16), g0, u0);
+    swiglu_bwd_one(__uint_as_float(gw[i] & 0xFFFF0000u), __uint_as_float(uw[i] & 0xFFFF0000u),
+                   __uint_as_float(hw[i] & 0xFFFF0000u), g1, u1);
+    const __nv_bfloat162 bg = __floats2bfloat162_rn(g0, g1);
+    const __nv_bfloat162 bu = __floats2bfloat162_rn(u0, u1);
+    ow_g[i] = *reinterpret_cast<const uint32_t *>(&bg);
+    ow_u[i] = *reinterpret_cast<const uint32_t *>(&bu);
+  }
+  dg = make_uint4(ow_g[0], ow_g[1], ow_g[2], ow_g[3]);
+  du = make_uint4(ow_u[0], ow_u[1], ow_u[2], ow_u[3]);
 }
 
 // 2^(127 - code) as an fp32 (code in [0, 246] for bf16 inputs: always normal).
@@ -151,17 +198,28 @@ __device__ __forceinline__ void col_tile_locate(ColTile &t, const GroupTable &gr
   t.src0 = groups.off[t.g] + local0;
 }
 
-// kRows: also quantize the same tile row-wise (blocks of 32 along each row), so a
-// tensor needed both ways is read once.  The tile's 128 padded positions are the
-// row-wise scale layout's 128-row block j (both pad each group to 128 rows), so
-// its row-wise scales are one 512-byte tile too.
-template <bool kRows>
+// kMode kColsOnly: column-wise only.  kRowCol: also quantize the same tile
+// row-wise (blocks of 32 along each row), so a tensor needed both ways is read
+// once.  The tile's 128 padded positions are the row-wise scale layout's 128-row
+// block j (both pad each group to 128 rows), so its row-wise scales are one
+// 512-byte tile too.  kSwiGLUBwd: row-wise and column-wise, the tile produced from
+// gate/up rows x = [g | u] (cols = 2 * inter) and dh [rows x inter]: tile column
+// block jb covers gate columns 64 jb .. 64 jb + 63 (tile columns 0..63, dg) and
+// the same up columns (tile columns 64..127, du), so g and dh are read once; the
+// tile's halves land in different 128-column blocks of the outputs.
+enum ColMode { kColsOnly = 0, kRowCol = 1, kSwiGLUBwd = 2 };
+
+template <int kMode>
 __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
                                                          const int32_t *__restrict__ offsets, int num_groups,
                                                          uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
                                                          int64_t ld, int32_t *__restrict__ padded_offsets,
                                                          uint8_t *__restrict__ row_codes, uint8_t *__restrict__ row_sf,
-                                                         int32_t *status) {
+                                                         int32_t *status, const uint16_t *__restrict__ dh,
+                                                         uint16_t *__restrict__ d_out) {
+  constexpr bool kRows = kMode != kColsOnly;
+  constexpr bool kSw = kMode == kSwiGLUBwd;
+  constexpr int kPre = kSw ? 12 : 8;  // 16-byte words of the next tile held per thread
   __shared__ GroupTable groups;
   __shared__ int ok_flag;
   extern __shared__ __align__(16) uint8_t col_smem[];
@@ -183,7 +241,8 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
     if (blockIdx.x == 0 && tid == 0) report(status, kDevBadOffsets);
     return;
   }
-  const int cblocks = cols / 128;
+  const int inter = cols / 2;  // kSwiGLUBwd only
+  const int cblocks = kSw ? inter / 64 : cols / 128;
   const int64_t total = chunks * cblocks;
   const int64_t dj = gridDim.x / cblocks;
   const int dcb = gridDim.x % cblocks;
@@ -196,18 +255,34 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
     }
   };
 
-  auto load_tile = [&](const ColTile &t, uint4 (&dst)[8]) {
+  auto load_tile = [&](const ColTile &t, uint4 (&dst)[kPre]) {
+    if constexpr (kSw) {
+      // thread = (row pass * 32 + tid / 8, 8 consecutive gate columns): g, u, dh
 #pragma unroll
-    for (int pass = 0; pass < 8; ++pass) {
-      const int r = pass * 16 + (tid >> 4);
-      const int seg = tid & 15;
-      dst[pass] = (r < t.valid)
-                      ? __ldcs(reinterpret_cast<const uint4 *>(x + (t.src0 + r) * cols + t.cb * 128 + seg * 8))
-                      : make_uint4(0, 0, 0, 0);
+      for (int pass = 0; pass < 4; ++pass) {
+        const int r = pass * 32 + (tid >> 3);
+        const int c = t.cb * 64 + (tid & 7) * 8;
+        const bool in = r < t.valid;
+        const int64_t row = t.src0 + r;
+        dst[3 * pass] = in ? __ldcs(reinterpret_cast<const uint4 *>(x + row * cols + c)) : make_uint4(0, 0, 0, 0);
+        dst[3 * pass + 1] =
+            in ? __ldcs(reinterpret_cast<const uint4 *>(x + row * cols + inter + c)) : make_uint4(0, 0, 0, 0);
+        dst[3 * pass + 2] =
+            in ? __ldcs(reinterpret_cast<const uint4 *>(dh + row * inter + c)) : make_uint4(0, 0, 0, 0);
+      }
+    } else {
+#pragma unroll
+      for (int pass = 0; pass < 8; ++pass) {
+        const int r = pass * 16 + (tid >> 4);
+        const int seg = tid & 15;
+        dst[pass] = (r < t.valid)
+                        ? __ldcs(reinterpret_cast<const uint4 *>(x + (t.src0 + r) * cols + t.cb * 128 + seg * 8))
+                        : make_uint4(0, 0, 0, 0);
+      }
     }
   };
   ColTile cur{static_cast<int64_t>(blockIdx.x) / cblocks, static_cast<int>(blockIdx.x % cblocks), 0, 0, 0};
-  uint4 pre[8];
+  uint4 pre[kPre];
   if (cur.j < chunks) {
     col_tile_locate(cur, groups, num_groups);
     load_tile(cur, pre);
@@ -219,9 +294,21 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
     const int64_t j = cur.j;
     const int cb = cur.cb;
     __syncthreads();  // the previous tile's shared buffers are free
+    if constexpr (kSw) {
 #pragma unroll
-    for (int pass = 0; pass < 8; ++pass)
-      *reinterpret_cast<uint4 *>(&tile[pass * 16 + (tid >> 4)][(tid & 15) * 8]) = pre[pass];
+      for (int pass = 0; pass < 4; ++pass) {
+        const int r = pass * 32 + (tid >> 3);
+        const int c = (tid & 7) * 8;
+        uint4 dg = make_uint4(0, 0, 0, 0), du = make_uint4(0, 0, 0, 0);
+        if (r < cur.valid) swiglu_bwd_uint4(pre[3 * pass], pre[3 * pass + 1], pre[3 * pass + 2], dg, du);
+        *reinterpret_cast<uint4 *>(&tile[r][c]) = dg;
+        *reinterpret_cast<uint4 *>(&tile[r][64 + c]) = du;
+      }
+    } else {
+#pragma unroll
+      for (int pass = 0; pass < 8; ++pass)
+        *reinterpret_cast<uint4 *>(&tile[pass * 16 + (tid >> 4)][(tid & 15) * 8]) = pre[pass];
+    }
     __syncthreads();
     if (nxt.j < chunks) {
       col_tile_locate(nxt, groups, num_groups);
@@ -288,7 +375,8 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
 #pragma unroll
         for (int q = 0; q < 8; ++q) words[q] = e4m3x4_words(w[2 * q], w[2 * q + 1], s);
         if (r < cur.valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(row_codes + (cur.src0 + r) * cols + cb * 128 + 32 * b);
+          const int col = kSw ? (b < 2 ? cb * 64 + 32 * b : inter + cb * 64 + 32 * (b - 2)) : cb * 128 + 32 * b;
+          uint4 *dst = reinterpret_cast<uint4 *>(row_codes + (cur.src0 + r) * cols + col);
           dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
           dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
         }
@@ -302,14 +390,48 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
       const int ch = pass * 32 + (tid >> 3);
       const int seg = tid & 7;
       const uint4 v = *reinterpret_cast<const uint4 *>(&outq[ch][seg * 16]);
-      *reinterpret_cast<uint4 *>(codes_t + (static_cast<int64_t>(cb) * 128 + ch) * ld + j * 128 + seg * 16) = v;
+      const int64_t gch = kSw ? (ch < 64 ? cb * 64 + ch : inter + cb * 64 + ch - 64) : static_cast<int64_t>(cb) * 128 + ch;
+      *reinterpret_cast<uint4 *>(codes_t + gch * ld + j * 128 + seg * 16) = v;
     }
-    if (tid < 32) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
-      *reinterpret_cast<uint4 *>(sf_t + (static_cast<int64_t>(cb) * (ld / 128) + j) * 512 + tid * 16) = v;
-    } else if (kRows && tid < 64) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[(tid - 32) * 16]);
-      *reinterpret_cast<uint4 *>(row_sf + (j * cblocks + cb) * 512 + (tid - 32) * 16) = v;
+    if constexpr (kSw) {
+      // the gate and up halves are each half of a 512-byte scale tile: tile rows
+      // (channels) 0..63 or 64..127 by the parity of cb (inter is a multiple of 128)
+      const int odd = cb & 1;
+      const int64_t t_g = cb / 2, t_u = (inter / 64 + cb) / 2;
+      if (tid < 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
+        *reinterpret_cast<uint2 *>(sf_t + (t_g * (ld / 128) + j) * 512 + tid * 16 + 8 * odd) = make_uint2(v.x, v.y);
+        *reinterpret_cast<uint2 *>(sf_t + (t_u * (ld / 128) + j) * 512 + tid * 16 + 8 * odd) = make_uint2(v.z, v.w);
+      }
+      {
+        // row-wise scales: row r's 4-byte cell holds blocks (g0, g1, u0, u1)
+        const int r = tid >> 1;
+        const int half = tid & 1;
+        const int cell = (r & 31) * 16 + (r >> 5) * 4;
+        const uint16_t v = *reinterpret_cast<const uint16_t *>(&sfr[cell + 2 * half]);
+        const int64_t tcol = half ? t_u : t_g;
+        *reinterpret_cast<uint16_t *>(row_sf + (j * (cols / 128) + tcol) * 512 + cell + 2 * odd) = v;
+      }
+      if (d_out != nullptr) {
+#pragma unroll
+        for (int pass = 0; pass < 8; ++pass) {
+          const int r = pass * 16 + (tid >> 4);
+          const int seg = tid & 15;
+          if (r < cur.valid) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][seg * 8]);
+            const int col = seg < 8 ? cb * 64 + seg * 8 : inter + cb * 64 + (seg - 8) * 8;
+            *reinterpret_cast<uint4 *>(d_out + (cur.src0 + r) * cols + col) = v;
+          }
+        }
+      }
+    } else {
+      if (tid < 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
+        *reinterpret_cast<uint4 *>(sf_t + (static_cast<int64_t>(cb) * (ld / 128) + j) * 512 + tid * 16) = v;
+      } else if (kRows && tid < 64) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[(tid - 32) * 16]);
+        *reinterpret_cast<uint4 *>(row_sf + (j * cblocks + cb) * 512 + (tid - 32) * 16) = v;
+      }
     }
     cur = nxt;
     advance(nxt);
@@ -328,25 +450,30 @@ cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a) {
   return cudaGetLastError();
 }
 
-template <bool kRows>
+template <int kMode>
 static cudaError_t launch_cols(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
   const int threads = 256;
-  const int64_t tiles = (a.ld / 128) * (a.cols / 128);
+  const int64_t tiles = (a.ld / 128) * (a.cols / 128);  // kSwiGLUBwd: inter / 64 = cols / 128 column blocks
   const int64_t cap = static_cast<int64_t>(a.num_sms) * 2;
   const int blocks = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
-  cudaError_t err = cudaFuncSetAttribute(mxfp8_cols_kernel<kRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(mxfp8_cols_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kColSmemBytes);
   if (err != cudaSuccess) return err;
-  mxfp8_cols_kernel<kRows><<<blocks, threads, kColSmemBytes, a.stream>>>(
+  mxfp8_cols_kernel<kMode><<<blocks, threads, kColSmemBytes, a.stream>>>(
       static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.cols), a.offsets, a.num_groups, a.codes, a.sf,
-      a.ld, a.padded_offsets, row_codes, row_sf, a.status);
+      a.ld, a.padded_offsets, row_codes, row_sf, a.status, static_cast<const uint16_t *>(a.dh),
+      static_cast<uint16_t *>(a.d_out));
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a) { return launch_cols<false>(a, nullptr, nullptr); }
+cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a) { return launch_cols<kColsOnly>(a, nullptr, nullptr); }
 
 cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
-  return launch_cols<true>(a, row_codes, row_sf);
+  return launch_cols<kRowCol>(a, row_codes, row_sf);
+}
+
+cudaError_t launch_swiglu_bwd_mxfp8(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
+  return launch_cols<kSwiGLUBwd>(a, row_codes, row_sf);
 }
 
 }  // namespace fme

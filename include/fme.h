@@ -14,6 +14,8 @@
  *                             outputs per token.
  *   quantize_mxfp8            standard MXFP8 of the backward: E4M3 codes, one E8M0
  *                             scale per 32 values, row-wise or column-wise.
+ *   swiglu_backward_quantize_mxfp8   the SwiGLU backward, d(gate/up) quantized
+ *                             row-wise and column-wise for the gate/up gradients.
  *   grouped_gemm_fwd_nvfp4    Y_e = X_e W_e^T per expert, per-token scales applied
  *                             in the epilogue, bf16 out.
  *   grouped_gemm_fwd_mxfp8    the same product with MXFP8 operands (no per-token scale).
@@ -288,6 +290,29 @@ fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axi
 fme_status quantize_mxfp8_rowcol(const void *x, int64_t rows, int64_t cols, const int32_t *offsets,
                                  int32_t num_groups, uint8_t *row_codes, uint8_t *row_sf, uint8_t *col_codes,
                                  uint8_t *col_sf, int32_t *padded_offsets, int32_t *dev_status, void *stream);
+
+/*
+ * swiglu_backward_quantize_mxfp8 -- the gate/up side of the expert backward.  With
+ * the forward's h = silu(g) * u of the gate/up output [g | u] (silu(v) = v sigma(v),
+ * "Scaling and Optimizing Frontier Model Training", "MXFP8 expert kernels": the
+ * DeepSeek-V3-class experts; the activation read as SwiGLU) and dh the gradient of
+ * h, computes d(gate/up) = [dg | du],
+ *   dg = dh * u * sigma(g) * (1 + g * sigma(-g)),   du = dh * g * sigma(g),
+ * in fp32, rounds it to bf16 and quantizes it as quantize_mxfp8_rowcol would
+ * (row-wise for the gate/up dgrad, column-wise for its wgrad), in one pass.
+ *   gate_up    device bf16 [rows x 2*inter]: [g | u] per row
+ *   dh         device bf16 [rows x inter]
+ *   inter      a multiple of 128, 128 .. 32768
+ *   row_codes, row_sf, col_codes, col_sf, padded_offsets
+ *              as quantize_mxfp8_rowcol of a [rows x 2*inter] tensor
+ *   d_gate_up  device bf16 [rows x 2*inter] or NULL: the bf16 d(gate/up) that was
+ *              quantized
+ */
+fme_status swiglu_backward_quantize_mxfp8(const void *gate_up, const void *dh, int64_t rows, int64_t inter,
+                                          const int32_t *offsets, int32_t num_groups, uint8_t *row_codes,
+                                          uint8_t *row_sf, uint8_t *col_codes, uint8_t *col_sf,
+                                          int32_t *padded_offsets, void *d_gate_up, int32_t *dev_status,
+                                          void *stream);
 
 /*
  * grouped_gemm_fwd_nvfp4 -- Y[t, :] = S_x[t] * S_w[e, :] * sum_k A'[t,k] B'_e[:,k]

@@ -83,10 +83,11 @@ def _declare(lib):
     lib.fme_orc_gemm_abt.argtypes = [P, P, I64, I64, I64, P]
     lib.fme_orc_swiglu.argtypes = [P, I64, I64, P]
     lib.fme_orc_route.argtypes = [P, I64, I32, P, P, P]
+    lib.fme_orc_swiglu_bwd.argtypes = [P, P, I64, I64, P]
     lib.fme_orc_combine.argtypes = [P, P, P, I64, I32, I64, P]
     for name in ("fme_orc_e2m1_encode_array", "fme_orc_e4m3_encode_array", "fme_orc_quant_nvfp4",
                  "fme_orc_dequant_nvfp4", "fme_orc_quant_mxfp8_rows", "fme_orc_quant_mxfp8_cols",
-                 "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt", "fme_orc_swiglu", "fme_orc_route",
+                 "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt", "fme_orc_swiglu", "fme_orc_route", "fme_orc_swiglu_bwd",
                  "fme_orc_combine"):
         getattr(lib, name).restype = None
     return lib
@@ -206,6 +207,18 @@ class Oracle:
         h = np.empty((rows, inter), np.float64)
         self.lib.fme_orc_swiglu(_p(y), rows, inter, _p(h))
         return h
+
+    def swiglu_bwd(self, y_gu_bits, dh_bits) -> np.ndarray:
+        """d(gate/up) = [dg | du] in fp64 of h = silu(g) * u for upstream dh (bf16 bits)."""
+        y = _bits(y_gu_bits)
+        dh = _bits(dh_bits)
+        rows, two_inter = y.shape
+        inter = two_inter // 2
+        if dh.shape != (rows, inter):
+            raise ValueError("dh must be [rows x inter]")
+        out = np.empty((rows, two_inter), np.float64)
+        self.lib.fme_orc_swiglu_bwd(_p(y), _p(dh), rows, inter, _p(out))
+        return out
 
     # routing -------------------------------------------------------------
     def route(self, ids, num_experts: int):

@@ -28,7 +28,8 @@
  *     intermediate 2048; the gate/up projection is twice the intermediate
  *     width).  The activation between the two projections is read as SwiGLU,
  *     h = silu(g) * u with silu(v) = v / (1 + e^-v), g and u the two halves of
- *     the gate/up output; the oracle evaluates it in fp64.
+ *     the gate/up output; the oracle evaluates it in fp64, and its gradient
+ *     (the backward of the gate/up side, d(gate/up) from dh) in fp64 too.
  *   - "Cursor Composer 2 report deep dive", section 2, and the report's
  *     section 6.1: tokens are quantized before dispatch to their experts and
  *     the experts' outputs are combined per token in BF16; section 6.2: the
@@ -378,6 +379,23 @@ void fme_orc_swiglu(const uint16_t *y_gu, int64_t rows, int64_t inter, double *h
             const double g = (double)bf16_value(row[j]);
             const double u = (double)bf16_value(row[inter + j]);
             h[t * inter + j] = g / (1.0 + exp(-g)) * u;
+        }
+    }
+}
+
+/* d(gate/up) [rows x 2 inter] of h = silu(g) * u for the upstream gradient dh
+ * [rows x inter] (bf16), in fp64: with s = 1 / (1 + e^-g) (the logistic function),
+ * dh/dg = dh * u * (s + g * s * (1 - s)) and dh/du = dh * g * s; row t of the
+ * result is [dg_t | du_t]. */
+void fme_orc_swiglu_bwd(const uint16_t *y_gu, const uint16_t *dh, int64_t rows, int64_t inter, double *d_gu) {
+    for (int64_t t = 0; t < rows; ++t) {
+        for (int64_t j = 0; j < inter; ++j) {
+            const double g = (double)bf16_value(y_gu[t * 2 * inter + j]);
+            const double u = (double)bf16_value(y_gu[t * 2 * inter + inter + j]);
+            const double d = (double)bf16_value(dh[t * inter + j]);
+            const double s = 1.0 / (1.0 + exp(-g));
+            d_gu[t * 2 * inter + j] = d * u * (s + g * s * (1.0 - s));
+            d_gu[t * 2 * inter + inter + j] = d * g * s;
         }
     }
 }

@@ -426,6 +426,43 @@ def check_swiglu_vs_scipy(orc):
     assert np.allclose(h, want, rtol=4e-16, atol=1e-300)
 
 
+def check_swiglu_bwd_finite_differences(orc):
+    """The backward is the derivative of the forward: dg / (dh u) against central
+    differences of silu (scipy's logistic function, fp64, step 1e-5), and
+    du / dh against silu itself, on bf16 inputs over the range that matters."""
+    from scipy.special import expit
+
+    rng = np.random.default_rng(31)
+    g = synth.bf16_float(synth.bf16_bits(rng.standard_normal((4, 64)) * 4.0))
+    u = synth.bf16_float(synth.bf16_bits(rng.standard_normal((4, 64))))
+    dh = synth.bf16_float(synth.bf16_bits(rng.standard_normal((4, 64))))
+    d = orc.swiglu_bwd(_swiglu_rows(g, u), synth.bf16_bits(dh))
+    gd, ud, hd = (a.astype(np.float64) for a in (g, u, dh))
+    silu = lambda v: v * expit(v)  # noqa: E731
+    eps = 1e-5
+    dsilu = (silu(gd + eps) - silu(gd - eps)) / (2 * eps)
+    assert np.allclose(d[:, :64], hd * ud * dsilu, rtol=1e-7, atol=1e-9)
+    assert np.allclose(d[:, 64:], hd * silu(gd), rtol=1e-14, atol=1e-300)
+
+
+def check_swiglu_bwd_closed_forms(orc):
+    """silu'(0) = 1/2 and silu(0) = 0; silu' -> 1 and silu(g) -> g for large g, both
+    -> 0 for very negative g; u = 0 gives dg = 0; silu' changes sign between
+    g = -1.2734375 and -1.28515625 (its root is near -1.2785); the gate and up
+    halves of the gradient are [dg | du]."""
+    g = np.array([[0.0, 0.0, 60.0, -60.0, 2.5, -1.2734375, -1.28515625, 1.0]], np.float32)
+    u = np.array([[1.5, -2.0, 0.75, 3.0, 0.0, 1.0, 1.0, -1.0]], np.float32)
+    dh = np.array([[1.0, 0.5, -2.0, 1.0, 4.0, 1.0, 1.0, 2.0]], np.float32)
+    d = orc.swiglu_bwd(_swiglu_rows(g, u), synth.bf16_bits(dh))
+    dg, du = d[0, :8], d[0, 8:]
+    assert dg[0] == 0.75 and dg[1] == -0.5 and du[0] == 0.0 and du[1] == 0.0
+    assert abs(dg[2] - (-1.5)) < 1e-20 and abs(du[2] - (-120.0)) < 1e-20
+    assert abs(dg[3]) < 1e-20 and abs(du[3]) < 1e-20
+    assert dg[4] == 0.0 and du[4] != 0.0
+    assert dg[5] > 0.0 > dg[6] and abs(dg[5]) < 1e-2 and abs(dg[6]) < 1e-2
+    assert np.isclose(du[7], 2.0 * 1.0 / (1.0 + np.exp(-1.0)), rtol=1e-15)
+
+
 # --------------------------------------------------------------- routing ----
 def check_route_vs_stable_argsort(orc):
     """Grouping = numpy's stable argsort of the ids (another sort algorithm);

@@ -28,7 +28,7 @@ def test_header_declares_the_five_calls():
                  "grouped_gemm_fwd_nvfp4",
                  "grouped_gemm_fwd_mxfp8",
                  "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8", "moe_route", "permute_quantize_nvfp4",
-                 "permute_quantize_mxfp8", "moe_combine"):
+                 "permute_quantize_mxfp8", "moe_combine", "swiglu_backward_quantize_mxfp8"):
         assert call in names
 
 
@@ -101,6 +101,13 @@ def test_host_argument_checks(lib):
     assert m(good, 10, 96, 1, None, 1, good, good, good, None, _stream()) == 3   # column-wise needs cols % 128
     assert m(good, 10, 256, 1, None, 1, good, good, None, None, _stream()) == 1
     assert m(good, 10, 256, 1, None, 1, good, odd, good, None, _stream()) == 2
+    sb = lib.swiglu_backward_quantize_mxfp8
+    assert sb(good, good, 10, 192, None, 1, good, good, good, good, good, None, None, _stream()) == 3   # inter % 128
+    assert sb(good, good, 10, 32896, None, 1, good, good, good, good, good, None, None, _stream()) == 3
+    assert sb(good, good, 10, 256, None, 2, good, good, good, good, good, None, None, _stream()) == 1  # no offsets
+    assert sb(good, None, 10, 256, None, 1, good, good, good, good, good, None, None, _stream()) == 1   # dh
+    assert sb(good, good, 10, 256, None, 1, good, good, good, good, None, None, None, _stream()) == 1  # padded
+    assert sb(good, good, 10, 256, None, 1, good, good, good, good, good, odd, None, _stream()) == 2   # d out
     f = lib.grouped_gemm_fwd_nvfp4
     assert f(good, good, good, good, good, good, good, 4, 100, 100, 256, good, None, _stream()) == 3
     assert f(good, good, good, good, good, good, good, 4, 100, 256, 100, good, None, _stream()) == 3

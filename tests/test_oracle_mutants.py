@@ -49,6 +49,12 @@ MUTANTS = {
     "swiglu_gate_up_halves_swapped": ("const double g = (double)bf16_value(row[j]);\n            const double u = (double)bf16_value(row[inter + j]);",
                                       "const double u = (double)bf16_value(row[j]);\n            const double g = (double)bf16_value(row[inter + j]);"),
     "swiglu_drops_up": ("h[t * inter + j] = g / (1.0 + exp(-g)) * u;", "h[t * inter + j] = g / (1.0 + exp(-g));"),
+    "swiglu_bwd_reads_up_as_gate": ("const double g = (double)bf16_value(y_gu[t * 2 * inter + j]);",
+                                    "const double g = (double)bf16_value(y_gu[t * 2 * inter + inter + j]);"),
+    "swiglu_bwd_drops_sigma_derivative": ("d * u * (s + g * s * (1.0 - s))", "d * u * s"),
+    "swiglu_bwd_one_minus_s_as_s": ("d * u * (s + g * s * (1.0 - s))", "d * u * (s + g * s * s)"),
+    "swiglu_bwd_halves_swapped": ("d_gu[t * 2 * inter + j] = d * u", "d_gu[t * 2 * inter + inter + j] = d * u"),
+    "swiglu_bwd_du_uses_u": ("d_gu[t * 2 * inter + inter + j] = d * g * s;", "d_gu[t * 2 * inter + inter + j] = d * u * s;"),
     "route_unstable": ("        for (int64_t a = 0; a < n; ++a) {\n            if (ids[a] == e) {",
                        "        for (int64_t a = n - 1; a >= 0; --a) {\n            if (ids[a] == e) {"),
     "route_offsets_not_summed": ("offsets[e + 1] += offsets[e];", "offsets[e + 1] += 0;"),
