@@ -62,6 +62,7 @@ SYMBOLS = {
     # name: (restype, argtypes)
     "quantize_nvfp4_pertoken": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p"]),
     "quantize_nvfp4_weights": ("i32", ["p", "i64", "i64", "p", "p", "p", "p", "p"]),
+    "quantize_nvfp4_pertensor": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p"]),
     "swiglu_quantize_nvfp4": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8": ("i32", ["p", "i64", "i64", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8_rowcol": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p", "p"]),
@@ -173,6 +174,29 @@ def quantize_nvfp4_pertoken(x, offsets=None, num_groups=None, *, codes=None, sf=
                                        _ptr(status), _stream(stream))
     _check(st, "quantize_nvfp4_pertoken")
     return codes, sf, row_scale
+
+
+def quantize_nvfp4_pertensor(x, offsets=None, num_groups=None, *, codes=None, sf=None, row_scale=None,
+                             tensor_amax=None, status=None, stream=None):
+    """Standard NVFP4 (one FP32 scale for the tensor) of bf16 x [rows, k] ->
+    (codes, sf, row_scale (S in every row), tensor_amax [1])."""
+    import torch
+
+    rows, k = x.shape
+    offsets, g = _groups(offsets, num_groups)
+    dev = x.device
+    if codes is None:
+        codes = _empty((rows, k // 2), torch.uint8, dev)
+    if sf is None:
+        sf = _empty((max(sf_bytes(rows, k, 16, g), 16),), torch.uint8, dev)
+    if row_scale is None:
+        row_scale = _empty((max(rows, 1),), torch.float32, dev)
+    if tensor_amax is None:
+        tensor_amax = _empty((4,), torch.float32, dev)
+    st = lib().quantize_nvfp4_pertensor(_ptr(x), rows, k, _ptr(offsets), g, _ptr(codes), _ptr(sf),
+                                        _ptr(row_scale), _ptr(tensor_amax), _ptr(status), _stream(stream))
+    _check(st, "quantize_nvfp4_pertensor")
+    return codes, sf, row_scale[:rows], tensor_amax[:1]
 
 
 def quantize_nvfp4_weights(w, *, codes=None, sf=None, row_scale=None, status=None, stream=None):

@@ -215,6 +215,26 @@ fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_nvfp4_pertoken launch");
 }
 
+fme_status quantize_nvfp4_pertensor(const void *x, int64_t rows, int64_t k, const int32_t *offsets,
+                                    int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale,
+                                    float *tensor_amax, int32_t *dev_status, void *stream) {
+  if (rows < 0 || check_groups(num_groups) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
+  if (offsets == nullptr && num_groups != 1) return FME_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0 || k < 64 || k > 8192) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (rows > (int64_t(1) << 31) - 1 - 128 * static_cast<int64_t>(num_groups)) return FME_ERR_UNSUPPORTED_SHAPE;
+  if (!tensor_amax) return FME_ERR_INVALID_ARGUMENT;
+  if (rows > 0 && (!x || !codes || !sf || !row_scale)) return FME_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) || !aligned16(row_scale) || !aligned16(tensor_amax))
+    return FME_ERR_MISALIGNED;
+  int sms = 0;
+  fme_status st = current_device(&sms);
+  if (st != FME_OK) return st;
+  fme::LaunchNvfp4 a{x, rows, k, offsets, num_groups, codes, sf, row_scale, dev_status, sms,
+                     static_cast<cudaStream_t>(stream)};
+  cudaError_t err = fme::launch_quantize_nvfp4_pertensor(a, tensor_amax);
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_nvfp4_pertensor launch");
+}
+
 fme_status quantize_nvfp4_weights(const void *x, int64_t rows, int64_t k, uint8_t *codes, uint8_t *sf,
                                   float *row_scale, int32_t *dev_status, void *stream) {
   if (rows < 0) return FME_ERR_INVALID_ARGUMENT;

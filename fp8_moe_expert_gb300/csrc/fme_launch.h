@@ -24,6 +24,7 @@ struct LaunchNvfp4 {
   const int32_t *gather = nullptr;  // row r reads input row gather[r] / gather_div (permuted tokens)
   int32_t gather_div = 1;
   int64_t gather_limit = 0;         // input rows; gathered rows outside [0, limit) are reported
+  const float *tensor_amax = nullptr;  // standard NVFP4: every row scaled by this amax (device)
 };
 
 struct LaunchRoute {
@@ -90,6 +91,9 @@ struct LaunchGemm {
 };
 
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a);
+// Standard NVFP4 (one FP32 scale for the whole tensor): zero *tensor_amax, reduce
+// max |x| into it, then quantize every row with it in place of the row's amax.
+cudaError_t launch_quantize_nvfp4_pertensor(const LaunchNvfp4 &a, float *tensor_amax);
 cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a);
 cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf);

@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
                           int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
                           float *__restrict__ row_scale, uint16_t *__restrict__ h_out, int32_t *status,
-                          int stages, const int32_t *__restrict__ gather, int gather_div, int64_t gather_limit) {
+                          int stages, const int32_t *__restrict__ gather, int gather_div, int64_t gather_limit,
+                          const float *__restrict__ tensor_amax) {
   __shared__ int ok_flag;
   __shared__ int abort_flag;
   __shared__ uint32_t part[2][kNvMaxThreads / 32];  // per-warp amax of the row, double-buffered by row parity
@@ -292,7 +293,8 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       s = 0;
       parity ^= 1u;
     }
-    const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, lane < nwarps ? part[i & 1][lane] : 0u);
+    uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, lane < nwarps ? part[i & 1][lane] : 0u);
+    if (tensor_amax != nullptr) amax_bits = __float_as_uint(*tensor_amax) >> 16;  // standard NVFP4: one scale
     uint8_t *sf_row = sf + sf_row_of[i & 1];
     uint8_t *codes_row = codes + row * (k / 2);
     const float amax = bf16_bits_to_float(amax_bits);
@@ -370,8 +372,45 @@ static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   kernel<<<blocks, threads, smem, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.k),
                                               a.offsets, a.num_groups, a.codes, a.sf, a.row_scale,
                                               static_cast<uint16_t *>(a.h_out), a.status, static_cast<int>(stages),
-                                              a.gather, a.gather_div, a.gather_limit);
+                                              a.gather, a.gather_div, a.gather_limit, a.tensor_amax);
   return cudaGetLastError();
+}
+
+// max |x| over n bf16 values (n a multiple of 8) into *out (zeroed before): the
+// bf16 maximum as an fp32 whose bits order like unsigned integers, so one
+// atomicMax per CTA merges the CTAs' maxima.
+__global__ void __launch_bounds__(256) tensor_amax_kernel(const uint16_t *__restrict__ x, int64_t n, float *out) {
+  uint32_t m = 0;
+  const int64_t words = n / 8;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < words;
+       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(x) + w);
+    m = max(m, amax16_bits(v, v));
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t wm[8];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t v = threadIdx.x < (blockDim.x >> 5) ? wm[threadIdx.x] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int *>(out), v << 16);
+  }
+}
+
+cudaError_t launch_quantize_nvfp4_pertensor(const LaunchNvfp4 &a, float *tensor_amax) {
+  cudaError_t err = cudaMemsetAsync(tensor_amax, 0, sizeof(float), a.stream);
+  if (err != cudaSuccess) return err;
+  const int64_t words = a.rows * a.k / 8;
+  const int64_t need = (words + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
+  const int blocks = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+  tensor_amax_kernel<<<blocks, 256, 0, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows * a.k, tensor_amax);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  LaunchNvfp4 b = a;
+  b.tensor_amax = tensor_amax;
+  return launch_quantize_nvfp4(b);
 }
 
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {

@@ -5,6 +5,7 @@
  * row-wise + column-wise MXFP8 quantizer for tensors needed both ways):
  *   quantize_nvfp4_pertoken   NVFP4 variant of the forward: E2M1 codes, one E4M3
  *                             scale per 16 values along K, one FP32 scale per token.
+ *   quantize_nvfp4_pertensor  standard NVFP4 (one FP32 scale per tensor), the comparator.
  *   quantize_nvfp4_weights    the same quantization of the stacked expert weights,
  *                             scales written in the forward GEMM's B-operand layout.
  *   swiglu_quantize_nvfp4     silu(gate) * up of the gate/up output, quantized as above.
@@ -121,6 +122,21 @@ typedef int32_t fme_status;
 fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const int32_t *offsets,
                                    int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale,
                                    int32_t *dev_status, void *stream);
+
+/*
+ * quantize_nvfp4_pertensor -- standard NVFP4, the comparator of the per-token
+ * variant: the same steps with one FP32 scale for the whole tensor, S =
+ * fl32(amax_x / 2688) where amax_x = max |x| over every row ("Cursor Composer 2
+ * report deep dive", section 1, and "Composer 2 Technical Report", section 6.1:
+ * standard NVFP4 scales per tensor, which makes a token's codes depend on the rest
+ * of the batch).  Arguments as quantize_nvfp4_pertoken; row_scale[t] = S for
+ * every row, so grouped_gemm_fwd_nvfp4 consumes the outputs unchanged.
+ *   tensor_amax  device float [1], overwritten with amax_x (it is zeroed and
+ *                reduced into on the stream first)
+ */
+fme_status quantize_nvfp4_pertensor(const void *x, int64_t rows, int64_t k, const int32_t *offsets,
+                                    int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale,
+                                    float *tensor_amax, int32_t *dev_status, void *stream);
 
 /*
  * quantize_nvfp4_weights -- quantize_nvfp4_pertoken of the stacked expert weights

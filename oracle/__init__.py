@@ -76,6 +76,7 @@ def _declare(lib):
     lib.fme_orc_e2m1_encode_array.argtypes = [P, I64, P]
     lib.fme_orc_e4m3_encode_array.argtypes = [P, I64, P]
     lib.fme_orc_quant_nvfp4.argtypes = [P, I64, I64, P, P, P]
+    lib.fme_orc_quant_nvfp4_pertensor.argtypes = [P, I64, I64, P, P, P]
     lib.fme_orc_dequant_nvfp4.argtypes = [P, P, P, I64, I64, P]
     lib.fme_orc_quant_mxfp8_rows.argtypes = [P, I64, I64, P, P]
     lib.fme_orc_quant_mxfp8_cols.argtypes = [P, I64, I64, P, I32, I64, P, P, P]
@@ -88,6 +89,7 @@ def _declare(lib):
     for name in ("fme_orc_e2m1_encode_array", "fme_orc_e4m3_encode_array", "fme_orc_quant_nvfp4",
                  "fme_orc_dequant_nvfp4", "fme_orc_quant_mxfp8_rows", "fme_orc_quant_mxfp8_cols",
                  "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt", "fme_orc_swiglu", "fme_orc_route", "fme_orc_swiglu_bwd",
+                 "fme_orc_quant_nvfp4_pertensor",
                  "fme_orc_combine"):
         getattr(lib, name).restype = None
     return lib
@@ -145,6 +147,18 @@ class Oracle:
         sf = np.zeros((rows, k // 16), np.uint8)
         scale = np.zeros(rows, np.float32)
         self.lib.fme_orc_quant_nvfp4(_p(x), rows, k, _p(codes), _p(sf), _p(scale))
+        return codes, sf, scale
+
+    def quant_nvfp4_pertensor(self, x_bits):
+        """Standard NVFP4 (one scale for the tensor) -> codes, sf, scale [rows] (all S)."""
+        x = _bits(x_bits)
+        rows, k = x.shape
+        if k % 16:
+            raise ValueError("k must be a multiple of 16")
+        codes = np.zeros((rows, k // 2), np.uint8)
+        sf = np.zeros((rows, k // 16), np.uint8)
+        scale = np.zeros(rows, np.float32)
+        self.lib.fme_orc_quant_nvfp4_pertensor(_p(x), rows, k, _p(codes), _p(sf), _p(scale))
         return codes, sf, scale
 
     def dequant_nvfp4(self, codes, sf, scale) -> np.ndarray:

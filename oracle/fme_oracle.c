@@ -184,11 +184,19 @@ uint8_t fme_orc_e4m3_encode(double v) {
  *   scale [rows]        S_t.
  * Nothing crosses rows: a row's outputs depend on that row alone.
  */
-void fme_orc_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t k,
-                         uint8_t *codes, uint8_t *sf, float *scale) {
+static void quant_nvfp4_rows(const uint16_t *x, int64_t rows, int64_t k, int per_tensor,
+                             uint8_t *codes, uint8_t *sf, float *scale) {
     const int64_t nblk = k / 16;
     if (rows <= 0 || k <= 0)
         return;
+    float tensor_amax = 0.0f;
+    if (per_tensor) {
+        for (int64_t i = 0; i < rows * k; ++i) {
+            float a = fabsf(bf16_value(x[i]));
+            if (a > tensor_amax)
+                tensor_amax = a;
+        }
+    }
     for (int64_t t = 0; t < rows; ++t) {
         const uint16_t *xr = x + t * k;
         uint8_t *cr = codes + t * (k / 2);
@@ -200,6 +208,8 @@ void fme_orc_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t k,
             if (a > amax)
                 amax = a;
         }
+        if (per_tensor)
+            amax = tensor_amax;
         memset(cr, 0, (size_t)(k / 2));
         if (amax == 0.0f) {
             scale[t] = 0.0f;
@@ -236,6 +246,22 @@ void fme_orc_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t k,
             }
         }
     }
+}
+
+void fme_orc_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t k,
+                         uint8_t *codes, uint8_t *sf, float *scale) {
+    quant_nvfp4_rows(x, rows, k, 0, codes, sf, scale);
+}
+
+/*
+ * Standard NVFP4, the comparator ("Cursor Composer 2 report deep dive", section
+ * 1; report section 6.1: standard NVFP4 has a per-tensor FP32 scale): the steps
+ * above with amax_t replaced by the amax of the whole tensor, so S (scale[t]) is
+ * the same for every row and a row's codes depend on every other row.
+ */
+void fme_orc_quant_nvfp4_pertensor(const uint16_t *x, int64_t rows, int64_t k,
+                                   uint8_t *codes, uint8_t *sf, float *scale) {
+    quant_nvfp4_rows(x, rows, k, 1, codes, sf, scale);
 }
 
 /* x_hat = dec_E2M1(q) * dec_E4M3(sb) * S_t, exact in fp64. */

@@ -426,6 +426,38 @@ def check_swiglu_vs_scipy(orc):
     assert np.allclose(h, want, rtol=4e-16, atol=1e-300)
 
 
+def check_nvfp4_pertensor_special_cases(orc):
+    """Standard NVFP4 is the per-token variant when the tensor is one row, or when
+    every row has the tensor's amax; its scale is fl32(amax_tensor / 2688) (numpy
+    binary32 division) in every row."""
+    x, _, _ = synth.quantizer_batch(rows=24, cols=512, seed=41)
+    one = x[5:6]
+    assert all(np.array_equal(a, b) for a, b in zip(orc.quant_nvfp4_pertensor(one), orc.quant_nvfp4(one)))
+    same = x.copy()
+    big = synth.bf16_bits(np.float32(-4.0) * np.abs(synth.bf16_float(x)).max())
+    same[:, 7] = big
+    assert all(np.array_equal(a, b) for a, b in zip(orc.quant_nvfp4_pertensor(same), orc.quant_nvfp4(same)))
+    _, _, scale = orc.quant_nvfp4_pertensor(x)
+    amax = np.abs(synth.bf16_float(x)).max()
+    assert np.all(scale.view(np.uint32) == (np.float32(amax) / np.float32(2688.0)).view(np.uint32))
+
+
+def check_nvfp4_pertensor_batch_variance(orc):
+    """The reason for the per-token variant: with one scale per tensor a row's codes
+    change when a row with a larger amax joins the batch (here appended last, so
+    a later token changes earlier tokens' codes), while the per-token codes of the
+    same rows do not."""
+    x, _, small = synth.quantizer_batch(rows=32, cols=256, seed=43)
+    loud = synth.bf16_bits(synth.bf16_float(x[:1]) * np.float32(64.0))
+    both = np.concatenate([x, loud])
+    c0, s0, _ = orc.quant_nvfp4_pertensor(x)
+    c1, s1, _ = orc.quant_nvfp4_pertensor(both)
+    assert not np.array_equal(c1[:32], c0) and not np.array_equal(s1[:32], s0)
+    p0, ps0, _ = orc.quant_nvfp4(x)
+    p1, ps1, _ = orc.quant_nvfp4(both)
+    assert np.array_equal(p1[:32], p0) and np.array_equal(ps1[:32], ps0)
+
+
 def check_swiglu_bwd_finite_differences(orc):
     """The backward is the derivative of the forward: dg / (dh u) against central
     differences of silu (scipy's logistic function, fp64, step 1e-5), and

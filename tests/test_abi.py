@@ -24,7 +24,7 @@ def declared_functions():
 
 def test_header_declares_the_five_calls():
     names = declared_functions()
-    for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_weights", "swiglu_quantize_nvfp4", "quantize_mxfp8",
+    for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_pertensor", "quantize_nvfp4_weights", "swiglu_quantize_nvfp4", "quantize_mxfp8",
                  "grouped_gemm_fwd_nvfp4",
                  "grouped_gemm_fwd_mxfp8",
                  "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8", "moe_route", "permute_quantize_nvfp4",
@@ -79,6 +79,11 @@ def test_host_argument_checks(lib):
     assert q(None, 10, 256, None, 1, good, good, good, None, _stream()) == 1
     assert q(odd, 10, 256, None, 1, good, good, good, None, _stream()) == 2
     assert q(good, 0, 256, None, 1, None, None, None, None, _stream()) == 0     # nothing to do
+    qt = lib.quantize_nvfp4_pertensor
+    assert qt(good, 10, 96, None, 1, good, good, good, good, None, _stream()) == 3     # k % 64
+    assert qt(good, 10, 256, None, 1, good, good, good, None, None, _stream()) == 1    # no amax word
+    assert qt(good, 10, 256, None, 3, good, good, good, good, None, _stream()) == 1    # groups without offsets
+    assert qt(good, 10, 256, None, 1, good, good, good, odd, None, _stream()) == 2
     qw = lib.quantize_nvfp4_weights
     assert qw(good, -256, 256, good, good, good, None, _stream()) == 1
     assert qw(good, 100, 256, good, good, good, None, _stream()) == 3     # rows % 256

@@ -339,3 +339,37 @@ def test_moe_skewed_long_batch(fme, orc):
     counts = synth.zipf_counts()
     _moe_fwd_sampled(fme, orc, counts, seed=4, label="zipf")
     _moe_bwd_sampled(fme, orc, counts, seed=4, label="zipf")
+
+
+def test_fwd_pertensor_comparator(fme, orc):
+    """The forward GEMM on standard-NVFP4 X (one scale for the batch) against the
+    oracle, and the reason for the per-token variant ("Composer 2 Technical
+    Report", section 6.1): with a louder token appended to the batch, the earlier
+    tokens' outputs change under the per-tensor scale and stay bit-identical under
+    the per-token one."""
+    import torch
+
+    x_bits, _, _ = synth.quantizer_batch(rows=1024, cols=1024, seed=71)
+    w_bits = synth.normal_bits((256, 1024), 0.02, seed=72)
+    loud = synth.bf16_bits(synth.bf16_float(x_bits[:128]) * np.float32(64.0))
+    st = _status()
+    w = bf16_tensor(w_bits)
+    wq = fme.quantize_nvfp4_weights(w, status=st)
+
+    def fwd(xb, per_tensor):
+        off = _i32([0, xb.shape[0]])
+        x = bf16_tensor(xb)
+        q = fme.quantize_nvfp4_pertensor(x, off, status=st)[:3] if per_tensor else \
+            fme.quantize_nvfp4_pertoken(x, off, status=st)
+        return fme.grouped_gemm_fwd_nvfp4(*q, *wq, off, 256, 1024, status=st)
+
+    y_t = fwd(x_bits, True)
+    a = orc.dequant_nvfp4(*orc.quant_nvfp4_pertensor(x_bits))
+    b = orc.dequant_nvfp4(*orc.quant_nvfp4(w_bits))
+    check_gemm_tolerance(bf16_to_f64(y_t), orc.gemm_abt(a, b), what="fwd per-tensor")
+    both = np.concatenate([x_bits, loud])
+    y_t2 = fwd(both, True)
+    y_p, y_p2 = fwd(x_bits, False), fwd(both, False)
+    _ok(fme, st)
+    assert not torch.equal(y_t, y_t2[:1024])
+    assert torch.equal(y_p, y_p2[:1024])

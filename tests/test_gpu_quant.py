@@ -316,3 +316,49 @@ def test_bad_offsets_set_device_status(fme):
     short = torch.tensor([0, 10, 20], dtype=torch.int32, device="cuda")   # does not reach rows
     fme.quantize_mxfp8(x, fme.COLWISE, short, status=st)
     assert fme.read_device_status(st)[1] & fme.DEV_BAD_OFFSETS
+
+
+# ------------------------------------------------ standard NVFP4 (per tensor) --
+def run_nvfp4_pertensor(fme, x_bits, offsets=None):
+    x = bf16_tensor(x_bits)
+    st = _status()
+    codes, sf, scale, amax = fme.quantize_nvfp4_pertensor(x, _dev_offsets(offsets), status=st)
+    code, raw = fme.read_device_status(st)
+    assert code == 0, raw
+    rows, k = x_bits.shape
+    return to_np(codes), unswizzle(to_np(sf), rows, k // 16, offsets), to_np(scale), float(to_np(amax)[0])
+
+
+@pytest.mark.parametrize("case", ["tiny", "batch", "groups", "one_row", "zeros"])
+def test_nvfp4_pertensor_matches_oracle(fme, orc, case):
+    off = None
+    if case == "tiny":
+        x, _ = synth.tiny(0)
+    elif case == "batch":
+        x, _, _ = synth.quantizer_batch(rows=4096)
+    elif case == "groups":
+        off = synth.offsets_from_counts([37, 0, 200, 1, 129])
+        x, _, _ = synth.quantizer_batch(rows=int(off[-1]), cols=2048, seed=3)
+    elif case == "one_row":
+        x, _, _ = synth.quantizer_batch(rows=1, cols=7168, seed=4)
+    else:
+        x = np.zeros((64, 512), np.uint16)
+    codes, sf, scale, amax = run_nvfp4_pertensor(fme, x, off)
+    oc, osf, oscale = orc.quant_nvfp4_pertensor(x)
+    assert amax == float(np.abs(synth.bf16_float(x)).max())
+    assert np.array_equal(scale.view(np.uint32), oscale.view(np.uint32))
+    assert np.array_equal(sf, osf)
+    assert np.array_equal(codes, oc)
+
+
+def test_nvfp4_pertensor_batch_variance_on_gpu(fme):
+    """A louder row joining the batch changes the other rows' standard-NVFP4 codes
+    and leaves their per-token codes alone."""
+    x, _, _ = synth.quantizer_batch(rows=512, cols=1024, seed=8)
+    loud = synth.bf16_bits(synth.bf16_float(x[:1]) * np.float32(64.0))
+    both = np.concatenate([x, loud])
+    a = run_nvfp4_pertensor(fme, x)
+    b = run_nvfp4_pertensor(fme, both)
+    assert not np.array_equal(a[0], b[0][:512])
+    pa, pb = run_nvfp4(fme, x), run_nvfp4(fme, both)
+    assert np.array_equal(pa[0], pb[0][:512]) and np.array_equal(pa[1], pb[1][:512])

@@ -49,6 +49,8 @@ MUTANTS = {
     "swiglu_gate_up_halves_swapped": ("const double g = (double)bf16_value(row[j]);\n            const double u = (double)bf16_value(row[inter + j]);",
                                       "const double u = (double)bf16_value(row[j]);\n            const double g = (double)bf16_value(row[inter + j]);"),
     "swiglu_drops_up": ("h[t * inter + j] = g / (1.0 + exp(-g)) * u;", "h[t * inter + j] = g / (1.0 + exp(-g));"),
+    "pertensor_keeps_row_amax": ("        if (per_tensor)\n            amax = tensor_amax;\n", ""),
+    "pertensor_amax_of_first_row": ("for (int64_t i = 0; i < rows * k; ++i)", "for (int64_t i = 0; i < k; ++i)"),
     "swiglu_bwd_reads_up_as_gate": ("const double g = (double)bf16_value(y_gu[t * 2 * inter + j]);",
                                     "const double g = (double)bf16_value(y_gu[t * 2 * inter + inter + j]);"),
     "swiglu_bwd_drops_sigma_derivative": ("d * u * (s + g * s * (1.0 - s))", "d * u * s"),
