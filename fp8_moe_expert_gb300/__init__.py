@@ -18,6 +18,7 @@ LIBRARY = os.path.join(HERE, "libfme.so")
 ROWWISE = 0
 COLWISE = 1
 MAX_GROUPS = 1024
+MX_SCALE_CEIL = 0x100
 DEV_TIMEOUT = 0x1
 DEV_BAD_OFFSETS = 0x2
 DEV_BAD_INDEX = 0x4
@@ -254,7 +255,7 @@ def quantize_mxfp8(x, axis=ROWWISE, offsets=None, num_groups=None, *, codes=None
     rows, cols = x.shape
     offsets, g = _groups(offsets, num_groups)
     dev = x.device
-    if axis == ROWWISE:
+    if (axis & ~MX_SCALE_CEIL) == ROWWISE:
         if codes is None:
             codes = _empty((rows, cols), torch.uint8, dev)
         if sf is None:

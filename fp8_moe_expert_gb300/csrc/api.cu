@@ -383,6 +383,8 @@ fme_status moe_combine(const void *y, int64_t rows_y, const int32_t *row_of, con
 fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axis, const int32_t *offsets,
                           int32_t num_groups, uint8_t *codes, uint8_t *sf, int32_t *padded_offsets,
                           int32_t *dev_status, void *stream) {
+  const bool ceil_scale = (axis & FME_MX_SCALE_CEIL) != 0;
+  axis &= ~FME_MX_SCALE_CEIL;
   if (rows < 0 || check_groups(num_groups) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
   if (offsets == nullptr && num_groups != 1) return FME_ERR_INVALID_ARGUMENT;
   if (axis != FME_ROWWISE && axis != FME_COLWISE) return FME_ERR_INVALID_ARGUMENT;
@@ -403,6 +405,7 @@ fme_status quantize_mxfp8(const void *x, int64_t rows, int64_t cols, int32_t axi
   if (st != FME_OK) return st;
   fme::LaunchMxfp8 a{x, rows, cols, offsets, num_groups, codes, sf, padded_offsets,
                      fme_colwise_ld(rows, num_groups), dev_status, sms, static_cast<cudaStream_t>(stream)};
+  a.ceil_scale = ceil_scale;
   cudaError_t err =
       (axis == FME_ROWWISE) ? fme::launch_quantize_mxfp8_rows(a) : fme::launch_quantize_mxfp8_cols(a);
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_mxfp8 launch");

@@ -70,6 +70,7 @@ struct LaunchMxfp8 {
   // [rows x cols/2], optional bf16 d(gate/up) out [rows x cols].
   const void *dh = nullptr;
   void *d_out = nullptr;
+  bool ceil_scale = false;  // row-wise / column-wise only: X = 2^ceil(log2(amax / 448))
 };
 
 enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2, kFwdMxfp8 = 3 };

@@ -25,6 +25,20 @@ __device__ __forceinline__ uint32_t mx_code_from_bf16_amax(uint32_t amax_bits) {
   return static_cast<uint32_t>(e > 8 ? e - 8 : 0);
 }
 
+// The round-up scale variant X = 2^ceil(log2(amax / 448)) (no element saturates):
+// with 448 = 1.75 * 2^8 that is the exponent field minus 8, plus one when the
+// significand is above 1.75 (fraction bits above 0x60); clamped at 0.
+__device__ __forceinline__ uint32_t mx_code_ceil_from_bf16_amax(uint32_t amax_bits) {
+  const int e = static_cast<int>((amax_bits >> 7) & 0xFF);
+  const int c = e - 8 + ((amax_bits & 0x7Fu) > 0x60u ? 1 : 0);
+  return static_cast<uint32_t>(c > 0 ? c : 0);
+}
+
+template <bool kCeil>
+__device__ __forceinline__ uint32_t mx_code(uint32_t amax_bits) {
+  return kCeil ? mx_code_ceil_from_bf16_amax(amax_bits) : mx_code_from_bf16_amax(amax_bits);
+}
+
 __device__ __forceinline__ float rcp_fast(float v) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
@@ -104,6 +118,7 @@ __device__ __forceinline__ uint32_t e4m3x4_words(uint32_t a, uint32_t b, float s
 // outside [0, gather_limit) is reported and reads source row 0.
 constexpr int kRowUnroll = 4;
 
+template <bool kCeil>
 __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
                                                          const int32_t *__restrict__ offsets, int num_groups,
                                                          uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
@@ -147,7 +162,7 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
         uint32_t bmax = max(bm & 0x7FFFu, (bm >> 16) & 0x7FFFu);
         bmax = max(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
         bmax = max(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 2));
-        const uint32_t code = mx_code_from_bf16_amax(bmax);
+        const uint32_t code = mx_code<kCeil>(bmax);
         const float s = mx_inv_scale(code);
         uint2 out;
         out.x = e4m3x4_words(v[u].x, v[u].y, s);
@@ -209,7 +224,7 @@ __device__ __forceinline__ void col_tile_locate(ColTile &t, const GroupTable &gr
 // tile's halves land in different 128-column blocks of the outputs.
 enum ColMode { kColsOnly = 0, kRowCol = 1, kSwiGLUBwd = 2 };
 
-template <int kMode>
+template <int kMode, bool kCeil>
 __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
                                                          const int32_t *__restrict__ offsets, int num_groups,
                                                          uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
@@ -327,8 +342,8 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
         vals[i] = *reinterpret_cast<const uint32_t *>(&tile[32 * b + i][2 * cp]);
         m = absmax_bf16x2(m, vals[i]);
       }
-      const uint32_t code_lo = mx_code_from_bf16_amax(m & 0x7FFFu);
-      const uint32_t code_hi = mx_code_from_bf16_amax((m >> 16) & 0x7FFFu);
+      const uint32_t code_lo = mx_code<kCeil>(m & 0x7FFFu);
+      const uint32_t code_hi = mx_code<kCeil>((m >> 16) & 0x7FFFu);
       const float s_lo = mx_inv_scale(code_lo);
       const float s_hi = mx_inv_scale(code_hi);
       uint32_t wl[8], wh[8];
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
         uint32_t m = 0;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) m = absmax_bf16x2(m, absmax_bf16x2(w[i], w[i + 1]));
-        const uint32_t code = mx_code_from_bf16_amax(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
+        const uint32_t code = mx_code<kCeil>(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
         const float s = mx_inv_scale(code);
         uint32_t words[8];
 #pragma unroll
@@ -443,30 +458,33 @@ cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a) {
   const int64_t need = (a.rows + 7) / 8;
   const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
   const int blocks = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
-  mxfp8_rows_kernel<<<blocks, threads, 0, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows,
-                                                       static_cast<int>(a.cols), a.offsets, a.num_groups,
-                                                       a.codes, a.sf, a.status, a.gather, a.gather_div,
-                                                       a.gather_limit);
+  auto kernel = a.ceil_scale ? mxfp8_rows_kernel<true> : mxfp8_rows_kernel<false>;
+  kernel<<<blocks, threads, 0, a.stream>>>(static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.cols),
+                                           a.offsets, a.num_groups, a.codes, a.sf, a.status, a.gather,
+                                           a.gather_div, a.gather_limit);
   return cudaGetLastError();
 }
 
-template <int kMode>
+template <int kMode, bool kCeil = false>
 static cudaError_t launch_cols(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
   const int threads = 256;
   const int64_t tiles = (a.ld / 128) * (a.cols / 128);  // kSwiGLUBwd: inter / 64 = cols / 128 column blocks
   const int64_t cap = static_cast<int64_t>(a.num_sms) * 2;
   const int blocks = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
-  cudaError_t err = cudaFuncSetAttribute(mxfp8_cols_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kColSmemBytes);
+  auto kernel = mxfp8_cols_kernel<kMode, kCeil>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kColSmemBytes);
   if (err != cudaSuccess) return err;
-  mxfp8_cols_kernel<kMode><<<blocks, threads, kColSmemBytes, a.stream>>>(
+  kernel<<<blocks, threads, kColSmemBytes, a.stream>>>(
       static_cast<const uint16_t *>(a.x), a.rows, static_cast<int>(a.cols), a.offsets, a.num_groups, a.codes, a.sf,
       a.ld, a.padded_offsets, row_codes, row_sf, a.status, static_cast<const uint16_t *>(a.dh),
       static_cast<uint16_t *>(a.d_out));
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a) { return launch_cols<kColsOnly>(a, nullptr, nullptr); }
+cudaError_t launch_quantize_mxfp8_cols(const LaunchMxfp8 &a) {
+  return a.ceil_scale ? launch_cols<kColsOnly, true>(a, nullptr, nullptr)
+                      : launch_cols<kColsOnly, false>(a, nullptr, nullptr);
+}
 
 cudaError_t launch_quantize_mxfp8_rowcol(const LaunchMxfp8 &a, uint8_t *row_codes, uint8_t *row_sf) {
   return launch_cols<kRowCol>(a, row_codes, row_sf);

@@ -95,6 +95,8 @@ typedef int32_t fme_status;
 
 #define FME_ROWWISE 0
 #define FME_COLWISE 1
+/* OR-ed into quantize_mxfp8's axis: the round-up scale variant (see there). */
+#define FME_MX_SCALE_CEIL 0x100
 
 #define FME_MAX_GROUPS 1024
 
@@ -270,6 +272,10 @@ fme_status moe_combine(const void *y, int64_t rows_y, const int32_t *row_of, con
  * q = E4M3(x / X), round to nearest even, saturating at 448.  X is a power of
  * two, so x / X is exact and the fast division the pages allow for MXFP8 gives
  * the same codes.
+ *
+ * axis | FME_MX_SCALE_CEIL: the round-up scale variant, X = 2^ceil(log2(amax /
+ * 448)) (code clamp(ceil(log2(amax / 448)) + 127, 0, 254)), the smallest power of
+ * two that keeps every |x / X| <= 448, so no element saturates.  Layouts as below.
  *
  * axis = FME_ROWWISE: blocks run along each row of x [rows x cols].
  *   cols a multiple of 32, 32 <= cols <= 65536.

@@ -80,6 +80,8 @@ def _declare(lib):
     lib.fme_orc_dequant_nvfp4.argtypes = [P, P, P, I64, I64, P]
     lib.fme_orc_quant_mxfp8_rows.argtypes = [P, I64, I64, P, P]
     lib.fme_orc_quant_mxfp8_cols.argtypes = [P, I64, I64, P, I32, I64, P, P, P]
+    lib.fme_orc_quant_mxfp8_rows_ceil.argtypes = [P, I64, I64, P, P]
+    lib.fme_orc_quant_mxfp8_cols_ceil.argtypes = [P, I64, I64, P, I32, I64, P, P, P]
     lib.fme_orc_dequant_mxfp8.argtypes = [P, P, I64, I64, P]
     lib.fme_orc_gemm_abt.argtypes = [P, P, I64, I64, I64, P]
     lib.fme_orc_swiglu.argtypes = [P, I64, I64, P]
@@ -89,7 +91,7 @@ def _declare(lib):
     for name in ("fme_orc_e2m1_encode_array", "fme_orc_e4m3_encode_array", "fme_orc_quant_nvfp4",
                  "fme_orc_dequant_nvfp4", "fme_orc_quant_mxfp8_rows", "fme_orc_quant_mxfp8_cols",
                  "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt", "fme_orc_swiglu", "fme_orc_route", "fme_orc_swiglu_bwd",
-                 "fme_orc_quant_nvfp4_pertensor",
+                 "fme_orc_quant_nvfp4_pertensor", "fme_orc_quant_mxfp8_rows_ceil", "fme_orc_quant_mxfp8_cols_ceil",
                  "fme_orc_combine"):
         getattr(lib, name).restype = None
     return lib
@@ -170,18 +172,20 @@ class Oracle:
         self.lib.fme_orc_dequant_nvfp4(_p(codes), _p(sf), _p(scale), rows, 2 * half, _p(out))
         return out
 
-    def quant_mxfp8_rows(self, x_bits):
-        """-> codes [rows, cols] uint8 (E4M3), sf [rows, cols/32] uint8 (E8M0)."""
+    def quant_mxfp8_rows(self, x_bits, ceil_scale: bool = False):
+        """-> codes [rows, cols] uint8 (E4M3), sf [rows, cols/32] uint8 (E8M0).
+        ``ceil_scale``: the round-up scale rule X = 2^ceil(log2(amax / 448))."""
         x = _bits(x_bits)
         rows, cols = x.shape
         if cols % 32:
             raise ValueError("cols must be a multiple of 32")
         codes = np.zeros((rows, cols), np.uint8)
         sf = np.zeros((rows, cols // 32), np.uint8)
-        self.lib.fme_orc_quant_mxfp8_rows(_p(x), rows, cols, _p(codes), _p(sf))
+        fn = self.lib.fme_orc_quant_mxfp8_rows_ceil if ceil_scale else self.lib.fme_orc_quant_mxfp8_rows
+        fn(_p(x), rows, cols, _p(codes), _p(sf))
         return codes, sf
 
-    def quant_mxfp8_cols(self, x_bits, offsets, ld: int | None = None):
+    def quant_mxfp8_cols(self, x_bits, offsets, ld: int | None = None, ceil_scale: bool = False):
         """Column-wise MXFP8 over row groups.
 
         -> codes_t [cols, ld] uint8, sf_t [cols, ld/32] uint8, poff [G+1] int32.
@@ -201,7 +205,8 @@ class Oracle:
         codes = np.zeros((cols, ld), np.uint8)
         sf = np.zeros((cols, ld // 32), np.uint8)
         poff = np.zeros(g + 1, np.int32)
-        self.lib.fme_orc_quant_mxfp8_cols(_p(x), rows, cols, _p(offsets), g, ld, _p(codes), _p(sf), _p(poff))
+        fn = self.lib.fme_orc_quant_mxfp8_cols_ceil if ceil_scale else self.lib.fme_orc_quant_mxfp8_cols
+        fn(_p(x), rows, cols, _p(offsets), g, ld, _p(codes), _p(sf), _p(poff))
         return codes, sf, poff
 
     def dequant_mxfp8(self, codes, sf) -> np.ndarray:

@@ -295,17 +295,31 @@ static uint8_t mx_scale_code(float amax) {
     return (uint8_t)code;
 }
 
+/* The round-up scale rule (a variant, not the standard's): X = 2^ceil(log2(amax
+ * / 448)), the smallest power of two with amax / X <= 448, so no element
+ * saturates.  E8M0 code clamped to [0, 254]; an all-zero block gets code 0. */
+static uint8_t mx_scale_code_ceil(float amax) {
+    if (!(amax > 0.0f))
+        return 0;
+    int e2;
+    const double m = frexp((double)amax / 448.0, &e2); /* amax/448 = m * 2^e2, m in [0.5, 1) */
+    const int up = (m == 0.5) ? e2 - 1 : e2;            /* ceil(log2(amax / 448)) */
+    const int c = up + 127;
+    return (uint8_t)(c < 0 ? 0 : (c > 254 ? 254 : c));
+}
+
 /* Quantize one block of n (<= 32) values given as floats; missing values of a
- * short block count as zeros and are not written. */
+ * short block count as zeros and are not written.  ceil_rule selects the
+ * round-up scale instead of the standard one. */
 static void mx_block(const float *v, int n, uint8_t *codes_out, int64_t code_stride,
-                     uint8_t *scale_out) {
+                     uint8_t *scale_out, int ceil_rule) {
     float amax = 0.0f;
     for (int j = 0; j < n; ++j) {
         float a = fabsf(v[j]);
         if (a > amax)
             amax = a;
     }
-    uint8_t sc = mx_scale_code(amax);
+    uint8_t sc = ceil_rule ? mx_scale_code_ceil(amax) : mx_scale_code(amax);
     *scale_out = sc;
     for (int j = 0; j < n; ++j) {
         double q = ldexp((double)v[j], 127 - (int)sc); /* x / X, exact */
@@ -318,14 +332,14 @@ static void mx_block(const float *v, int n, uint8_t *codes_out, int64_t code_str
  * (cols a multiple of 32).  codes [rows x cols] E4M3, sf [rows x cols/32]
  * E8M0, logical layouts.
  */
-void fme_orc_quant_mxfp8_rows(const uint16_t *x, int64_t rows, int64_t cols,
-                              uint8_t *codes, uint8_t *sf) {
+static void quant_mxfp8_rows(const uint16_t *x, int64_t rows, int64_t cols, int ceil_rule,
+                             uint8_t *codes, uint8_t *sf) {
     float v[32];
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t b = 0; b < cols / 32; ++b) {
             for (int j = 0; j < 32; ++j)
                 v[j] = bf16_value(x[r * cols + b * 32 + j]);
-            mx_block(v, 32, codes + r * cols + b * 32, 1, sf + r * (cols / 32) + b);
+            mx_block(v, 32, codes + r * cols + b * 32, 1, sf + r * (cols / 32) + b, ceil_rule);
         }
     }
 }
@@ -343,9 +357,9 @@ void fme_orc_quant_mxfp8_rows(const uint16_t *x, int64_t rows, int64_t cols,
  * ld (a multiple of 128, at least poff[num_groups]) is the row length of the
  * outputs; positions from poff[num_groups] to ld are written as zeros.
  */
-void fme_orc_quant_mxfp8_cols(const uint16_t *x, int64_t rows, int64_t cols,
-                              const int32_t *offsets, int32_t num_groups, int64_t ld,
-                              uint8_t *codes_t, uint8_t *sf_t, int32_t *poff) {
+static void quant_mxfp8_cols(const uint16_t *x, int64_t rows, int64_t cols,
+                             const int32_t *offsets, int32_t num_groups, int64_t ld, int ceil_rule,
+                             uint8_t *codes_t, uint8_t *sf_t, int32_t *poff) {
     (void)rows;
     float v[32];
     memset(codes_t, 0, (size_t)(cols * ld));
@@ -361,12 +375,36 @@ void fme_orc_quant_mxfp8_cols(const uint16_t *x, int64_t rows, int64_t cols,
                     int64_t local = pb + j;
                     v[j] = (local < n_g) ? bf16_value(x[(offsets[g] + local) * cols + c]) : 0.0f;
                 }
-                mx_block(v, 32, codes_t + c * ld + p0 + pb, 1, sf_t + c * (ld / 32) + (p0 + pb) / 32);
+                mx_block(v, 32, codes_t + c * ld + p0 + pb, 1, sf_t + c * (ld / 32) + (p0 + pb) / 32,
+                         ceil_rule);
             }
         }
         p0 += padded;
     }
     poff[num_groups] = (int32_t)p0;
+}
+
+void fme_orc_quant_mxfp8_rows(const uint16_t *x, int64_t rows, int64_t cols,
+                              uint8_t *codes, uint8_t *sf) {
+    quant_mxfp8_rows(x, rows, cols, 0, codes, sf);
+}
+
+void fme_orc_quant_mxfp8_cols(const uint16_t *x, int64_t rows, int64_t cols,
+                              const int32_t *offsets, int32_t num_groups, int64_t ld,
+                              uint8_t *codes_t, uint8_t *sf_t, int32_t *poff) {
+    quant_mxfp8_cols(x, rows, cols, offsets, num_groups, ld, 0, codes_t, sf_t, poff);
+}
+
+/* The same two quantizers with the round-up scale rule. */
+void fme_orc_quant_mxfp8_rows_ceil(const uint16_t *x, int64_t rows, int64_t cols,
+                                   uint8_t *codes, uint8_t *sf) {
+    quant_mxfp8_rows(x, rows, cols, 1, codes, sf);
+}
+
+void fme_orc_quant_mxfp8_cols_ceil(const uint16_t *x, int64_t rows, int64_t cols,
+                                   const int32_t *offsets, int32_t num_groups, int64_t ld,
+                                   uint8_t *codes_t, uint8_t *sf_t, int32_t *poff) {
+    quant_mxfp8_cols(x, rows, cols, offsets, num_groups, ld, 1, codes_t, sf_t, poff);
 }
 
 /* x_hat = dec_E4M3(q) * 2^(scale - 127) for blocks of 32 along each row of a

@@ -426,6 +426,52 @@ def check_swiglu_vs_scipy(orc):
     assert np.allclose(h, want, rtol=4e-16, atol=1e-300)
 
 
+def check_mxfp8_ceil_scale_brute_force(orc):
+    """Round-up scale rule on every positive finite bf16 amax (one 32-block per
+    value, the amax in the block's first element): the code is the smallest c
+    with amax <= 448 * 2^(c - 127), found by search, clamped at 0; no element
+    saturates (every E4M3 code decodes to at most 448 in magnitude, exact x / X
+    below 448 is the torch float8_e4m3fn cast); the code is the standard rule's or
+    one more."""
+    import torch
+
+    bits = _all_bf16_finite()
+    vals = synth.bf16_float(bits).astype(np.float64)
+    pos = bits[vals > 0]
+    pv = synth.bf16_float(pos).astype(np.float64)
+    x = np.zeros((len(pos), 32), np.uint16)
+    x[:, 0] = pos
+    x[:, 1] = synth.bf16_bits(-synth.bf16_float(pos) * np.float32(0.75))
+    codes, sf = orc.quant_mxfp8_rows(x, ceil_scale=True)
+    c = np.zeros(len(pos), np.int64)
+    for k in range(256):                     # c ends as the first k with pv <= 448 * 2^(k-127)
+        c[pv > 448.0 * 2.0 ** (k - 127)] = k + 1
+    assert np.array_equal(sf[:, 0].astype(np.int64), c)
+    _, sf_std = orc.quant_mxfp8_rows(x)
+    d = sf[:, 0].astype(np.int64) - sf_std[:, 0].astype(np.int64)
+    assert np.all((d == 0) | (d == 1))
+    q = synth.bf16_float(x[:, :2]).astype(np.float64) / np.ldexp(1.0, sf[:, :1].astype(np.int64) - 127)
+    assert np.all(np.abs(q) <= 448.0)
+    want = torch.from_numpy(q.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes[:, :2], want)
+
+
+def check_mxfp8_ceil_scale_worked(orc):
+    """Worked values: amax 448 -> code 127 (X = 1); 450 -> 128; 3.0 -> 120 (as the
+    standard rule); 3.75 -> 121 where the standard rule's 120 saturates 3.75 * 128
+    = 480 to 448; the column-wise quantizer follows the same rule along tokens."""
+    x = np.zeros((4, 32), np.float32)
+    x[0, 3], x[1, 0], x[2, 5], x[3, 31] = 448.0, -450.0, 3.0, 3.75
+    xb = synth.bf16_bits(x)
+    codes, sf = orc.quant_mxfp8_rows(xb, ceil_scale=True)
+    assert sf[:, 0].tolist() == [127, 128, 120, 121]
+    assert orc.e4m3_value(codes[3, 31:32])[0] == 240.0
+    _, sf_std = orc.quant_mxfp8_rows(xb)
+    assert sf_std[3, 0] == 120
+    ct, st, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(xb.T), np.array([0, 32]), ceil_scale=True)
+    assert st[:, 0].tolist() == [127, 128, 120, 121]
+
+
 def check_nvfp4_pertensor_special_cases(orc):
     """Standard NVFP4 is the per-token variant when the tensor is one row, or when
     every row has the tensor's amax; its scale is fl32(amax_tensor / 2688) (numpy

@@ -113,6 +113,9 @@ def test_host_argument_checks(lib):
     assert sb(good, None, 10, 256, None, 1, good, good, good, good, good, None, None, _stream()) == 1   # dh
     assert sb(good, good, 10, 256, None, 1, good, good, good, good, None, None, None, _stream()) == 1  # padded
     assert sb(good, good, 10, 256, None, 1, good, good, good, good, good, odd, None, _stream()) == 2   # d out
+    assert m(good, 10, 256, 0x102, None, 1, good, good, None, None, _stream()) == 1   # ceil flag, bad axis
+    assert m(good, 10, 96, 0x101, None, 1, good, good, good, None, _stream()) == 3   # ceil, column-wise cols % 128
+    assert m(good, 10, 48, 0x100, None, 1, good, good, None, None, _stream()) == 3   # ceil, row-wise cols % 32
     f = lib.grouped_gemm_fwd_nvfp4
     assert f(good, good, good, good, good, good, good, 4, 100, 100, 256, good, None, _stream()) == 3
     assert f(good, good, good, good, good, good, good, 4, 100, 256, 100, good, None, _stream()) == 3

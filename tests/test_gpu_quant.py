@@ -362,3 +362,43 @@ def test_nvfp4_pertensor_batch_variance_on_gpu(fme):
     assert not np.array_equal(a[0], b[0][:512])
     pa, pb = run_nvfp4(fme, x), run_nvfp4(fme, both)
     assert np.array_equal(pa[0], pb[0][:512]) and np.array_equal(pa[1], pb[1][:512])
+
+
+# ------------------------------------------------ MXFP8, round-up scale rule --
+def test_mxfp8_ceil_rows_and_cols(fme, orc):
+    """Both quantizers with FME_MX_SCALE_CEIL against the oracle's round-up rule,
+    on the heterogeneous batch (ragged groups for the column-wise one)."""
+    off = synth.offsets_from_counts([300, 0, 129, 1, 594])
+    x, _, _ = synth.quantizer_batch(rows=int(off[-1]), cols=1024, seed=12)
+    st = _status()
+    codes, sf = fme.quantize_mxfp8(bf16_tensor(x), fme.ROWWISE | fme.MX_SCALE_CEIL, _dev_offsets(off), status=st)
+    ct, cs, poff, ld = fme.quantize_mxfp8(bf16_tensor(x), fme.COLWISE | fme.MX_SCALE_CEIL, _dev_offsets(off),
+                                         status=st)
+    assert fme.read_device_status(st)[0] == 0
+    oc, osf = orc.quant_mxfp8_rows(x, ceil_scale=True)
+    assert np.array_equal(to_np(codes), oc)
+    assert np.array_equal(unswizzle(to_np(sf), x.shape[0], 1024 // 32, off), osf)
+    occ, ocs, opoff = orc.quant_mxfp8_cols(x, off, ld=ld, ceil_scale=True)
+    p = int(opoff[-1])
+    assert np.array_equal(to_np(poff), opoff)
+    assert np.array_equal(to_np(ct)[:, :p], occ[:, :p])
+    assert np.array_equal(unswizzle(to_np(cs), 1024, ld // 32)[:, : p // 32], ocs[:, : p // 32])
+    # the standard rule differs from it somewhere on this batch
+    std, _ = fme.quantize_mxfp8(bf16_tensor(x), fme.ROWWISE, _dev_offsets(off), status=st)
+    assert not np.array_equal(to_np(std), to_np(codes))
+
+
+def test_mxfp8_ceil_every_bf16_amax(fme, orc):
+    """Every positive finite bf16 value as a block's amax (with a -0.75x partner)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = synth.bf16_float(bits)
+    pos = bits[np.isfinite(vals) & (vals > 0)]
+    x = np.zeros((len(pos), 32), np.uint16)
+    x[:, 0] = pos
+    x[:, 9] = synth.bf16_bits(-synth.bf16_float(pos) * np.float32(0.75))
+    st = _status()
+    codes, sf = fme.quantize_mxfp8(bf16_tensor(x), fme.ROWWISE | fme.MX_SCALE_CEIL, status=st)
+    assert fme.read_device_status(st)[0] == 0
+    oc, osf = orc.quant_mxfp8_rows(x, ceil_scale=True)
+    assert np.array_equal(unswizzle(to_np(sf), len(pos), 1), osf)
+    assert np.array_equal(to_np(codes), oc)

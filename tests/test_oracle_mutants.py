@@ -49,6 +49,9 @@ MUTANTS = {
     "swiglu_gate_up_halves_swapped": ("const double g = (double)bf16_value(row[j]);\n            const double u = (double)bf16_value(row[inter + j]);",
                                       "const double u = (double)bf16_value(row[j]);\n            const double g = (double)bf16_value(row[inter + j]);"),
     "swiglu_drops_up": ("h[t * inter + j] = g / (1.0 + exp(-g)) * u;", "h[t * inter + j] = g / (1.0 + exp(-g));"),
+    "mx_ceil_ignores_exact_powers": ("const int up = (m == 0.5) ? e2 - 1 : e2;", "const int up = e2;"),
+    "mx_ceil_is_floor": ("const int up = (m == 0.5) ? e2 - 1 : e2;", "const int up = e2 - 1;"),
+    "mx_ceil_divides_by_256": ("frexp((double)amax / 448.0, &e2);", "frexp((double)amax / 256.0, &e2);"),
     "pertensor_keeps_row_amax": ("        if (per_tensor)\n            amax = tensor_amax;\n", ""),
     "pertensor_amax_of_first_row": ("for (int64_t i = 0; i < rows * k; ++i)", "for (int64_t i = 0; i < k; ++i)"),
     "swiglu_bwd_reads_up_as_gate": ("const double g = (double)bf16_value(y_gu[t * 2 * inter + j]);",
