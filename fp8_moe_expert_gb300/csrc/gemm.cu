@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) pair::arrive_remote(leader_acc_empty);
+      if (lane == 0) pair::arrive_remote_relaxed(leader_acc_empty);  // registers hold the data
       acc_phase ^= 1;
       if (K == GemmKind::kFwdNvfp4) {
         reinterpret_cast<float4 *>(sw)[lane] = swv;
