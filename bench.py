@@ -409,7 +409,16 @@ def run_extras(step, args, bf16_sus):
         out[name] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac_fp8": round(ach / (bf16_sus * 2), 3)}
     del xq, wq, hq, wdq
     out.update(run_routing_extras(step, args, hbm))
-    out.update(run_gate_up_bwd_extras(step, args, hbm, bf16_sus))
+    # the down projection's wgrad added into an fp32 gradient buffer (accumulation)
+    acc = torch.zeros((E, H, I), dtype=torch.float32, device=step.dev)
+    ms = _time_call(lambda: f.grouped_gemm_wgrad_mxfp8_accumulate(step.dyc[0], step.dyc[1], step.ld_r, step.hc[0],
+                                                                  step.hc[1], step.ld_r, step.dyc[2], H, I, acc,
+                                                                  status=st), args.steps)
+    ach = 2 * R * H * I / (ms * 1e-3) / 1e12
+    out["gemm_wgrad_accumulate_fp32"] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1),
+                                         "frac_fp8": round(ach / (bf16_sus * 2), 3)}
+    del acc
+    out.update(run_gate_up_bwd_extras(step, args, hbm, bf16_sus))  # reuses the dY column-wise buffers
     return out
 
 

@@ -81,6 +81,8 @@ SYMBOLS = {
     "permute_quantize_nvfp4": ("i32", ["p", "i64", "i64", "p", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
     "permute_quantize_mxfp8": ("i32", ["p", "i64", "i64", "p", "i32", "p", "i32", "p", "p", "p", "p"]),
     "moe_combine": ("i32", ["p", "i64", "p", "p", "i64", "i32", "i64", "p", "p", "p"]),
+    "grouped_gemm_wgrad_mxfp8_accumulate": ("i32", ["p", "p", "i64", "p", "p", "i64", "p", "i32", "i64", "i64", "p",
+                                                    "p", "p"]),
     "fme_route_workspace_bytes": ("i64", ["i64", "i32", "i32"]),
     "fme_sf_padded_rows": ("i64", ["i64", "i32"]),
     "fme_sf_bytes": ("i64", ["i64", "i64", "i32", "i32"]),
@@ -483,6 +485,17 @@ def moe_combine(y, row_of, weights, *, out=None, status=None, stream=None):
                            _stream(stream))
     _check(st, "moe_combine")
     return out
+
+
+def grouped_gemm_wgrad_mxfp8_accumulate(a_codes, a_sf, lda, b_codes, b_sf, ldb, padded_offsets, m, n, dw_acc, *,
+                                        status=None, stream=None):
+    """dw_acc [E, m, n] (fp32) += dY_e^T H_e, the wgrad's fp32 result per expert."""
+    e = padded_offsets.numel() - 1
+    st = lib().grouped_gemm_wgrad_mxfp8_accumulate(_ptr(a_codes), _ptr(a_sf), lda, _ptr(b_codes), _ptr(b_sf), ldb,
+                                                   _ptr(padded_offsets), e, m, n, _ptr(dw_acc), _ptr(status),
+                                                   _stream(stream))
+    _check(st, "grouped_gemm_wgrad_mxfp8_accumulate")
+    return dw_acc
 
 
 def read_device_status(status, stream=None) -> tuple[int, int]:

@@ -583,10 +583,10 @@ fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_dgrad_mxfp8 launch");
 }
 
-fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda,
-                                    const uint8_t *b_codes, const uint8_t *b_sf, int64_t ldb,
-                                    const int32_t *padded_offsets, int32_t num_experts, int64_t m, int64_t n,
-                                    void *y, int32_t *dev_status, void *stream) {
+static fme_status wgrad_call(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda, const uint8_t *b_codes,
+                             const uint8_t *b_sf, int64_t ldb, const int32_t *padded_offsets, int32_t num_experts,
+                             int64_t m, int64_t n, void *y, bool accumulate, int32_t *dev_status, void *stream,
+                             const char *what) {
   if (m < 0 || n < 0 || lda < 0 || ldb < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
   if (m % 256 != 0 || m == 0 || n % 256 != 0 || n == 0 || lda % 128 != 0 || ldb % 128 != 0)
     return FME_ERR_UNSUPPORTED_SHAPE;
@@ -626,11 +626,28 @@ fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
   a.lda = lda;
   a.ldb = ldb;
   a.y = y;
+  a.accumulate = accumulate;
   a.status = dev_status;
   a.num_sms = sms;
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t err = fme::launch_grouped_gemm(a);
-  return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_wgrad_mxfp8 launch");
+  return err == cudaSuccess ? FME_OK : cuda_fail(err, what);
+}
+
+fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda,
+                                    const uint8_t *b_codes, const uint8_t *b_sf, int64_t ldb,
+                                    const int32_t *padded_offsets, int32_t num_experts, int64_t m, int64_t n,
+                                    void *y, int32_t *dev_status, void *stream) {
+  return wgrad_call(a_codes, a_sf, lda, b_codes, b_sf, ldb, padded_offsets, num_experts, m, n, y, false, dev_status,
+                    stream, "grouped_gemm_wgrad_mxfp8 launch");
+}
+
+fme_status grouped_gemm_wgrad_mxfp8_accumulate(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda,
+                                               const uint8_t *b_codes, const uint8_t *b_sf, int64_t ldb,
+                                               const int32_t *padded_offsets, int32_t num_experts, int64_t m,
+                                               int64_t n, float *dw_acc, int32_t *dev_status, void *stream) {
+  return wgrad_call(a_codes, a_sf, lda, b_codes, b_sf, ldb, padded_offsets, num_experts, m, n, dw_acc, true,
+                    dev_status, stream, "grouped_gemm_wgrad_mxfp8_accumulate launch");
 }
 
 }  // extern "C"

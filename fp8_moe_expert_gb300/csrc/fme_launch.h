@@ -89,6 +89,7 @@ struct LaunchGemm {
   int num_sms;
   int stages;  // operand ring depth, set by launch_grouped_gemm
   cudaStream_t stream;
+  bool accumulate = false;  // wgrad only: y is fp32 and receives y += result
 };
 
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a);

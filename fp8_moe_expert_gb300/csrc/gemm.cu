@@ -512,8 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       const Tile tl = tile_at<K>(p, grp, t, rank);
       const bool valid = r < tl.rows_valid;
       __nv_bfloat16 *yrow = y + tl.y_off + static_cast<int64_t>(r) * p.n + c0;
-      if (tl.num_k == 0) {
-        if (valid)
+      const bool acc_out = K == GemmKind::kWgradMxfp8 && p.accumulate;
+      if (tl.num_k == 0) {  // an empty expert: dW = 0 (accumulating: nothing to add)
+        if (valid && !acc_out)
           for (int c = 0; c < kBN / 2; c += 8) *reinterpret_cast<uint4 *>(yrow + c) = make_uint4(0, 0, 0, 0);
         continue;
       }
@@ -541,6 +542,32 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       if (K == GemmKind::kFwdNvfp4) {
         reinterpret_cast<float4 *>(sw)[lane] = swv;
         __syncwarp();
+      }
+      if (acc_out) {
+        // fp32 gradient accumulation: each thread adds its row's 128 columns into
+        // y (fp32), one unfused add per element; every element has one owner
+        float *arow = static_cast<float *>(p.y) + tl.y_off + static_cast<int64_t>(r) * p.n + c0;
+        auto add_chunk = [&](const uint32_t(&v)[32], int c) {
+          float4 *d = reinterpret_cast<float4 *>(arow + 32 * c);
+          float4 o[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) o[j] = d[j];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            o[j].x = __fadd_rn(o[j].x, __uint_as_float(v[4 * j]));
+            o[j].y = __fadd_rn(o[j].y, __uint_as_float(v[4 * j + 1]));
+            o[j].z = __fadd_rn(o[j].z, __uint_as_float(v[4 * j + 2]));
+            o[j].w = __fadd_rn(o[j].w, __uint_as_float(v[4 * j + 3]));
+            d[j] = o[j];
+          }
+        };
+        if (valid) {
+          add_chunk(v0, 0);
+          add_chunk(v1, 1);
+          add_chunk(v2, 2);
+          add_chunk(v3, 3);
+        }
+        continue;
       }
       const int warp_rows = tl.rows_valid - 32 * q;  // rows of this warp's 32 that are the expert's
       if (warp_rows > 0) {

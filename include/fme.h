@@ -21,7 +21,8 @@
  *                             in the epilogue, bf16 out.
  *   grouped_gemm_fwd_mxfp8    the same product with MXFP8 operands (no per-token scale).
  *   grouped_gemm_dgrad_mxfp8  dX_e = dY_e W_e per expert, bf16 out.
- *   grouped_gemm_wgrad_mxfp8  dW_e = dY_e^T H_e per expert, bf16 out.
+ *   grouped_gemm_wgrad_mxfp8  dW_e = dY_e^T H_e per expert, bf16 out (or added into
+ *                             fp32: grouped_gemm_wgrad_mxfp8_accumulate).
  *
  * Source passages ("Composer 2 Technical Report", papercache.org summary,
  * section 6.1): the NVFP4-variant paragraph (E2M1, E4M3 per block of 16, FP32
@@ -409,6 +410,20 @@ fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
                                     const uint8_t *b_codes, const uint8_t *b_sf, int64_t ldb,
                                     const int32_t *padded_offsets, int32_t num_experts, int64_t m,
                                     int64_t n, void *y, int32_t *dev_status, void *stream);
+
+/*
+ * grouped_gemm_wgrad_mxfp8_accumulate -- the same weight gradient added into an
+ * fp32 buffer instead of written as bf16 (gradient accumulation over
+ * micro-batches): dw_acc[e, i, j] = fl32(dw_acc[e, i, j] + Y_e[i, j]), one unfused
+ * fp32 add per element, Y_e the fp32 accumulator of grouped_gemm_wgrad_mxfp8
+ * (that call's bf16 output is Y_e rounded to bf16).  Experts with no rows leave
+ * their dw_acc block untouched.  Arguments as grouped_gemm_wgrad_mxfp8, with
+ *   dw_acc   device float [num_experts x m x n], read and written
+ */
+fme_status grouped_gemm_wgrad_mxfp8_accumulate(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda,
+                                               const uint8_t *b_codes, const uint8_t *b_sf, int64_t ldb,
+                                               const int32_t *padded_offsets, int32_t num_experts, int64_t m,
+                                               int64_t n, float *dw_acc, int32_t *dev_status, void *stream);
 
 /* Rows of the padded scale layout for `rows` rows in `num_groups` groups: an
  * upper bound of 128 * sum ceil(n_g / 128) that needs no offsets. */

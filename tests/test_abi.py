@@ -163,6 +163,10 @@ def test_host_argument_checks(lib):
     assert c(good, 80, None, good, 10, 8, 256, good, None, _stream()) == 1
     assert c(good, 80, good, good, 10, 8, 256, odd, None, _stream()) == 2
     assert c(None, 0, None, None, 0, 8, 256, None, None, _stream()) == 0                  # no tokens
+    wa = lib.grouped_gemm_wgrad_mxfp8_accumulate
+    assert wa(good, good, 128, good, good, 128, good, 4, 128, 256, good, None, _stream()) == 3   # m % 256
+    assert wa(good, good, 128, good, good, 128, good, 4, 256, 256, None, None, _stream()) == 1   # no buffer
+    assert wa(good, good, 128, good, good, 128, good, 4, 256, 256, odd, None, _stream()) == 2
     assert lib.fme_read_device_status(None, _stream(), None) == 1
 
 

@@ -196,6 +196,47 @@ def test_wgrad_ragged_experts(fme, orc):
         check_gemm_tolerance(y[g], ref, what=f"wgrad expert {g}")
 
 
+def test_wgrad_accumulate_fp32(fme, orc):
+    """The fp32-accumulating wgrad: from zero it is the wgrad's fp32 result (its
+    bf16 rounding equals the bf16 wgrad bit for bit, and it is within the GEMM
+    tolerance of the oracle); a second call doubles it exactly; on a random
+    buffer it is that buffer plus the result, one binary32 add per element (numpy);
+    empty experts keep their buffer."""
+    import torch
+
+    off = synth.offsets_from_counts(COUNTS)
+    m, n = 256, 512
+    dy_bits = synth.normal_bits((int(off[-1]), m), 1e-2, seed=33)
+    h_bits = synth.normal_bits((int(off[-1]), n), 1.0, seed=34)
+    st = _status()
+    o = _i32(off)
+    a_codes, a_sf, poff, lda = fme.quantize_mxfp8(bf16_tensor(dy_bits), fme.COLWISE, o, status=st)
+    b_codes, b_sf, _, ldb = fme.quantize_mxfp8(bf16_tensor(h_bits), fme.COLWISE, o, status=st)
+    E = len(COUNTS)
+    y16 = fme.grouped_gemm_wgrad_mxfp8(a_codes, a_sf, lda, b_codes, b_sf, ldb, poff, m, n, status=st)
+    acc = torch.zeros((E, m, n), dtype=torch.float32, device="cuda")
+    fme.grouped_gemm_wgrad_mxfp8_accumulate(a_codes, a_sf, lda, b_codes, b_sf, ldb, poff, m, n, acc, status=st)
+    first = acc.clone()
+    fme.grouped_gemm_wgrad_mxfp8_accumulate(a_codes, a_sf, lda, b_codes, b_sf, ldb, poff, m, n, acc, status=st)
+    rng = np.random.default_rng(35)
+    init = rng.standard_normal((E, m, n)).astype(np.float32)
+    acc2 = torch.from_numpy(init).cuda()
+    fme.grouped_gemm_wgrad_mxfp8_accumulate(a_codes, a_sf, lda, b_codes, b_sf, ldb, poff, m, n, acc2, status=st)
+    _ok(fme, st)
+    f = to_np(first)
+    live = np.array([c > 0 for c in COUNTS])
+    assert np.array_equal(bf16_bits_np(first.to(torch.bfloat16))[live], bf16_bits_np(y16)[live])
+    assert np.array_equal(to_np(acc), 2.0 * f)
+    want = init.copy()
+    want[live] = (init[live] + f[live]).astype(np.float32)
+    assert np.array_equal(to_np(acc2), want)
+    assert not f[~live].any()
+    for g, c in enumerate(COUNTS):
+        if c:
+            ref = ref_wgrad(orc, dy_bits[off[g]:off[g + 1]], h_bits[off[g]:off[g + 1]])
+            check_gemm_tolerance(f[g].astype(np.float64), ref, what=f"accumulating wgrad expert {g}")
+
+
 def test_row_invariance_and_determinism(fme):
     """A row's forward and dgrad outputs are bit-identical when other experts'
     rows are appended (no split over K, no M-dependent reduction order), and two
