@@ -62,6 +62,22 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The slowest rank's time: an all-reduce MAX over the process group (any backend)."""
+    if world <= 1:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, flops_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's step time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def counts_for(wl):
     from fp8_moe_expert_gb300 import synth
 
@@ -280,11 +296,7 @@ def run_ours(args, rank, world, local_rank):
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     code, raw = fme.read_device_status(step.status)
     if code != 0:
         raise RuntimeError(f"device status {raw:#x} in the timed region")
@@ -293,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
                 for i, name in enumerate(MoEStep.CALLS)}
     ms_per_step = elapsed_ms / args.steps
     flops = step.gemm_flops()
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_value(world, flops, ms_per_step)
 
     peaks, peak_kind = load_peaks()
     bf16_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -601,14 +613,10 @@ def run_e2e(step, calls, args, world):
     torch.cuda.synchronize()
     for n, t in sets[0].items():
         setattr(step, n, t)
-    ms = start.elapsed_time(end) / steps
-    if world > 1:
-        t = torch.tensor([ms], device=step.dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end) / steps, world, step.dev)
     bi = sum(t.numel() * t.element_size() for t in h_in.values())
     bo = sum(t.numel() * t.element_size() for t in h_out[0].values())
-    return {"value": round(world * step.gemm_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(job_value(world, step.gemm_flops(), ms), 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "pipelined": "uploads, calls and downloads on three streams, two device buffer sets"}
 
