@@ -45,17 +45,18 @@ __device__ __forceinline__ float rcp_fast(float v) {
   return r;
 }
 
-// (dg, du) of one element: gate g, up u, upstream gradient dh.  sigma(g) and
-// sigma(-g) come from t = e^(-|g|) as (1 or t) / (1 + t), so neither is formed as
-// 1 - sigma (no cancellation for large |g|) and e^(-|g|) never overflows.
-__device__ __forceinline__ void swiglu_bwd_one(float g, float u, float dh, float &dg, float &du) {
-  const float s = __expf(-0.5f * fabsf(g));
-  const float t = s * s;
-  const float r = rcp_fast(1.0f + t);
-  const float sig = (g >= 0.0f ? 1.0f : t) * r;
-  const float sig_neg = (g >= 0.0f ? t : 1.0f) * r;
-  du = dh * (g * sig);
-  dg = (dh * u) * (sig * (1.0f + g * sig_neg));
+// (dg, du) of two elements: gate g, up u, upstream gradient dh, on the packed
+// f32x2 pipe.  sigma(g) and sigma(-g) come from t = e^(-|g|) as (1 or t) / (1 + t),
+// so neither is formed as 1 - sigma (no cancellation for large |g|) and
+// e^(-|g|) never overflows.
+__device__ __forceinline__ void swiglu_bwd_pair(float2 g, float2 u, float2 dh, float2 &dg, float2 &du) {
+  const float2 s = make_float2(__expf(-0.5f * fabsf(g.x)), __expf(-0.5f * fabsf(g.y)));
+  const float2 t = __fmul2_rn(s, s);
+  const float2 r = make_float2(rcp_fast(1.0f + t.x), rcp_fast(1.0f + t.y));
+  const float2 sig = __fmul2_rn(make_float2(g.x >= 0.0f ? 1.0f : t.x, g.y >= 0.0f ? 1.0f : t.y), r);
+  const float2 sig_neg = __fmul2_rn(make_float2(g.x >= 0.0f ? t.x : 1.0f, g.y >= 0.0f ? t.y : 1.0f), r);
+  du = __fmul2_rn(dh, __fmul2_rn(g, sig));
+  dg = __fmul2_rn(__fmul2_rn(dh, u), __fmul2_rn(sig, __ffma2_rn(g, sig_neg, make_float2(1.0f, 1.0f))));
 }
 
 // Eight elements (one 16-byte word of g, u and dh each) -> the bf16 words of dg
@@ -66,12 +67,13 @@ __device__ __forceinline__ void swiglu_bwd_uint4(const uint4 &g, const uint4 &u,
   uint32_t ow_g[4], ow_u[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float g0, u0, g1, u1;
-    swiglu_bwd_one(__uint_as_float(gw[i] << 16), __uint_as_float(uw[i] << 16), __uint_as_float(hw[i] << 16), g0, u0);
-    swiglu_bwd_one(__uint_as_float(gw[i] & 0xFFFF0000u), __uint_as_float(uw[i] & 0xFFFF0000u),
-                   __uint_as_float(hw[i] & 0xFFFF0000u), g1, u1);
-    const __nv_bfloat162 bg = __floats2bfloat162_rn(g0, g1);
-    const __nv_bfloat162 bu = __floats2bfloat162_rn(u0, u1);
+    const float2 gf = make_float2(__uint_as_float(gw[i] << 16), __uint_as_float(gw[i] & 0xFFFF0000u));
+    const float2 uf = make_float2(__uint_as_float(uw[i] << 16), __uint_as_float(uw[i] & 0xFFFF0000u));
+    const float2 hf = make_float2(__uint_as_float(hw[i] << 16), __uint_as_float(hw[i] & 0xFFFF0000u));
+    float2 dgf, duf;
+    swiglu_bwd_pair(gf, uf, hf, dgf, duf);
+    const __nv_bfloat162 bg = __floats2bfloat162_rn(dgf.x, dgf.y);
+    const __nv_bfloat162 bu = __floats2bfloat162_rn(duf.x, duf.y);
     ow_g[i] = *reinterpret_cast<const uint32_t *>(&bg);
     ow_u[i] = *reinterpret_cast<const uint32_t *>(&bu);
   }
