@@ -683,10 +683,62 @@ def oracle_sample(step, counts, rows_per_gemm, cols, rng_seed=0):
     return secs, flops, desc
 
 
+def oracle_rows_sample(step):
+    """The oracle on a small sample of each NEXT row, on one host core, in the units
+    the bench reports that row in (GB/s over the same per-row bytes; grouping in
+    million assignments per second).  Inputs are copied to the host first."""
+    import numpy as np
+
+    import oracle
+    from fp8_moe_expert_gb300 import synth
+    from tests.fmetest import bf16_bits_np
+
+    orc = oracle.Oracle()
+    H, I, E = step.H, step.I, step.E
+    rows = 64
+    gu = bf16_bits_np(step.y_gu[:rows])
+    dh = bf16_bits_np(step.dh[:rows])
+    x = bf16_bits_np(step.x[:rows])
+    y = bf16_bits_np(step.y_d[:rows * 8])
+    ids, w = synth.topk_routing(tokens=4096, top_k=8, experts=E)
+    out = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    s = timed(lambda: orc.quant_nvfp4(orc_bits(orc.swiglu(gu))))
+    out["swiglu_quantize_nvfp4"] = rows * (2 * 2 * I + 2 * I + I // 2 + I // 16 + 4) / s / 1e9
+    def swiglu_bwd_both():
+        d = orc_bits(orc.swiglu_bwd(gu, dh))
+        orc.quant_mxfp8_rows(d)
+        orc.quant_mxfp8_cols(d, np.array([0, rows]))
+
+    s = timed(swiglu_bwd_both)
+    out["swiglu_backward_quantize_mxfp8"] = rows * (2 * 2 * I + 2 * I + 2 * I + 2 * I + 2 * (2 * I // 32)) / s / 1e9
+    s = timed(lambda: orc.route(ids, E))
+    out["moe_route_massign_per_s"] = ids.size / s / 1e6
+    ro = np.arange(rows * 8, dtype=np.int32).reshape(rows, 8)
+    s = timed(lambda: orc.combine(y, ro, w[:rows]))
+    out["moe_combine"] = rows * (8 * (2 * H + 8) + 2 * H) / s / 1e9
+    s = timed(lambda: orc.quant_nvfp4_pertensor(x))
+    out["quantize_nvfp4_pertensor"] = rows * (2 * H + H // 2 + H // 16 + 4) / s / 1e9
+    return {k: round(v, 4) for k, v in out.items()}
+
+
+def orc_bits(v):
+    """fp64 values -> bf16 bit patterns (nearest even), the oracle's inputs."""
+    from fp8_moe_expert_gb300 import synth
+
+    return synth.bf16_bits(v.astype("float32"))
+
+
 def cpu_baseline(step, counts):
     secs, flops, desc = oracle_sample(step, counts, rows_per_gemm=16, cols=None)
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": desc, "seconds": round(secs, 3)}
+            "sample": desc, "seconds": round(secs, 3),
+            "next_rows_gbs": oracle_rows_sample(step)}
 
 
 def run_reference(args, rank, world, local_rank):
