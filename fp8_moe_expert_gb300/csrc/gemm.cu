@@ -544,29 +544,47 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncwarp();
       }
       if (acc_out) {
-        // fp32 gradient accumulation: each thread adds its row's 128 columns into
-        // y (fp32), one unfused add per element; every element has one owner
-        float *arow = static_cast<float *>(p.y) + tl.y_off + static_cast<int64_t>(r) * p.n + c0;
+        // fp32 gradient accumulation, one unfused add per element (each element has
+        // one owner).  Each 32 x 16 fp32 half-chunk goes through the warp's 2 KB
+        // staging block (16-byte chunk j of row r at j ^ ((r >> 1) & 3)), so that
+        // four lanes read-add-write 64 contiguous bytes of one row and an
+        // instruction covers 8 rows.
+        float *ywarp = static_cast<float *>(p.y) + tl.y_off + static_cast<int64_t>(32 * q) * p.n + c0;
         auto add_chunk = [&](const uint32_t(&v)[32], int c) {
-          float4 *d = reinterpret_cast<float4 *>(arow + 32 * c);
-          float4 o[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[j] = d[j];
+          for (int hf = 0; hf < 2; ++hf) {
+            uint8_t *row = stage_blk + lane * 64;
+            const int xs = (lane >> 1) & 3;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            o[j].x = __fadd_rn(o[j].x, __uint_as_float(v[4 * j]));
-            o[j].y = __fadd_rn(o[j].y, __uint_as_float(v[4 * j + 1]));
-            o[j].z = __fadd_rn(o[j].z, __uint_as_float(v[4 * j + 2]));
-            o[j].w = __fadd_rn(o[j].w, __uint_as_float(v[4 * j + 3]));
-            d[j] = o[j];
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4 *>(row + 16 * (j ^ xs)) =
+                  make_uint4(v[16 * hf + 4 * j], v[16 * hf + 4 * j + 1], v[16 * hf + 4 * j + 2], v[16 * hf + 4 * j + 3]);
+            __syncwarp();
+            const int j = lane & 3;
+            float4 o[4], add[4];
+            float4 *dst[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = 8 * i + (lane >> 2);
+              add[i] = *reinterpret_cast<const float4 *>(stage_blk + rr * 64 + 16 * (j ^ ((rr >> 1) & 3)));
+              dst[i] = reinterpret_cast<float4 *>(ywarp + static_cast<int64_t>(rr) * p.n + 32 * c + 16 * hf + 4 * j);
+              o[i] = *dst[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[i].x = __fadd_rn(o[i].x, add[i].x);
+              o[i].y = __fadd_rn(o[i].y, add[i].y);
+              o[i].z = __fadd_rn(o[i].z, add[i].z);
+              o[i].w = __fadd_rn(o[i].w, add[i].w);
+              *dst[i] = o[i];
+            }
+            __syncwarp();
           }
         };
-        if (valid) {
-          add_chunk(v0, 0);
-          add_chunk(v1, 1);
-          add_chunk(v2, 2);
-          add_chunk(v3, 3);
-        }
+        add_chunk(v0, 0);
+        add_chunk(v1, 1);
+        add_chunk(v2, 2);
+        add_chunk(v3, 3);
         continue;
       }
       const int warp_rows = tl.rows_valid - 32 * q;  // rows of this warp's 32 that are the expert's
