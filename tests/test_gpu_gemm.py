@@ -414,3 +414,32 @@ def test_fwd_pertensor_comparator(fme, orc):
     _ok(fme, st)
     assert not torch.equal(y_t, y_t2[:1024])
     assert torch.equal(y_p, y_p2[:1024])
+
+
+def test_many_experts_fwd_dgrad_wgrad(fme, orc):
+    """1024 experts (the ABI's maximum: the group tables take 12 KB of shared memory
+    and may shorten the operand ring), most of them empty, some with a single row;
+    checked on a sample of experts."""
+    rng = np.random.default_rng(91)
+    counts = np.zeros(1024, np.int64)
+    live = rng.choice(1024, size=40, replace=False)
+    counts[live] = rng.integers(1, 300, size=40)
+    counts[live[:3]] = 1
+    off = synth.offsets_from_counts(counts)
+    R, n, k = int(off[-1]), 256, 256
+    x_bits = synth.normal_bits((R, k), 1.0, seed=92)
+    w_bits = synth.normal_bits((1024 * n, k), 0.02, seed=93)
+    y = bf16_to_f64(gpu_fwd(fme, bf16_tensor(x_bits), bf16_tensor(w_bits), off, n, k))
+    wd_bits = synth.normal_bits((1024 * k, n), 0.02, seed=94)
+    yd = bf16_to_f64(gpu_dgrad(fme, bf16_tensor(x_bits), bf16_tensor(wd_bits), off, n, k))
+    h_bits = synth.normal_bits((R, n), 1.0, seed=95)
+    dw = bf16_to_f64(gpu_wgrad(fme, bf16_tensor(x_bits), bf16_tensor(h_bits), off))
+    for g in list(live[:6]) + [int(np.argmax(counts))]:
+        lo, hi = int(off[g]), int(off[g + 1])
+        check_gemm_tolerance(y[lo:hi], ref_fwd_rows(orc, x_bits[lo:hi], w_bits[g * n:(g + 1) * n]),
+                             what=f"many-expert fwd {g}")
+        check_gemm_tolerance(yd[lo:hi], ref_dgrad_rows(orc, x_bits[lo:hi], wd_bits[g * k:(g + 1) * k]),
+                             what=f"many-expert dgrad {g}")
+        check_gemm_tolerance(dw[g], ref_wgrad(orc, x_bits[lo:hi], h_bits[lo:hi]), what=f"many-expert wgrad {g}")
+    empty = [g for g in range(1024) if counts[g] == 0][:50]
+    assert not dw[empty].any()
