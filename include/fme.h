@@ -9,8 +9,8 @@
  *   quantize_nvfp4_weights    the same quantization of the stacked expert weights,
  *                             scales written in the forward GEMM's B-operand layout.
  *   swiglu_quantize_nvfp4     silu(gate) * up of the gate/up output, quantized as above.
- *   moe_route, permute_quantize_nvfp4, permute_quantize_mxfp8, moe_combine
- *                             grouping the routed tokens by expert (quantizing
+ *   moe_route (moe_route_noalloc), permute_quantize_nvfp4, permute_quantize_mxfp8,
+ *   moe_combine               grouping the routed tokens by expert (quantizing
  *                             them in grouped order) and combining the experts'
  *                             outputs per token.
  *   quantize_mxfp8            standard MXFP8 of the backward: E4M3 codes, one E8M0
@@ -45,11 +45,14 @@
  *   - bf16 tensors are row-major with the last dimension contiguous.  Every
  *     pointer must be 16-byte aligned.
  *   - Inputs must be finite; NaN or Inf inputs are outside the contract.
- *   - Errors the kernels detect (malformed offsets, a bounded wait that ran out)
- *     are OR-ed as FME_DEV_* bits into `dev_status`, a caller-owned device int32
- *     that the caller zeroes; dev_status may be NULL to ignore them.  A kernel
- *     that detects an error writes nothing more and returns.
- *   - Calls are thread-safe; the library keeps no per-call state.
+ *   - Errors the kernels detect (malformed offsets, an index out of range, a
+ *     bounded wait that ran out) are OR-ed as FME_DEV_* bits into `dev_status`, a
+ *     caller-owned device int32 that the caller zeroes; dev_status may be NULL to
+ *     ignore them.  A kernel that finds malformed offsets or runs out of time
+ *     writes nothing more and returns; an out-of-range index is skipped (or read
+ *     as row 0, where the call says so) and the rest of the work completes.
+ *   - Calls are thread-safe and keep no per-call state, except moe_route_noalloc,
+ *     whose counters are one static device array: its calls must be ordered.
  *
  * Grouped rows (experts)
  *   `offsets` is a device int32 array of num_groups + 1 non-decreasing prefix
