@@ -70,6 +70,22 @@ __device__ __forceinline__ uint32_t e2m1_pair_exact(uint32_t w, float e) {
   return e2m1_pair(__fdiv_rn(__uint_as_float(w << 16), e), __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), e));
 }
 
+// The E2M1 codes of four pairs (v[2i], v[2i+1]) packed as bytes 0..3 of a word,
+// the pair's first value in the byte's low nibble: four conversions into byte
+// registers and one vector move.
+__device__ __forceinline__ uint32_t e2m1_x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
 // Bytes 0..3 of a, b, c, d (each holding two codes in its low byte) as one word.
 __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
@@ -93,18 +109,24 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
 __device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float e, float r, bool normal_e) {
   constexpr float kBelow = 1.0f - 1.0f / 524288.0f;  // 1 - 2^-19, exact in fp32
   constexpr float kAbove = 1.0f + 1.0f / 524288.0f;  // 1 + 2^-19
-  uint32_t lo[8], hi[8];
+  float lo[16], hi[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float2 x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
     const float2 q = __fmul2_rn(x, make_float2(r, r));
     const float2 a = __fmul2_rn(q, make_float2(kBelow, kBelow));
     const float2 b = __fmul2_rn(q, make_float2(kAbove, kAbove));
-    lo[i] = e2m1_pair(a.x, a.y);
-    hi[i] = e2m1_pair(b.x, b.y);
+    lo[2 * i] = a.x;
+    lo[2 * i + 1] = a.y;
+    hi[2 * i] = b.x;
+    hi[2 * i + 1] = b.y;
   }
-  uint2 out = make_uint2(pack4(lo[0], lo[1], lo[2], lo[3]), pack4(lo[4], lo[5], lo[6], lo[7]));
-  const uint2 amb = make_uint2(out.x ^ pack4(hi[0], hi[1], hi[2], hi[3]), out.y ^ pack4(hi[4], hi[5], hi[6], hi[7]));
+  const float(&lo0)[8] = *reinterpret_cast<const float(*)[8]>(&lo[0]);
+  const float(&lo1)[8] = *reinterpret_cast<const float(*)[8]>(&lo[8]);
+  const float(&hi0)[8] = *reinterpret_cast<const float(*)[8]>(&hi[0]);
+  const float(&hi1)[8] = *reinterpret_cast<const float(*)[8]>(&hi[8]);
+  uint2 out = make_uint2(e2m1_x8(lo0), e2m1_x8(lo1));
+  const uint2 amb = make_uint2(out.x ^ e2m1_x8(hi0), out.y ^ e2m1_x8(hi1));
   if (!normal_e) {
     out.x = pack4(e2m1_pair_exact(w[0], e), e2m1_pair_exact(w[1], e), e2m1_pair_exact(w[2], e),
                   e2m1_pair_exact(w[3], e));
