@@ -97,9 +97,10 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
 // quotient sits next to a rounding boundary of the E2M1 grid.
 //
 // With r an approximate reciprocal of a normal fp32 e (rcp.approx: within 2^-22
-// relative), q = fl32(x r) differs from the exact x/e by less than 2^-21.7
-// relative, and Q = fl32(x/e) by less than 2^-24, so Q lies strictly between
-// fl32(q (1 - 2^-19)) and fl32(q (1 + 2^-19)).  Rounding to the E2M1 grid is
+// relative) and r_lo = fl32(r (1 - 2^-19)), r_hi = fl32(r (1 + 2^-19)), the
+// products a = fl32(x r_lo) and b = fl32(x r_hi) differ from x/e (1 -+ 2^-19) by
+// less than 2^-22 + 2^-23 relative, while Q = fl32(x/e) is within 2^-24 of x/e:
+// so Q lies strictly between a and b.  Rounding to the E2M1 grid is
 // monotone in |v| (same sign throughout), so when both ends round to the same
 // code, Q does too.  The pairs where they differ (a quotient within about 2^-19
 // of a grid midpoint: with per-token scales x/e lands that close to a midpoint
@@ -109,13 +110,14 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
 __device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float e, float r, bool normal_e) {
   constexpr float kBelow = 1.0f - 1.0f / 524288.0f;  // 1 - 2^-19, exact in fp32
   constexpr float kAbove = 1.0f + 1.0f / 524288.0f;  // 1 + 2^-19
+  const float r_lo = __fmul_rn(r, kBelow);
+  const float r_hi = __fmul_rn(r, kAbove);
   float lo[16], hi[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float2 x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-    const float2 q = __fmul2_rn(x, make_float2(r, r));
-    const float2 a = __fmul2_rn(q, make_float2(kBelow, kBelow));
-    const float2 b = __fmul2_rn(q, make_float2(kAbove, kAbove));
+    const float2 a = __fmul2_rn(x, make_float2(r_lo, r_lo));
+    const float2 b = __fmul2_rn(x, make_float2(r_hi, r_hi));
     lo[2 * i] = a.x;
     lo[2 * i + 1] = a.y;
     hi[2 * i] = b.x;
