@@ -84,13 +84,6 @@ __device__ __forceinline__ void swiglu_bwd_uint4(const uint4 &g, const uint4 &u,
 // 2^(127 - code) as an fp32 (code in [0, 246] for bf16 inputs: always normal).
 __device__ __forceinline__ float mx_inv_scale(uint32_t code) { return __uint_as_float((254u - code) << 23); }
 
-// Two E4M3 codes: `lo` in bits 0..7, `hi` in bits 8..15.
-__device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // max(|a|, |b|) per bf16 half (sign bits hold the xor of the input signs).
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -98,17 +91,31 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Two values given as fp32 bit patterns (bf16 widened) times s, one packed
-// multiply (exact: s is a power of two) -> two E4M3 codes, `lo` in bits 0..7.
-__device__ __forceinline__ uint32_t e4m3x2_scaled(uint32_t lo, uint32_t hi, float s) {
-  const float2 p = __fmul2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)), make_float2(s, s));
-  return e4m3_pair(p.x, p.y);
+// Four E4M3 codes in value order, packed into a word by one vector move of two
+// 16-bit conversion results.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
+      "mov.b32 %0, {h0, h1};\n\t}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return r;
+}
+
+// Four values given as fp32 bit patterns (bf16 widened) times s (two packed
+// multiplies, exact: s is a power of two) -> four E4M3 codes in that order.
+__device__ __forceinline__ uint32_t e4m3x4_scaled(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, float s) {
+  const float2 p = __fmul2_rn(make_float2(__uint_as_float(w0), __uint_as_float(w1)), make_float2(s, s));
+  const float2 q = __fmul2_rn(make_float2(__uint_as_float(w2), __uint_as_float(w3)), make_float2(s, s));
+  return e4m3x4(p.x, p.y, q.x, q.y);
 }
 
 // The two bf16 of each of words a, b (elements a.lo, a.hi, b.lo, b.hi) times s
 // -> four E4M3 codes in element order.
 __device__ __forceinline__ uint32_t e4m3x4_words(uint32_t a, uint32_t b, float s) {
-  return __byte_perm(e4m3x2_scaled(a << 16, a & 0xFFFF0000u, s), e4m3x2_scaled(b << 16, b & 0xFFFF0000u, s), 0x5410);
+  return e4m3x4_scaled(a << 16, a & 0xFFFF0000u, b << 16, b & 0xFFFF0000u, s);
 }
 
 // ---------------------------------------------------------------- row-wise --
@@ -352,10 +359,8 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint32_t *v = vals + 4 * q;
-        wl[q] = __byte_perm(e4m3x2_scaled(v[0] << 16, v[1] << 16, s_lo), e4m3x2_scaled(v[2] << 16, v[3] << 16, s_lo),
-                            0x5410);
-        wh[q] = __byte_perm(e4m3x2_scaled(v[0] & 0xFFFF0000u, v[1] & 0xFFFF0000u, s_hi),
-                            e4m3x2_scaled(v[2] & 0xFFFF0000u, v[3] & 0xFFFF0000u, s_hi), 0x5410);
+        wl[q] = e4m3x4_scaled(v[0] << 16, v[1] << 16, v[2] << 16, v[3] << 16, s_lo);
+        wh[q] = e4m3x4_scaled(v[0] & 0xFFFF0000u, v[1] & 0xFFFF0000u, v[2] & 0xFFFF0000u, v[3] & 0xFFFF0000u, s_hi);
       }
       const int c = 2 * cp;
       *reinterpret_cast<uint4 *>(&outq[c][32 * b]) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
