@@ -145,18 +145,15 @@ __device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float 
   return out;
 }
 
-// E4M3 code of the correctly rounded quotient fl32(v / d), v >= 0, with rd an
-// approximate reciprocal of d (rcp.approx; d normal).  The same bracket as in
-// e2m1_block_codes: fl32(v rd) is within 2^-21.7 of v/d and fl32(v/d) within
-// 2^-24, so if fl32(q (1 - 2^-19)) and fl32(q (1 + 2^-19)) round to the same E4M3
-// code (one cvt converts both), that is the code of fl32(v/d).  Otherwise, or when
-// d is not normal, the quotient is computed with an IEEE division.
-__device__ __forceinline__ uint32_t e4m3_quotient_code(float v, float d, float rd, bool normal_d) {
-  constexpr float kBelow = 1.0f - 1.0f / 524288.0f;
-  constexpr float kAbove = 1.0f + 1.0f / 524288.0f;
-  const float q = __fmul_rn(v, rd);
+// E4M3 code of the correctly rounded quotient fl32(v / d), v >= 0, with rd_lo /
+// rd_hi an approximate reciprocal of d (rcp.approx; d normal) times 1 -+ 2^-19,
+// rounded.  The same bracket as in e2m1_block_codes: fl32(v rd_lo) and
+// fl32(v rd_hi) enclose fl32(v/d), so if they round to the same E4M3 code (one
+// cvt converts both), that is the code of fl32(v/d).  Otherwise, or when d is not
+// normal, the quotient is computed with an IEEE division.
+__device__ __forceinline__ uint32_t e4m3_quotient_code(float v, float d, float rd_lo, float rd_hi, bool normal_d) {
   uint16_t pair;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(__fmul_rn(q, kAbove)), "f"(__fmul_rn(q, kBelow)));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(__fmul_rn(v, rd_hi)), "f"(__fmul_rn(v, rd_lo)));
   const uint32_t lo = pair & 0xFFu;
   if (normal_d && lo == (static_cast<uint32_t>(pair) >> 8)) return lo;
   return e4m3_code(__fdiv_rn(v, d));
@@ -326,11 +323,13 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     const float d = __fmul_rn(6.0f, s_t);
     const bool normal_d = d >= 1.17549435e-38f;
     const float rd = rcp_approx(d);
+    const float rd_lo = __fmul_rn(rd, 1.0f - 1.0f / 524288.0f);  // 1 - 2^-19, exact
+    const float rd_hi = __fmul_rn(rd, 1.0f + 1.0f / 524288.0f);
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       const int blk = tid + j * T;
       uint32_t sb = 0;
-      if (bmax[j] != 0) sb = e4m3_quotient_code(bf16_bits_to_float(bmax[j]), d, rd, normal_d);
+      if (bmax[j] != 0) sb = e4m3_quotient_code(bf16_bits_to_float(bmax[j]), d, rd_lo, rd_hi, normal_d);
       uint2 packed = make_uint2(0, 0);
       if (sb != 0) {
         const float e = __fmul_rn(e4m3_value(sb), s_t);
@@ -342,10 +341,8 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       if (blk < nblk) *reinterpret_cast<uint2 *>(codes_row + blk * 8) = packed;
       // scales: threads 4g .. 4g+3 hold blocks blk .. blk+3 (blk = 4g + jT); thread 4g
       // stores them as one word
-      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
-      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-      const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);  // complete in lanes 4g
+      const uint32_t pair = __byte_perm(sb, __shfl_down_sync(0xFFFFFFFFu, sb, 1), 0x0040);
+      const uint32_t word = __byte_perm(pair, __shfl_down_sync(0xFFFFFFFFu, pair, 2), 0x5410);  // lanes 4g
       if (kRep) {
         // all four lanes of the group store one of the word's four copies
         const uint32_t w = __shfl_sync(0xFFFFFFFFu, word, lane & ~3);
