@@ -177,12 +177,10 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
         out.x = e4m3x4_words(v[u].x, v[u].y, s);
         out.y = e4m3x4_words(v[u].z, v[u].w, s);
         if (col < cols) *reinterpret_cast<uint2 *>(cr + col) = out;
-        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 4);
-        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 8);
-        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, code, 12);
+        const uint32_t pair = __byte_perm(code, __shfl_down_sync(0xFFFFFFFFu, code, 4), 0x0040);
+        const uint32_t word = __byte_perm(pair, __shfl_down_sync(0xFFFFFFFFu, pair, 8), 0x5410);
         if ((lane & 15) == 0 && col < cols) {
           const int64_t cb = (base + u * 256) / 32 + lane / 4;
-          const uint32_t word = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
           *reinterpret_cast<uint32_t *>(sf + sf_offset(prow, cb, c4)) = word;
         }
       }
