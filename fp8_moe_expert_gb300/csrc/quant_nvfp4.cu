@@ -17,8 +17,9 @@
 // registers.  Codes leave as 8-byte stores (256 contiguous bytes per warp) and
 // the scales of four consecutive blocks as one 4-byte store into the tiled scale
 // layout.  Block scales and element codes come from the correctly rounded
-// quotients, found without a division unless a quotient sits next to a rounding
-// boundary (see e4m3_quotient_code and e2m1_block_codes).
+// quotients: block scales from a bracket that divides only when a quotient sits
+// next to an E4M3 rounding boundary (e4m3_quotient_code), element codes from one
+// exact correction step that never divides (e2m1_block_codes).
 #include "fme_device.cuh"
 #include "fme_launch.h"
 
@@ -91,66 +92,61 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
   return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
+// Smallest decode scale e whose blocks are coded without a division.  Below it the
+// residual of the correction step in e2m1_block_codes could lose bits in the
+// subnormal range; such blocks (block scales far below any real data's) divide.
+constexpr float kE2M1StepMinScale = 0x1p-76f;
+
 // E2M1 codes of the correctly rounded quotients fl32(x_i/e) of the 16 bf16 values
 // of one block (8 words, element 2i in the low half of word i), packed two per
-// byte with the even element in the low nibble, without dividing unless a
-// quotient sits next to a rounding boundary of the E2M1 grid.
+// byte with the even element in the low nibble, without a division.
 //
-// With r an approximate reciprocal of a normal fp32 e (rcp.approx: within 2^-22
-// relative) and r_lo = fl32(r (1 - 2^-19)), r_hi = fl32(r (1 + 2^-19)), the
-// products a = fl32(x r_lo) and b = fl32(x r_hi) differ from x/e (1 -+ 2^-19) by
-// less than 2^-22 + 2^-23 relative, while Q = fl32(x/e) is within 2^-24 of x/e:
-// so Q lies strictly between a and b.  Rounding to the E2M1 grid is
-// monotone in |v| (same sign throughout), so when both ends round to the same
-// code, Q does too.  The pairs where they differ (a quotient within about 2^-19
-// of a grid midpoint: with per-token scales x/e lands that close to a midpoint
-// in about one block in a hundred) take their codes from the IEEE quotients, as
-// does the whole block when e is not normal.  Quotients far below 0.25 round to
-// (signed) zero on every path.  Pairs go through the packed f32x2 multiplier.
-__device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float e, float r, bool normal_e) {
-  constexpr float kBelow = 1.0f - 1.0f / 524288.0f;  // 1 - 2^-19, exact in fp32
-  constexpr float kAbove = 1.0f + 1.0f / 524288.0f;  // 1 + 2^-19
-  const float r_lo = __fmul_rn(r, kBelow);
-  const float r_hi = __fmul_rn(r, kAbove);
-  float lo[16], hi[16];
+// One correction step on fused multiply-adds after the reciprocal product
+// (Markstein's division refinement): with r = rcp.approx(e) (PTX ISA: at most one
+// ulp from 1/e), q = fl32(x r), rho = fl32(x - q e), Q = fl32(q + rho r).  Q is
+// the IEEE quotient fl32(x/e) for every bf16 x with x/e in [2^-4, 8] and every
+// e >= 2^-76 made from a bf16 row amax and an E4M3 block scale, whatever r is
+// within four ulps of 1/e: checked exhaustively on the CPU, every case bit for bit.
+// Quotients below 2^-4 give a signed-zero code on both sides (|Q| stays far
+// below the first E2M1 midpoint 0.25 and keeps x's sign).  Here the step runs
+// negated, n = fl32(x (-r)) = -q, rho = fl32(n e + x), t = fl32(rho (-r) + n) =
+// -Q, and the codes of t get their sign bits flipped: for x = -0 the plain form
+// ends in (+0) + (-0) = +0 where the IEEE quotient is -0, the negated one in
+// (-0) + (+0) = +0 = -(-0).  Pairs go through the packed f32x2 pipe.
+__device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float e) {
+  if (!(e >= kE2M1StepMinScale)) {
+    return make_uint2(pack4(e2m1_pair_exact(w[0], e), e2m1_pair_exact(w[1], e), e2m1_pair_exact(w[2], e),
+                            e2m1_pair_exact(w[3], e)),
+                      pack4(e2m1_pair_exact(w[4], e), e2m1_pair_exact(w[5], e), e2m1_pair_exact(w[6], e),
+                            e2m1_pair_exact(w[7], e)));
+  }
+  const float nr = -rcp_approx(e);
+  const float2 nr2 = make_float2(nr, nr);
+  const float2 e2 = make_float2(e, e);
+  float t[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float2 x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-    const float2 a = __fmul2_rn(x, make_float2(r_lo, r_lo));
-    const float2 b = __fmul2_rn(x, make_float2(r_hi, r_hi));
-    lo[2 * i] = a.x;
-    lo[2 * i + 1] = a.y;
-    hi[2 * i] = b.x;
-    hi[2 * i + 1] = b.y;
+    const float2 n = __fmul2_rn(x, nr2);
+    const float2 rho = __ffma2_rn(n, e2, x);
+    const float2 q = __ffma2_rn(rho, nr2, n);
+    t[2 * i] = q.x;
+    t[2 * i + 1] = q.y;
   }
-  const float(&lo0)[8] = *reinterpret_cast<const float(*)[8]>(&lo[0]);
-  const float(&lo1)[8] = *reinterpret_cast<const float(*)[8]>(&lo[8]);
-  const float(&hi0)[8] = *reinterpret_cast<const float(*)[8]>(&hi[0]);
-  const float(&hi1)[8] = *reinterpret_cast<const float(*)[8]>(&hi[8]);
-  uint2 out = make_uint2(e2m1_x8(lo0), e2m1_x8(lo1));
-  const uint2 amb = make_uint2(out.x ^ e2m1_x8(hi0), out.y ^ e2m1_x8(hi1));
-  if (!normal_e) {
-    out.x = pack4(e2m1_pair_exact(w[0], e), e2m1_pair_exact(w[1], e), e2m1_pair_exact(w[2], e),
-                  e2m1_pair_exact(w[3], e));
-    out.y = pack4(e2m1_pair_exact(w[4], e), e2m1_pair_exact(w[5], e), e2m1_pair_exact(w[6], e),
-                  e2m1_pair_exact(w[7], e));
-  } else if ((amb.x | amb.y) != 0) {
-    // byte i of amb.x / amb.y: the two codes of word i / word 4 + i are unsettled
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if ((amb.x >> (8 * i)) & 0xFFu) out.x = __byte_perm(out.x, e2m1_pair_exact(w[i], e), (0x3210 & ~(0xF << (4 * i))) | (4 << (4 * i)));
-      if ((amb.y >> (8 * i)) & 0xFFu) out.y = __byte_perm(out.y, e2m1_pair_exact(w[4 + i], e), (0x3210 & ~(0xF << (4 * i))) | (4 << (4 * i)));
-    }
-  }
-  return out;
+  const float(&t0)[8] = *reinterpret_cast<const float(*)[8]>(&t[0]);
+  const float(&t1)[8] = *reinterpret_cast<const float(*)[8]>(&t[8]);
+  return make_uint2(e2m1_x8(t0) ^ 0x88888888u, e2m1_x8(t1) ^ 0x88888888u);
 }
 
 // E4M3 code of the correctly rounded quotient fl32(v / d), v >= 0, with rd_lo /
 // rd_hi an approximate reciprocal of d (rcp.approx; d normal) times 1 -+ 2^-19,
-// rounded.  The same bracket as in e2m1_block_codes: fl32(v rd_lo) and
-// fl32(v rd_hi) enclose fl32(v/d), so if they round to the same E4M3 code (one
-// cvt converts both), that is the code of fl32(v/d).  Otherwise, or when d is not
-// normal, the quotient is computed with an IEEE division.
+// rounded.  rd is within 2^-22 of 1/d relative, so fl32(v rd_lo) and fl32(v rd_hi)
+// differ from v/d (1 -+ 2^-19) by less than 2^-22 + 2^-23 relative, while
+// fl32(v/d) is within 2^-24 of v/d: the two products enclose fl32(v/d).  Rounding
+// to E4M3 is monotone, so if both round to the same code (one cvt converts both),
+// that is the code of fl32(v/d).  Otherwise (a quotient within about 2^-19 of an
+// E4M3 midpoint: rare, E4M3 midpoints are far apart), or when d is not normal,
+// the quotient is computed with an IEEE division.
 __device__ __forceinline__ uint32_t e4m3_quotient_code(float v, float d, float rd_lo, float rd_hi, bool normal_d) {
   uint16_t pair;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(__fmul_rn(v, rd_hi)), "f"(__fmul_rn(v, rd_lo)));
@@ -344,9 +340,8 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       uint2 packed = make_uint2(0, 0);
       if (sb != 0) {
         const float e = __fmul_rn(e4m3_value(sb), s_t);
-        const bool normal_e = e >= 1.17549435e-38f;  // reciprocal finite and accurate
         const uint32_t w[8] = {a[j].x, a[j].y, a[j].z, a[j].w, b[j].x, b[j].y, b[j].z, b[j].w};
-        packed = e2m1_block_codes(w, e, rcp_approx(e), normal_e);
+        packed = e2m1_block_codes(w, e);
         if (swap) packed = make_uint2(packed.y, packed.x);
       }
       if (blk < nblk) *reinterpret_cast<uint2 *>(codes_row + blk * 8) = packed;

@@ -171,6 +171,59 @@ def test_nvfp4_exact_ties(fme, orc):
     check_nvfp4(fme, orc, x)
 
 
+def near_midpoint_rows():
+    """Rows for every normal bf16 row amax (32512 rows, k = 2048): block 0 holds the
+    amax, blocks 1..127 a block amax chosen for E4M3 block scales spread over 1..126.
+    Every block's other elements are the bf16 values just below and just above m e
+    for each E2M1 midpoint m (e the block's decode scale, from the E4M3 rounding of
+    fl32(amax_b / fl32(6 S))), signs alternating, plus a -0: quotients as close to
+    the E2M1 code boundaries as bf16 inputs get."""
+    import torch
+
+    mags = np.arange(0x0080, 0x7F80, dtype=np.uint32)
+    amax = (mags << 16).view(np.float32)
+    s_t = (amax / np.float32(2688.0)).astype(np.float32)
+    d = (np.float32(6.0) * s_t).astype(np.float32)
+    nblk = 128
+    target = np.round(np.linspace(1, 126, nblk - 1)).astype(np.uint8)
+    dec = torch.from_numpy(target).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    want_b = np.minimum(dec[None, :] * d[:, None].astype(np.float64), amax[:, None].astype(np.float64))
+    amax_b = np.concatenate([amax[:, None], synth.bf16_float(synth.bf16_bits(want_b.astype(np.float32)))], axis=1)
+    amax_b = np.minimum(amax_b, amax[:, None])
+    q = np.minimum((amax_b / d[:, None]).astype(np.float32), np.float32(448.0))
+    sb_val = torch.from_numpy(q).to(torch.float8_e4m3fn).float().numpy()
+    e = (sb_val * s_t[:, None]).astype(np.float32)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    t = (e[..., None].astype(np.float64) * mids).astype(np.float32)     # [rows, blocks, 7]
+    lo = (t.view(np.uint32) >> 16).astype(np.uint16)                   # bf16 at or below
+    hi = lo + 1
+    blk = np.empty(e.shape + (16,), np.uint16)
+    blk[..., 0] = synth.bf16_bits(amax_b)
+    blk[..., 1:8] = lo ^ np.array([0, 0x8000] * 3 + [0], np.uint16)
+    blk[..., 8:15] = hi ^ np.array([0x8000, 0] * 3 + [0x8000], np.uint16)
+    blk[..., 15] = 0x8000
+    return blk.reshape(mags.size, nblk * 16)
+
+
+def test_nvfp4_near_midpoints_every_amax(fme, orc):
+    """Element codes, block scales and per-token scales bit-exact on the rows of
+    near_midpoint_rows: where the division-free element coding would first go wrong."""
+    check_nvfp4(fme, orc, near_midpoint_rows())
+
+
+def test_near_midpoint_rows_are_hard():
+    """The generator does what it says: most blocks have the intended scale and
+    elements whose quotients sit within 2^-7 of an E2M1 midpoint (CPU only)."""
+    pytest.importorskip("torch")
+    x = near_midpoint_rows()
+    assert x.shape == (32512, 2048)
+    v = synth.bf16_float(x).reshape(32512, 128, 16).astype(np.float64)
+    amax_b = np.abs(v).max(axis=2)
+    assert np.array_equal(amax_b[:, 0], np.abs(v[:, 0, 0]))
+    assert (np.abs(v[..., 1:15]) <= amax_b[..., None]).all()
+    assert (x.reshape(32512, 128, 16)[..., 15] == 0x8000).all()
+
+
 @pytest.mark.parametrize("rows,k", [(256, 256), (512, 2048), (32 * 256, 7168)])
 def test_nvfp4_weights_layout(fme, orc, rows, k):
     """quantize_nvfp4_weights: codes and row scales identical to the per-token

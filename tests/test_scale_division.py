@@ -1,12 +1,25 @@
-"""The per-token scale S = fl32(amax / 2688) is computed on the GPU without a
-division: q = fl32(amax r) with r = fl32(1/2688), then S = fl32(q + (amax - q 2688) r)
-on fused multiply-adds.  Here that claim is checked for every positive finite bf16
-amax with exact rational arithmetic (each step rounded once to binary32, subnormals
-included) against numpy's correctly rounded binary32 division.  No GPU involved; the
-GPU tests check the device's results against the oracle for the same values."""
+"""Division-free quotients in the NVFP4 quantizer, checked on the CPU.
+
+1. The per-token scale S = fl32(amax / 2688) is computed on the GPU without a
+   division: q = fl32(amax r) with r = fl32(1/2688), then S = fl32(q + (amax - q 2688) r)
+   on fused multiply-adds.  Checked for every positive finite bf16 amax with exact
+   rational arithmetic (each step rounded once to binary32, subnormals included)
+   against numpy's correctly rounded binary32 division.
+2. The element codes E2M1(fl32(x / e)) come from one negated correction step after
+   an approximate reciprocal (see ``quotient_check.c``): checked exhaustively over
+   every row amax, block scale and bf16 x, for every reciprocal within four ulps of
+   1/e, by a C program using the C library's correctly rounded fmaf.
+
+No GPU involved; the GPU tests check the device's results against the oracle."""
+import os
+import shutil
+import subprocess
 from fractions import Fraction
 
 import numpy as np
+import pytest
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def _rn32(x: Fraction) -> Fraction:
@@ -42,3 +55,28 @@ def test_scale_without_division_matches_ieee_for_every_bf16_amax():
         res = _rn32(fa - q * c)
         s = _rn32(q + res * r)
         assert float(s) == float(w), (float(a), float(s), float(w))
+
+
+def _build_checker() -> str:
+    out_dir = os.path.join(_HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "quotient_check")
+    src = os.path.join(_HERE, "quotient_check.c")
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-o", exe, src, "-lm"]
+    if subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True).returncode != 0:
+        subprocess.run(base, check=True)  # no OpenMP: one thread, same result
+    return exe
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_e2m1_correction_step_is_the_ieee_quotient_exhaustively():
+    exe = _build_checker()
+    # reciprocals within 4 ulps of 1/e (rcp.approx is documented within 1);
+    # every 2999-th row amax also over all small quotients and negative x
+    res = subprocess.run([exe, "4", "2999"], capture_output=True, text=True, timeout=900)
+    line = res.stdout.strip().splitlines()[-1]
+    fields = dict(kv.split("=") for kv in line.split())
+    assert int(fields["mismatches"]) == 0, line
+    # 32639 amax x ~126 scales x 9 reciprocals x ~600 x in [2^-4, 8]
+    assert int(fields["checked"]) > 2_000_000_000, line
+    assert res.returncode == 0
