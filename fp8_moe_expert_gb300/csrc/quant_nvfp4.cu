@@ -20,6 +20,8 @@
 // quotients: block scales from a bracket that divides only when a quotient sits
 // next to an E4M3 rounding boundary (e4m3_quotient_code), element codes from one
 // exact correction step that never divides (e2m1_block_codes).
+#include <type_traits>
+
 #include "fme_device.cuh"
 #include "fme_launch.h"
 
@@ -93,7 +95,7 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
 }
 
 // Smallest decode scale e whose blocks are coded without a division.  Below it the
-// residual of the correction step in e2m1_block_codes could lose bits in the
+// residual of the correction step (e2m1_step_codes) could lose bits in the
 // subnormal range; such blocks (block scales far below any real data's) divide.
 constexpr float kE2M1StepMinScale = 0x1p-76f;
 
@@ -112,14 +114,9 @@ constexpr float kE2M1StepMinScale = 0x1p-76f;
 // negated, n = fl32(x (-r)) = -q, rho = fl32(n e + x), t = fl32(rho (-r) + n) =
 // -Q, and the codes of t get their sign bits flipped: for x = -0 the plain form
 // ends in (+0) + (-0) = +0 where the IEEE quotient is -0, the negated one in
-// (-0) + (+0) = +0 = -(-0).  Pairs go through the packed f32x2 pipe.
-__device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float e) {
-  if (!(e >= kE2M1StepMinScale)) {
-    return make_uint2(pack4(e2m1_pair_exact(w[0], e), e2m1_pair_exact(w[1], e), e2m1_pair_exact(w[2], e),
-                            e2m1_pair_exact(w[3], e)),
-                      pack4(e2m1_pair_exact(w[4], e), e2m1_pair_exact(w[5], e), e2m1_pair_exact(w[6], e),
-                            e2m1_pair_exact(w[7], e)));
-  }
+// (-0) + (+0) = +0 = -(-0).  Pairs go through the packed f32x2 pipe.  Valid for
+// e >= kE2M1StepMinScale (e2m1_block_codes below adds the test).
+__device__ __forceinline__ uint2 e2m1_step_codes(const uint32_t (&w)[8], float e) {
   const float nr = -rcp_approx(e);
   const float2 nr2 = make_float2(nr, nr);
   const float2 e2 = make_float2(e, e);
@@ -136,6 +133,18 @@ __device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float 
   const float(&t0)[8] = *reinterpret_cast<const float(*)[8]>(&t[0]);
   const float(&t1)[8] = *reinterpret_cast<const float(*)[8]>(&t[8]);
   return make_uint2(e2m1_x8(t0) ^ 0x88888888u, e2m1_x8(t1) ^ 0x88888888u);
+}
+
+// The same codes for any e > 0: the correction step where it is exact, IEEE
+// divisions below kE2M1StepMinScale.
+__device__ __forceinline__ uint2 e2m1_block_codes(const uint32_t (&w)[8], float e) {
+  if (!(e >= kE2M1StepMinScale)) {
+    return make_uint2(pack4(e2m1_pair_exact(w[0], e), e2m1_pair_exact(w[1], e), e2m1_pair_exact(w[2], e),
+                            e2m1_pair_exact(w[3], e)),
+                      pack4(e2m1_pair_exact(w[4], e), e2m1_pair_exact(w[5], e), e2m1_pair_exact(w[6], e),
+                            e2m1_pair_exact(w[7], e)));
+  }
+  return e2m1_step_codes(w, e);
 }
 
 // E4M3 code of the correctly rounded quotient fl32(v / d), v >= 0, with rd_lo /
@@ -332,30 +341,46 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     const float rd = rcp_approx(d);
     const float rd_lo = __fmul_rn(rd, 1.0f - 1.0f / 524288.0f);  // 1 - 2^-19, exact
     const float rd_hi = __fmul_rn(rd, 1.0f + 1.0f / 524288.0f);
+    // Codes and scales of this thread's blocks.  step_all: every block of the row
+    // takes the correction step, without a per-block test or branch (every e is at
+    // least 2^-9 s_t, the smallest E4M3 value times s_t, so s_t >= 2^-67 puts every
+    // e at or above 2^-76).  Activation rows take it (7% faster for k = 7168);
+    // the weights' variant measured no faster with it and keeps the per-block test.
+    auto code_blocks = [&](auto step_all) {
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      const int blk = tid + j * T;
-      uint32_t sb = 0;
-      if (bmax[j] != 0) sb = e4m3_quotient_code(bf16_bits_to_float(bmax[j]), d, rd_lo, rd_hi, normal_d);
-      uint2 packed = make_uint2(0, 0);
-      if (sb != 0) {
-        const float e = __fmul_rn(e4m3_value(sb), s_t);
+      for (int j = 0; j < R; ++j) {
+        const int blk = tid + j * T;
+        uint32_t sb = 0;
+        if (bmax[j] != 0) sb = e4m3_quotient_code(bf16_bits_to_float(bmax[j]), d, rd_lo, rd_hi, normal_d);
         const uint32_t w[8] = {a[j].x, a[j].y, a[j].z, a[j].w, b[j].x, b[j].y, b[j].z, b[j].w};
-        packed = e2m1_block_codes(w, e);
-        if (swap) packed = make_uint2(packed.y, packed.x);
+        uint2 packed = make_uint2(0, 0);
+        if constexpr (decltype(step_all)::value) {
+          // sb = 0 (codes 0): the step runs on e = 1, harmlessly, and is discarded
+          packed = e2m1_step_codes(w, sb != 0 ? __fmul_rn(e4m3_value(sb), s_t) : 1.0f);
+          if (swap) packed = make_uint2(packed.y, packed.x);
+          if (sb == 0) packed = make_uint2(0, 0);
+        } else if (sb != 0) {
+          packed = e2m1_block_codes(w, __fmul_rn(e4m3_value(sb), s_t));
+          if (swap) packed = make_uint2(packed.y, packed.x);
+        }
+        if (blk < nblk) *reinterpret_cast<uint2 *>(codes_row + blk * 8) = packed;
+        // scales: threads 4g .. 4g+3 hold blocks blk .. blk+3 (blk = 4g + jT); thread 4g
+        // stores them as one word
+        const uint32_t pair = __byte_perm(sb, __shfl_down_sync(0xFFFFFFFFu, sb, 1), 0x0040);
+        const uint32_t word = __byte_perm(pair, __shfl_down_sync(0xFFFFFFFFu, pair, 2), 0x5410);  // lanes 4g
+        if (kRep) {
+          // all four lanes of the group store one of the word's four copies
+          const uint32_t copy = __shfl_sync(0xFFFFFFFFu, word, lane & ~3);
+          if (blk < nblk) *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 4096 + 512 * (lane & 3)) = copy;
+        } else if ((lane & 3) == 0 && blk < nblk) {
+          *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = word;
+        }
       }
-      if (blk < nblk) *reinterpret_cast<uint2 *>(codes_row + blk * 8) = packed;
-      // scales: threads 4g .. 4g+3 hold blocks blk .. blk+3 (blk = 4g + jT); thread 4g
-      // stores them as one word
-      const uint32_t pair = __byte_perm(sb, __shfl_down_sync(0xFFFFFFFFu, sb, 1), 0x0040);
-      const uint32_t word = __byte_perm(pair, __shfl_down_sync(0xFFFFFFFFu, pair, 2), 0x5410);  // lanes 4g
-      if (kRep) {
-        // all four lanes of the group store one of the word's four copies
-        const uint32_t w = __shfl_sync(0xFFFFFFFFu, word, lane & ~3);
-        if (blk < nblk) *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 4096 + 512 * (lane & 3)) = w;
-      } else if ((lane & 3) == 0 && blk < nblk) {
-        *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = word;
-      }
+    };
+    if (!kRep && s_t >= 0x1p-67f) {
+      code_blocks(std::true_type{});
+    } else {
+      code_blocks(std::false_type{});
     }
     if (tid == 0) row_scale[row] = s_t;
   }
