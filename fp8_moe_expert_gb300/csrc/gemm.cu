@@ -16,8 +16,10 @@
 // scales arrive pre-replicated (quantize_nvfp4_weights), so B needs one wide
 // tensor-memory copy per 64-deep step instead of two narrow ones.  12 warps per CTA:
 //   warp 0      TMA producer (both CTAs): A, B and their scale tiles into a
-//               5-6 stage ring; every copy of the pair completes on the leader
-//               CTA's "full" barrier;
+//               4-6 stage ring; every copy of the pair completes on a barrier of
+//               the leader CTA, the scale tiles (issued first) on "sf_landed",
+//               A and B on "full", so that the scale copies below overlap the
+//               operand loads instead of following them;
 //   warp 1      allocates 512 tensor-memory columns in both CTAs together; in the
 //               leader, one thread issues the block-scaled MMAs (kind::mxf4nvf4
 //               or kind::mxf8f6f4, M = 256, N = 256); commits free the stage in
@@ -81,13 +83,17 @@ struct Cfg {
   static constexpr int kSfCols = kSfaCols + kSfbCols;
   static constexpr int kStages = kFp4 ? 5 : 6;  // ring depth when the shared memory allows
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStageTx = 2 * kStageBytes;  // both CTAs' copies land on the leader's barrier
+  // Both CTAs' copies land on the leader's barriers: the operands on "full", the
+  // scale tiles (issued first) on "sf_landed".
+  static constexpr int kOperandTx = 2 * (kABytes + kBBytes);
+  static constexpr int kScaleTx = 2 * (kSfaBytes + kSfbBytes);
   static_assert(kStages <= kMaxStages, "stage count");
   static_assert(kBN + kSfBuffers * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
 };
 
 struct SharedState {
-  uint64_t full[kMaxStages];
+  uint64_t full[kMaxStages];       // the stage's A and B tiles have landed
+  uint64_t sf_landed[kMaxStages];  // the stage's scale tiles have landed
   uint64_t empty[kMaxStages];
   uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b (one arrival per copier)
   uint64_t sf_empty[kSfBuffers];  // the MMAs reading buffer b are done
@@ -325,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&s.full[i], 1);
+      mbar_init(&s.sf_landed[i], 1);
       mbar_init(&s.empty[i], 1);
     }
     for (int i = 0; i < kSfBuffers; ++i) {
@@ -367,17 +374,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           stop = true;
           break;
         }
-        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], C::kStageTx);
+        // Scales first, on their own barrier: the copiers start on them while the
+        // operands are still arriving, so the tensor-memory copies are done by the
+        // time the MMAs could start (the copy latency was on the critical path).
+        if (rank == 0) mbar_arrive_expect_tx(&s.sf_landed[stage], C::kScaleTx);
+        const uint32_t sbar = pair::map_to_rank(&s.sf_landed[stage], 0);
+        pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, sbar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
+                          tl.sfa_row);
+        if (C::kFp4)  // four 64-deep steps of replicated blocks: 8 rows of 2 KB
+          pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, sbar, 0, tl.sfb_row + 8 * ks);
+        else
+          pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, sbar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
+                            tl.sfb_row);
+        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], C::kOperandTx);
         const uint32_t bar = pair::map_to_rank(&s.full[stage], 0);
         pair::tma_load_2d(smem_a + stage * kABytes, &p.map_a, bar, tl.a_x0 + ks * kStageKBytes, tl.a_y);
         pair::tma_load_2d(smem_b + stage * kBBytes, &p.map_b, bar, tl.b_x0 + ks * kStageKBytes, tl.b_y);
-        pair::tma_load_2d(smem_sfa + stage * C::kSfaBytes, &p.map_sfa, bar, (tl.sfa_x0 + ks * C::kAtoms) * 64,
-                          tl.sfa_row);
-        if (C::kFp4)  // four 64-deep steps of replicated blocks: 8 rows of 2 KB
-          pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, 0, tl.sfb_row + 8 * ks);
-        else
-          pair::tma_load_2d(smem_sfb + stage * C::kSfbBytes, &p.map_sfb, bar, (tl.sfb_x0 + ks * C::kAtoms) * 64,
-                            tl.sfb_row);
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
@@ -452,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
       const Tile tl = tile_at<K>(p, grp, t, 0);
       for (int ks = 0; ks < tl.num_k; ++ks) {
-        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
+        if (!mbar_wait(&s.sf_landed[stage], phase, abort_flag, p.status) ||
             !mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status)) {
           stop = true;
           break;
