@@ -18,6 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIBRARY = os.path.join(HERE, "libfme.so")
+BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["api.cu", "quant_nvfp4.cu", "quant_mxfp8.cu", "gemm.cu", "route.cu"]
 HEADERS = ["fme_device.cuh", "fme_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -49,12 +50,16 @@ def build(output: str = LIBRARY, extra_flags: list[str] | None = None, verbose: 
     """Compile and link the library; returns its path."""
     flags = NVCC_FLAGS + (extra_flags or [])
     tool = nvcc()
-    with tempfile.TemporaryDirectory(prefix="fme_build_") as tmp:
+    # objects and nvcc's own intermediates stay inside the package tree (git-ignored)
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    with tempfile.TemporaryDirectory(prefix=f"{os.getpid()}_", dir=BUILD_DIR) as tmp:
+        env = dict(os.environ, TMPDIR=tmp)
+
         def compile_one(src: str) -> str:
             obj = os.path.join(tmp, os.path.splitext(src)[0] + ".o")
             cmd = [tool, *ARCH, *flags, "-I", os.path.join(ROOT, "include"), "-c",
                    os.path.join(CSRC, src), "-o", obj]
-            res = subprocess.run(cmd, capture_output=True, text=True)
+            res = subprocess.run(cmd, capture_output=True, text=True, env=env)
             if res.returncode != 0:
                 raise RuntimeError(f"nvcc failed on {src}:\n{res.stdout}\n{res.stderr}")
             if verbose:
@@ -65,7 +70,7 @@ def build(output: str = LIBRARY, extra_flags: list[str] | None = None, verbose: 
             objs = list(pool.map(compile_one, SOURCES))
         tmp_out = output + ".tmp"
         cmd = [tool, *ARCH, "-shared", "-o", tmp_out, *objs]
-        res = subprocess.run(cmd, capture_output=True, text=True)
+        res = subprocess.run(cmd, capture_output=True, text=True, env=env)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
         os.replace(tmp_out, output)

@@ -36,7 +36,9 @@ _lock = threading.Lock()
 def build(source: str = SOURCE, output: str = LIBRARY) -> str:
     """Compile the oracle with gcc (no fused multiply-add, no fast math)."""
     cmd = ["gcc", *CFLAGS, "-o", output, source, "-lm"]
-    subprocess.run(cmd, check=True)
+    scratch = os.path.join(_HERE, "_build")  # gcc's intermediates stay in the tree (git-ignored)
+    os.makedirs(scratch, exist_ok=True)
+    subprocess.run(cmd, check=True, env=dict(os.environ, TMPDIR=scratch))
     return output
 
 

@@ -10,6 +10,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) and the CUDA library")
+    # temporary files of the tests (tmp_path) stay inside the repository, git-ignored;
+    # pytest empties this directory at the start of each session
+    if not config.option.basetemp:
+        config.option.basetemp = os.path.join(ROOT, "tests", "_tmp")
 
 
 @pytest.fixture(scope="session")

@@ -63,8 +63,9 @@ def _build_checker() -> str:
     exe = os.path.join(out_dir, "quotient_check")
     src = os.path.join(_HERE, "quotient_check.c")
     base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-o", exe, src, "-lm"]
-    if subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True).returncode != 0:
-        subprocess.run(base, check=True)  # no OpenMP: one thread, same result
+    env = dict(os.environ, TMPDIR=out_dir)  # gcc's intermediates stay in the tree
+    if subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True, env=env).returncode != 0:
+        subprocess.run(base, check=True, env=env)  # no OpenMP: one thread, same result
     return exe
 
 
