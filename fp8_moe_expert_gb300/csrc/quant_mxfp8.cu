@@ -335,6 +335,27 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
     if (nxt.j < chunks) {
       col_tile_locate(nxt, groups, num_groups);
       load_tile(nxt, pre);
+      // the tile after next: one 128-byte line per thread into L2, so that its
+      // register loads a tile from now find it there
+      ColTile nn = nxt;
+      advance(nn);
+      if (nn.j < chunks) {
+        col_tile_locate(nn, groups, num_groups);
+        const int r = tid & 127;
+        if (r < nn.valid) {
+          const int64_t row = nn.src0 + r;
+          const uint16_t *line;
+          if constexpr (kSw) {
+            line = (tid < 128) ? x + row * cols + nn.cb * 64 : x + row * cols + inter + nn.cb * 64;
+          } else {
+            line = x + row * cols + nn.cb * 128 + (tid >> 7) * 64;
+          }
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+          if constexpr (kSw) {
+            if (tid < 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(dh + row * inter + nn.cb * 64));
+          }
+        }
+      }
     }
 
     // thread = (channel pair cp, 32-position block b): both channels' 32 values
