@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
   const int swap = (tid >> 2) & 1;
   int i = 0, s = 0;
   uint32_t parity = 0;
+  int g_cur = 0;  // thread 0: group of the current row (activations)
   int64_t row = row_at(0);
   for (; row < rows; ++i, row = kRep ? row_at(i) : row + stride) {
     const bool ok = mbar_wait(&bars[s], parity, &abort_flag, status);
@@ -325,7 +326,9 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     if (lane == 0) part[i & 1][warp] = wmax;
     if (tid == 0) {
       if (!kRep) {
-        const int g = find_group(g_off, num_groups, row);
+        // rows only increase here (first + i stride): move the group cursor forward
+        while (g_cur + 1 < num_groups && g_off[g_cur + 1] <= row) ++g_cur;
+        const int g = g_cur;
         const int64_t prow = 128 * static_cast<int64_t>(g_tiles[g]) + (row - g_off[g]);
         sf_row_of[i & 1] = sf_offset(prow, 0, c4);
       }
