@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t *__restr
 constexpr int kColTilePad = 8;  // bf16 elements of padding per staged row
 constexpr int kColTileBytes = 128 * (128 + kColTilePad) * 2;
 constexpr int kColOutBytes = 128 * (128 + 16);
-constexpr int kColSmemBytes = kColTileBytes + kColOutBytes + 512 + 512;
+constexpr int kColStageBytes = kColOutBytes + 512 + 512;  // codes, column scales, row scales of a tile
+constexpr int kColSmemBytes = kColTileBytes + 2 * kColStageBytes;
 
 // One tile of the walk: chunk j of the padded positions, column block cb, the
 // chunk's group g, its first source row and how many of its 128 rows exist.
@@ -246,9 +247,13 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
   __shared__ int ok_flag;
   extern __shared__ __align__(16) uint8_t col_smem[];
   auto tile = reinterpret_cast<uint16_t(*)[128 + kColTilePad]>(col_smem);
-  auto outq = reinterpret_cast<uint8_t(*)[128 + 16]>(col_smem + kColTileBytes);
-  uint8_t *sfs = col_smem + kColTileBytes + kColOutBytes;
-  uint8_t *sfr = sfs + 512;  // row-wise scales of the tile (kRows)
+  // two staging buffers: tile t's outputs leave during tile t + 1, after its second
+  // barrier, so that each tile needs two barriers instead of three
+  auto outq_of = [&](int b) {
+    return reinterpret_cast<uint8_t(*)[128 + 16]>(col_smem + kColTileBytes + b * kColStageBytes);
+  };
+  auto sfs_of = [&](int b) { return col_smem + kColTileBytes + b * kColStageBytes + kColOutBytes; };
+  auto sfr_of = [&](int b) { return sfs_of(b) + 512; };  // row-wise scales of the tile (kRows)
 
   if (!load_groups(groups, offsets, num_groups, rows, &ok_flag)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(status, kDevBadOffsets);
@@ -303,6 +308,51 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
       }
     }
   };
+  // Column-wise codes and scales (and kRows: row-wise scales) of tile pt, staged in
+  // buffer b, to global memory.
+  auto write_staged = [&](const ColTile &pt, int b) {
+    const int cb = pt.cb;
+    auto outq = outq_of(b);
+    const uint8_t *sfs = sfs_of(b);
+    const uint8_t *sfr = sfr_of(b);
+
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+      const int ch = pass * 32 + (tid >> 3);
+      const int seg = tid & 7;
+      const uint4 v = *reinterpret_cast<const uint4 *>(&outq[ch][seg * 16]);
+      const int64_t gch = kSw ? (ch < 64 ? cb * 64 + ch : inter + cb * 64 + ch - 64) : static_cast<int64_t>(cb) * 128 + ch;
+      *reinterpret_cast<uint4 *>(codes_t + gch * ld + pt.j * 128 + seg * 16) = v;
+    }
+    if constexpr (kSw) {
+      // the gate and up halves are each half of a 512-byte scale tile: tile rows
+      // (channels) 0..63 or 64..127 by the parity of cb (inter is a multiple of 128)
+      const int odd = cb & 1;
+      const int64_t t_g = cb / 2, t_u = (inter / 64 + cb) / 2;
+      if (tid < 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
+        *reinterpret_cast<uint2 *>(sf_t + (t_g * (ld / 128) + pt.j) * 512 + tid * 16 + 8 * odd) = make_uint2(v.x, v.y);
+        *reinterpret_cast<uint2 *>(sf_t + (t_u * (ld / 128) + pt.j) * 512 + tid * 16 + 8 * odd) = make_uint2(v.z, v.w);
+      }
+      {
+        // row-wise scales: row r's 4-byte cell holds blocks (g0, g1, u0, u1)
+        const int r = tid >> 1;
+        const int half = tid & 1;
+        const int cell = (r & 31) * 16 + (r >> 5) * 4;
+        const uint16_t v = *reinterpret_cast<const uint16_t *>(&sfr[cell + 2 * half]);
+        const int64_t tcol = half ? t_u : t_g;
+        *reinterpret_cast<uint16_t *>(row_sf + (pt.j * (cols / 128) + tcol) * 512 + cell + 2 * odd) = v;
+      }
+    } else {
+      if (tid < 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
+        *reinterpret_cast<uint4 *>(sf_t + (static_cast<int64_t>(cb) * (ld / 128) + pt.j) * 512 + tid * 16) = v;
+      } else if (kRows && tid < 64) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[(tid - 32) * 16]);
+        *reinterpret_cast<uint4 *>(row_sf + (pt.j * cblocks + cb) * 512 + (tid - 32) * 16) = v;
+      }
+    }
+  };
   ColTile cur{static_cast<int64_t>(blockIdx.x) / cblocks, static_cast<int>(blockIdx.x % cblocks), 0, 0, 0};
   uint4 pre[kPre];
   if (cur.j < chunks) {
@@ -312,10 +362,15 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
   ColTile nxt = cur;
   advance(nxt);
 
+  ColTile prev = cur;  // the tile whose outputs are staged in buffer buf ^ 1
+  bool staged = false;
+  int buf = 0;
   for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-    const int64_t j = cur.j;
     const int cb = cur.cb;
-    __syncthreads();  // the previous tile's shared buffers are free
+    auto outq = outq_of(buf);
+    uint8_t *sfs = sfs_of(buf);
+    uint8_t *sfr = sfr_of(buf);
+    __syncthreads();  // the tile buffer is free; the previous tile's staged outputs are complete
     if constexpr (kSw) {
 #pragma unroll
       for (int pass = 0; pass < 4; ++pass) {
@@ -332,6 +387,7 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
         *reinterpret_cast<uint4 *>(&tile[pass * 16 + (tid >> 4)][(tid & 15) * 8]) = pre[pass];
     }
     __syncthreads();
+    if (staged) write_staged(prev, buf ^ 1);
     if (nxt.j < chunks) {
       col_tile_locate(nxt, groups, num_groups);
       load_tile(nxt, pre);
@@ -424,35 +480,7 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
         sfr[(r & 31) * 16 + (r >> 5) * 4 + b] = static_cast<uint8_t>(code);
       }
     }
-    __syncthreads();
-
-#pragma unroll
-    for (int pass = 0; pass < 4; ++pass) {
-      const int ch = pass * 32 + (tid >> 3);
-      const int seg = tid & 7;
-      const uint4 v = *reinterpret_cast<const uint4 *>(&outq[ch][seg * 16]);
-      const int64_t gch = kSw ? (ch < 64 ? cb * 64 + ch : inter + cb * 64 + ch - 64) : static_cast<int64_t>(cb) * 128 + ch;
-      *reinterpret_cast<uint4 *>(codes_t + gch * ld + j * 128 + seg * 16) = v;
-    }
     if constexpr (kSw) {
-      // the gate and up halves are each half of a 512-byte scale tile: tile rows
-      // (channels) 0..63 or 64..127 by the parity of cb (inter is a multiple of 128)
-      const int odd = cb & 1;
-      const int64_t t_g = cb / 2, t_u = (inter / 64 + cb) / 2;
-      if (tid < 32) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
-        *reinterpret_cast<uint2 *>(sf_t + (t_g * (ld / 128) + j) * 512 + tid * 16 + 8 * odd) = make_uint2(v.x, v.y);
-        *reinterpret_cast<uint2 *>(sf_t + (t_u * (ld / 128) + j) * 512 + tid * 16 + 8 * odd) = make_uint2(v.z, v.w);
-      }
-      {
-        // row-wise scales: row r's 4-byte cell holds blocks (g0, g1, u0, u1)
-        const int r = tid >> 1;
-        const int half = tid & 1;
-        const int cell = (r & 31) * 16 + (r >> 5) * 4;
-        const uint16_t v = *reinterpret_cast<const uint16_t *>(&sfr[cell + 2 * half]);
-        const int64_t tcol = half ? t_u : t_g;
-        *reinterpret_cast<uint16_t *>(row_sf + (j * (cols / 128) + tcol) * 512 + cell + 2 * odd) = v;
-      }
       if (d_out != nullptr) {
 #pragma unroll
         for (int pass = 0; pass < 8; ++pass) {
@@ -465,18 +493,15 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
           }
         }
       }
-    } else {
-      if (tid < 32) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
-        *reinterpret_cast<uint4 *>(sf_t + (static_cast<int64_t>(cb) * (ld / 128) + j) * 512 + tid * 16) = v;
-      } else if (kRows && tid < 64) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[(tid - 32) * 16]);
-        *reinterpret_cast<uint4 *>(row_sf + (j * cblocks + cb) * 512 + (tid - 32) * 16) = v;
-      }
     }
+    prev = cur;
+    staged = true;
+    buf ^= 1;
     cur = nxt;
     advance(nxt);
   }
+  __syncthreads();
+  if (staged) write_staged(prev, buf ^ 1);
 }
 
 cudaError_t launch_quantize_mxfp8_rows(const LaunchMxfp8 &a) {
