@@ -177,10 +177,9 @@ class MoEStep:
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
         # quantized operands and outputs, allocated once
         self.xq = (e((R, H // 2), u8), e((fme.sf_bytes(R, H, 16, E),), u8), e((R,), f32))
-        self.wguq = (e((E * 2 * I, H // 2), u8), e((fme.sf_bytes_nvfp4_weights(E * 2 * I, H),), u8),
-                     e((E * 2 * I,), f32))
+        self.wguq = (e((E * 2 * I, H // 2), u8), e((fme.sf_bytes(E * 2 * I, H, 16, 1),), u8), e((E * 2 * I,), f32))
         self.hq = (e((R, I // 2), u8), e((fme.sf_bytes(R, I, 16, E),), u8), e((R,), f32))
-        self.wdq = (e((E * H, I // 2), u8), e((fme.sf_bytes_nvfp4_weights(E * H, I),), u8), e((E * H,), f32))
+        self.wdq = (e((E * H, I // 2), u8), e((fme.sf_bytes(E * H, I, 16, 1),), u8), e((E * H,), f32))
         self.y_gu = e((R, 2 * I), bf16)
         self.y_d = e((R, H), bf16)
         self.dyr = (e((R, H), u8), e((fme.sf_bytes(R, H, 32, E),), u8))
@@ -195,9 +194,7 @@ class MoEStep:
     # algorithmic work per call: ("bytes"|"flops", amount)
     def work(self):
         R, H, I, E = self.R, self.H, self.I, self.E
-        # per row: bf16 in, E2M1 codes, E4M3 block scales, fp32 row scale (the weights'
-        # replicated scale layout writes k/4 scale bytes; counted here as the k/16 the
-        # method needs)
+        # per row: bf16 in, E2M1 codes, E4M3 block scales, fp32 row scale
         nv = lambda rows, k: rows * (2 * k + k // 2 + k // 16 + 4)  # noqa: E731
         mx = lambda rows, c: rows * (2 * c + c + c // 32)  # noqa: E731
         return {
@@ -223,13 +220,13 @@ class MoEStep:
         return [
             lambda: f.quantize_nvfp4_pertoken(self.x, off, codes=self.xq[0], sf=self.xq[1], row_scale=self.xq[2],
                                               status=st),
-            lambda: f.quantize_nvfp4_weights(self.w_gu, codes=self.wguq[0], sf=self.wguq[1], row_scale=self.wguq[2],
-                                             status=st),
+            lambda: f.quantize_nvfp4_pertoken(self.w_gu, codes=self.wguq[0], sf=self.wguq[1], row_scale=self.wguq[2],
+                                              status=st),
             lambda: f.grouped_gemm_fwd_nvfp4(*self.xq, *self.wguq, off, 2 * I, H, y=self.y_gu, status=st),
             lambda: f.quantize_nvfp4_pertoken(self.h, off, codes=self.hq[0], sf=self.hq[1], row_scale=self.hq[2],
                                               status=st),
-            lambda: f.quantize_nvfp4_weights(self.w_d, codes=self.wdq[0], sf=self.wdq[1], row_scale=self.wdq[2],
-                                             status=st),
+            lambda: f.quantize_nvfp4_pertoken(self.w_d, codes=self.wdq[0], sf=self.wdq[1], row_scale=self.wdq[2],
+                                              status=st),
             lambda: f.grouped_gemm_fwd_nvfp4(*self.hq, *self.wdq, off, H, I, y=self.y_d, status=st),
             lambda: f.quantize_mxfp8_rowcol(self.dy, off, row_codes=self.dyr[0], row_sf=self.dyr[1],
                                             col_codes=self.dyc[0], col_sf=self.dyc[1], padded_offsets=self.dyc[2],

@@ -62,7 +62,6 @@ def lib() -> ctypes.CDLL:
 SYMBOLS = {
     # name: (restype, argtypes)
     "quantize_nvfp4_pertoken": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p"]),
-    "quantize_nvfp4_weights": ("i32", ["p", "i64", "i64", "p", "p", "p", "p", "p"]),
     "quantize_nvfp4_pertensor": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p"]),
     "swiglu_quantize_nvfp4": ("i32", ["p", "i64", "i64", "p", "i32", "p", "p", "p", "p", "p", "p"]),
     "quantize_mxfp8": ("i32", ["p", "i64", "i64", "i32", "p", "i32", "p", "p", "p", "p", "p"]),
@@ -87,7 +86,6 @@ SYMBOLS = {
     "fme_sf_padded_rows": ("i64", ["i64", "i32"]),
     "fme_sf_bytes": ("i64", ["i64", "i64", "i32", "i32"]),
     "fme_colwise_ld": ("i64", ["i64", "i32"]),
-    "fme_sf_bytes_nvfp4_weights": ("i64", ["i64", "i64"]),
     "fme_read_device_status": ("i32", ["p", "p", "p"]),
     "fme_error_string": ("s", ["i32"]),
     "fme_last_cuda_error": ("s", []),
@@ -116,10 +114,6 @@ def sf_bytes(rows: int, cols: int, block: int, num_groups: int = 1) -> int:
 
 def colwise_ld(rows: int, num_groups: int = 1) -> int:
     return int(lib().fme_colwise_ld(rows, num_groups))
-
-
-def sf_bytes_nvfp4_weights(rows: int, k: int) -> int:
-    return int(lib().fme_sf_bytes_nvfp4_weights(rows, k))
 
 
 def route_workspace_bytes(tokens: int, top_k: int, num_experts: int) -> int:
@@ -200,26 +194,6 @@ def quantize_nvfp4_pertensor(x, offsets=None, num_groups=None, *, codes=None, sf
                                         _ptr(row_scale), _ptr(tensor_amax), _ptr(status), _stream(stream))
     _check(st, "quantize_nvfp4_pertensor")
     return codes, sf, row_scale[:rows], tensor_amax[:1]
-
-
-def quantize_nvfp4_weights(w, *, codes=None, sf=None, row_scale=None, status=None, stream=None):
-    """NVFP4 of stacked expert weights W [rows x k] for the B operand of
-    grouped_gemm_fwd_nvfp4 -> (codes [rows, k/2] u8, sf (B-operand layout) u8,
-    row_scale [rows] f32)."""
-    import torch
-
-    rows, k = w.shape
-    dev = w.device
-    if codes is None:
-        codes = _empty((rows, k // 2), torch.uint8, dev)
-    if sf is None:
-        sf = _empty((max(sf_bytes_nvfp4_weights(rows, k), 16),), torch.uint8, dev)
-    if row_scale is None:
-        row_scale = _empty((rows,), torch.float32, dev)
-    st = lib().quantize_nvfp4_weights(_ptr(w), rows, k, _ptr(codes), _ptr(sf), _ptr(row_scale), _ptr(status),
-                                      _stream(stream))
-    _check(st, "quantize_nvfp4_weights")
-    return codes, sf, row_scale
 
 
 def swiglu_quantize_nvfp4(gate_up, offsets=None, num_groups=None, *, codes=None, sf=None, row_scale=None, h=None,

@@ -19,8 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIBRARY = os.path.join(HERE, "libfme.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "quant_nvfp4.cu", "quant_mxfp8.cu", "gemm.cu", "route.cu"]
-HEADERS = ["fme_device.cuh", "fme_launch.h"]
+SOURCES = ["api.cu", "quant_nvfp4.cu", "quant_mxfp8.cu", "gemm.cu", "gemm_nvfp4.cu", "route.cu"]
+HEADERS = ["fme_device.cuh", "fme_launch.h", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]

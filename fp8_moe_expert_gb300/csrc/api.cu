@@ -157,11 +157,6 @@ int64_t fme_route_workspace_bytes(int64_t tokens, int32_t top_k, int32_t num_exp
   return b < 16 ? 16 : b;
 }
 
-int64_t fme_sf_bytes_nvfp4_weights(int64_t rows, int64_t k) {
-  if (rows < 0 || k < 0 || rows % 256 != 0 || k % 64 != 0) return 0;
-  return (rows / 256) * (k / 64) * 4096;
-}
-
 const char *fme_version(void) { return "fme 0.1.0 (sm_103a)"; }
 
 const char *fme_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
@@ -233,24 +228,6 @@ fme_status quantize_nvfp4_pertensor(const void *x, int64_t rows, int64_t k, cons
                      static_cast<cudaStream_t>(stream)};
   cudaError_t err = fme::launch_quantize_nvfp4_pertensor(a, tensor_amax);
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_nvfp4_pertensor launch");
-}
-
-fme_status quantize_nvfp4_weights(const void *x, int64_t rows, int64_t k, uint8_t *codes, uint8_t *sf,
-                                  float *row_scale, int32_t *dev_status, void *stream) {
-  if (rows < 0) return FME_ERR_INVALID_ARGUMENT;
-  if (rows % 256 != 0 || k % 256 != 0 || k < 256 || k > 8192) return FME_ERR_UNSUPPORTED_SHAPE;
-  if (rows > (int64_t(1) << 31) - 1 || (rows / 256) * (k / 64) * 2 > (int64_t(1) << 31) - 1)
-    return FME_ERR_UNSUPPORTED_SHAPE;
-  if (rows == 0) return FME_OK;
-  if (!x || !codes || !sf || !row_scale) return FME_ERR_INVALID_ARGUMENT;
-  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) || !aligned16(row_scale)) return FME_ERR_MISALIGNED;
-  int sms = 0;
-  fme_status st = current_device(&sms);
-  if (st != FME_OK) return st;
-  fme::LaunchNvfp4 a{x, rows, k, nullptr, 1, codes, sf, row_scale, dev_status, sms, static_cast<cudaStream_t>(stream)};
-  a.replicated_sf = true;
-  cudaError_t err = fme::launch_quantize_nvfp4(a);
-  return err == cudaSuccess ? FME_OK : cuda_fail(err, "quantize_nvfp4_weights launch");
 }
 
 fme_status swiglu_quantize_nvfp4(const void *gate_up, int64_t rows, int64_t inter, const int32_t *offsets,
@@ -463,8 +440,7 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
                                   void *y, int32_t *dev_status, void *stream) {
   if (m < 0 || n < 0 || k < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
   if (n % 256 != 0 || n == 0 || k % 256 != 0 || k == 0 || k > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
-  if (m > (int64_t(1) << 31) - 1 || static_cast<int64_t>(num_experts) * n > (int64_t(1) << 31) - 1 ||
-      static_cast<int64_t>(num_experts) * (n / 256) * (k / 64) * 2 > (int64_t(1) << 31) - 1)
+  if (m > (int64_t(1) << 31) - 1 || static_cast<int64_t>(num_experts) * n > (int64_t(1) << 31) - 1)
     return FME_ERR_UNSUPPORTED_SHAPE;
   if (!offsets) return FME_ERR_INVALID_ARGUMENT;
   if (m == 0) return FME_OK;
@@ -484,10 +460,10 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   if ((st = encode_scales_2d(&a.map_sfa, a_sf, padded_rows_bound(m, num_experts) / 128, (k / 64) * 512, 4, 1)) !=
       FME_OK)
     return st;
-  // B scales in the weights' replicated layout: 2 KB rows, 2 per 64-deep step per
-  // 256 rows; a stage takes 8 rows (16 KB)
-  if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * (n / 256) * (k / 64) * 2, 2048, 4,
-                             8)) != FME_OK)
+  // B scales: the same tiled layout (the stacked weights are one group of
+  // num_experts * n rows); a stage takes 4 tiles of each of the tile's two 128-row blocks
+  if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * n / 128, (k / 64) * 512, 4,
+                             2)) != FME_OK)
     return st;
   a.a_scale = a_scale;
   a.b_scale = b_scale;

@@ -18,8 +18,16 @@ constexpr int kDevBadIndex = 0x4;
 constexpr int kMaxGroups = 1024;
 
 // A bounded wait gives up after this long (ns of %globaltimer); real waits in
-// these kernels last microseconds to a fraction of a millisecond.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// these kernels last microseconds to a fraction of a millisecond.  A test build
+// may shorten it (-DFME_WAIT_LIMIT_NS=...) so that waits run out on purpose; the
+// waits that drain copies and MMAs already in flight before a CTA exits keep
+// their own, fixed limit (kDrainLimitNs), so the shortened build still lets
+// that work land.
+#ifndef FME_WAIT_LIMIT_NS
+#define FME_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = FME_WAIT_LIMIT_NS;
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ void report(int32_t *status, int bits) {
   if (status != nullptr) atomicOr(status, bits);
@@ -88,6 +96,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// Wait for the phase of `bar` with the given parity, up to kDrainLimitNs, with no
+// abort flag: used at the end of a role to let copies or MMAs already issued land.
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kDrainLimitNs) return false;
+  return true;
+}
+
 // ----------------------------------------------------------------- TMA copies --
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile(
@@ -124,6 +141,52 @@ __device__ __forceinline__ void tmem_ld_32x32(uint32_t taddr, uint32_t (&r)[32])
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x N consecutive 32-bit columns from registers: thread i writes lane
+// (quarter base + i).  The first column must be a multiple of N.
+__device__ __forceinline__ void tmem_st_32x32_x4(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Per-warpgroup register budgets (every warp of a warpgroup executes the same one).
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Shared-memory matrix descriptor, K-major operand tile written by TMA with
 // 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked
 // along M/N (stride 1024), descriptor version 1 (bit 46), layout code 2 = 128B swizzle.
@@ -142,20 +205,6 @@ __device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) {
 __device__ __forceinline__ uint64_t desc_scale_tile(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
-  d |= static_cast<uint64_t>(128 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  return d;
-}
-
-// Descriptor of a 4096-byte replicated scale block for the 128 x 256-bit copy:
-// no swizzle, 8-row x 16-byte core matrices; the left 16 bytes of the rows are
-// at 0 .. 2047 (8-row groups 128 bytes apart), the right 16 bytes 2048 further.
-// A block holding [tile0 x 4][tile1 x 4] (two 512-byte scale tiles, each four
-// times) puts tile0 row i % 32 and tile1 row i % 32 into lane i.
-__device__ __forceinline__ uint64_t desc_scale_rep(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
-  d |= static_cast<uint64_t>(2048 >> 4) << 16;
   d |= static_cast<uint64_t>(128 >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   return d;
@@ -284,12 +333,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // into four tensor-memory columns of that CTA, replicated over the lane quarters.
 __device__ __forceinline__ void copy_scales(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// Copy 128 rows x 32 bytes (described by `sdesc`) into eight tensor-memory
-// columns of all 128 lanes, row i to lane i, in both CTAs of the pair.
-__device__ __forceinline__ void copy_scales_wide(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive on the mbarrier at the same shared offset in both CTAs when the

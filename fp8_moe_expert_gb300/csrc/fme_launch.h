@@ -18,7 +18,6 @@ struct LaunchNvfp4 {
   int32_t *status;
   int num_sms;
   cudaStream_t stream;
-  bool replicated_sf = false;  // scales in the forward GEMM's B-operand layout (quantize_nvfp4_weights)
   bool swiglu = false;         // x is a gate/up output [rows x 2k]; quantize silu(gate) * up
   void *h_out = nullptr;       // swiglu: the bf16 activation [rows x k], or NULL
   const int32_t *gather = nullptr;  // row r reads input row gather[r] / gather_div (permuted tokens)

@@ -208,20 +208,10 @@ __device__ __forceinline__ uint4 swiglu_uint4(const uint4 &g, const uint4 &u) {
   return make_uint4(swiglu_word(g.x, u.x), swiglu_word(g.y, u.y), swiglu_word(g.z, u.z), swiglu_word(g.w, u.w));
 }
 
-// kRep: the scales go to the replicated layout of the forward GEMM's B operand
-// (quantize_nvfp4_weights): per 256 rows and 64-deep step a 4096-byte block
-// [tile0 x 4][tile1 x 4], tile0 / tile1 the 512-byte tiles of the block's rows
-// 0..127 / 128..255; each 4-scale word is stored four times.  The rows go in
-// units of eight, rows 2u and 2u + 1 of each 32-row quarter of a 128-row group
-// (u < 16): for one 64-deep step their words fill one 32-byte sector of each
-// copy.  A unit's words collect in shared memory and leave after its eighth row
-// as 16-byte stores that fill whole sectors.  Storing each word's four copies
-// directly (four 4-byte stores into four partly written sectors) measured 1.5x
-// slower for k = 7168.
 // kSwiGLU: the row is produced from a gate/up row [g (k values) | u (k values)]
 // staged whole in shared memory: h = silu(g) * u rounded to bf16, optionally
 // written to h_out, then quantized exactly as a bf16 input row would be.
-template <int R, bool kRep, bool kSwiGLU>
+template <int R, bool kSwiGLU>
 __global__ void __launch_bounds__(kNvMaxThreads, 4)
     nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
                           int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
@@ -251,16 +241,8 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
   const int64_t first = blockIdx.x;
   const int64_t stride = gridDim.x;
   const int64_t c4 = (nblk + 3) & ~3;
-  const int nw = nblk / 4;  // kRep: scale words per row
-  // kRep: words of the current unit's eight rows, [row of the unit][word]
-  uint32_t *unit_words = reinterpret_cast<uint32_t *>(g_tiles + num_groups + 1);
   // i-th row this CTA quantizes
-  auto row_at = [&](int64_t i) -> int64_t {
-    if (!kRep) return first + i * stride;
-    const int64_t unit = first + (i >> 3) * stride;
-    const int j = static_cast<int>(i & 7);
-    return (unit >> 4) * 128 + (unit & 15) * 2 + (j & 1) + 32 * (j >> 1);
-  };
+  auto row_at = [&](int64_t i) -> int64_t { return first + i * stride; };
 
   if (tid == 0) {
     abort_flag = 0;
@@ -294,7 +276,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
   uint32_t parity = 0;
   int g_cur = 0;  // thread 0: group of the current row (activations)
   int64_t row = row_at(0);
-  for (; row < rows; ++i, row = kRep ? row_at(i) : row + stride) {
+  for (; row < rows; ++i, row += stride) {
     const bool ok = mbar_wait(&bars[s], parity, &abort_flag, status);
     const uint8_t *buf = nv_smem + static_cast<size_t>(s) * row_bytes;
     uint4 a[R], b[R];
@@ -325,17 +307,15 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, m);
     if (lane == 0) part[i & 1][warp] = wmax;
     if (tid == 0) {
-      if (!kRep) {
-        // rows only increase here (first + i stride): move the group cursor forward
-        while (g_cur + 1 < num_groups && g_off[g_cur + 1] <= row) ++g_cur;
-        const int g = g_cur;
-        const int64_t prow = 128 * static_cast<int64_t>(g_tiles[g]) + (row - g_off[g]);
-        sf_row_of[i & 1] = sf_offset(prow, 0, c4);
-      }
+      // rows only increase here (first + i stride): move the group cursor forward
+      while (g_cur + 1 < num_groups && g_off[g_cur + 1] <= row) ++g_cur;
+      const int g = g_cur;
+      const int64_t prow = 128 * static_cast<int64_t>(g_tiles[g]) + (row - g_off[g]);
+      sf_row_of[i & 1] = sf_offset(prow, 0, c4);
     }
     if (__syncthreads_or(!ok)) break;  // every block of stage s is in registers: refill it
     if (tid == 0) {
-      const int64_t next = kRep ? row_at(i + stages) : row + stages * stride;
+      const int64_t next = row + stages * stride;
       if (next < rows) {
         fence_proxy_async_shared();
         mbar_arrive_expect_tx(&bars[s], row_bytes);
@@ -348,7 +328,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     }
     uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, lane < nwarps ? part[i & 1][lane] : 0u);
     if (tensor_amax != nullptr) amax_bits = __float_as_uint(*tensor_amax) >> 16;  // standard NVFP4: one scale
-    uint8_t *sf_row = kRep ? sf : sf + sf_row_of[i & 1];  // kRep stores through unit_words
+    uint8_t *sf_row = sf + sf_row_of[i & 1];
     uint8_t *codes_row = codes + row * (k / 2);
     const float amax = bf16_bits_to_float(amax_bits);
     const float s_t = (amax_bits == 0) ? 0.0f : per_token_scale(amax);
@@ -393,11 +373,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
         // stores them as one word
         const uint32_t pair = __byte_perm(sb, __shfl_down_sync(0xFFFFFFFFu, sb, 1), 0x0040);
         const uint32_t word = __byte_perm(pair, __shfl_down_sync(0xFFFFFFFFu, pair, 2), 0x5410);  // lanes 4g
-        if (kRep) {
-          if ((lane & 3) == 0 && blk < nblk) unit_words[(i & 7) * nw + (blk >> 2)] = word;
-        } else if ((lane & 3) == 0 && blk < nblk) {
-          *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = word;
-        }
+        if ((lane & 3) == 0 && blk < nblk) *reinterpret_cast<uint32_t *>(sf_row + (blk >> 2) * 512) = word;
       }
     };
     if (s_t >= 0x1p-67f) {
@@ -406,26 +382,13 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
       code_blocks(std::false_type{});
     }
     if (tid == 0) row_scale[row] = s_t;
-    if (kRep && (i & 7) == 7) {
-      // the unit's last row: write its words out, one 16-byte half-sector per
-      // thread and step (the next row's barrier orders the reuse of unit_words)
-      __syncthreads();
-      const int64_t r0 = row - 97;  // row 2u of the first quarter (this row is 2u + 1 + 96)
-      uint8_t *unit_sf = sf + (r0 / 256) * (k / 64) * 4096 + ((r0 % 256) / 128) * 2048 + (r0 % 32) * 16;
-      for (int idx = tid; idx < nw * 8; idx += T) {
-        const int w = idx >> 3, copy = (idx >> 1) & 3, half = idx & 1;
-        const uint4 v = make_uint4(unit_words[half * nw + w], unit_words[(2 + half) * nw + w],
-                                   unit_words[(4 + half) * nw + w], unit_words[(6 + half) * nw + w]);
-        *reinterpret_cast<uint4 *>(unit_sf + static_cast<int64_t>(w) * 4096 + 512 * copy + 16 * half) = v;
-      }
-    }
   }
   if (row < rows && tid == 0) {
     // gave up on a stage: wait (bounded) for the copies still in flight into this
     // CTA's shared memory before it exits
     const uint64_t t0 = globaltimer();
     for (int j = 0; j < stages && row_at(i + j) < rows; ++j) {
-      while (!mbar_try_wait(&bars[s], parity) && globaltimer() - t0 < kWaitLimitNs) {
+      while (!mbar_try_wait(&bars[s], parity) && globaltimer() - t0 < kDrainLimitNs) {
       }
       if (++s == stages) {
         s = 0;
@@ -439,21 +402,20 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
 // / R rounded up to warps.  CTAs per SM: as many as 1024 threads and the
 // shared-memory budget allow with at least 3 stages each; stages: the rest of
 // the budget, 3 to 16 rows.
-template <int R, bool kRep, bool kSwiGLU>
+template <int R, bool kSwiGLU>
 static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   const int64_t nblk = a.k / 16;
   const int64_t row_bytes = a.k * (kSwiGLU ? 4 : 2);
   const int threads = static_cast<int>(((nblk + R - 1) / R + 31) / 32 * 32);
-  const int64_t unit_bytes = kRep ? a.k / 2 : 0;  // kRep: 8 rows x k/64 scale words
-  const int64_t fixed = 1024 + 8 * (a.num_groups + 1) + unit_bytes;
+  const int64_t fixed = 1024 + 8 * (a.num_groups + 1);
   int per_sm = 1024 / threads;
   if (per_sm > 16) per_sm = 16;
   while (per_sm > 1 && per_sm * (static_cast<int64_t>(nv_smem_bytes(3, row_bytes, 0)) + fixed) > kNvSmemBudget)
     --per_sm;
   int64_t stages = (kNvSmemBudget / per_sm - fixed) / (row_bytes + 8);
   stages = stages < 3 ? 3 : (stages > 16 ? 16 : stages);
-  const size_t smem = nv_smem_bytes(static_cast<int>(stages), row_bytes, a.num_groups) + unit_bytes;
-  auto kernel = nvfp4_pertoken_kernel<R, kRep, kSwiGLU>;
+  const size_t smem = nv_smem_bytes(static_cast<int>(stages), row_bytes, a.num_groups);
+  auto kernel = nvfp4_pertoken_kernel<R, kSwiGLU>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int64_t cap = static_cast<int64_t>(a.num_sms) * per_sm;
@@ -507,9 +469,8 @@ cudaError_t launch_quantize_nvfp4_pertensor(const LaunchNvfp4 &a, float *tensor_
 // thread are slower).  The SwiGLU rows (twice the bytes per block) keep one block
 // per thread up to 256 blocks, measured 4% faster there.
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
-  if (a.swiglu) return a.k / 16 > kNvMaxThreads ? launch_nvfp4<2, false, true>(a) : launch_nvfp4<1, false, true>(a);
-  if (a.replicated_sf) return launch_nvfp4<2, true, false>(a);
-  return launch_nvfp4<2, false, false>(a);
+  if (a.swiglu) return a.k / 16 > kNvMaxThreads ? launch_nvfp4<2, true>(a) : launch_nvfp4<1, true>(a);
+  return launch_nvfp4<2, false>(a);
 }
 
 }  // namespace fme

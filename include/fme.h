@@ -6,8 +6,6 @@
  *   quantize_nvfp4_pertoken   NVFP4 variant of the forward: E2M1 codes, one E4M3
  *                             scale per 16 values along K, one FP32 scale per token.
  *   quantize_nvfp4_pertensor  standard NVFP4 (one FP32 scale per tensor), the comparator.
- *   quantize_nvfp4_weights    the same quantization of the stacked expert weights,
- *                             scales written in the forward GEMM's B-operand layout.
  *   swiglu_quantize_nvfp4     silu(gate) * up of the gate/up output, quantized as above.
  *   moe_route (moe_route_noalloc), permute_quantize_nvfp4, permute_quantize_mxfp8,
  *   moe_combine               grouping the routed tokens by expert (quantizing
@@ -143,30 +141,6 @@ fme_status quantize_nvfp4_pertoken(const void *x, int64_t rows, int64_t k, const
 fme_status quantize_nvfp4_pertensor(const void *x, int64_t rows, int64_t k, const int32_t *offsets,
                                     int32_t num_groups, uint8_t *codes, uint8_t *sf, float *row_scale,
                                     float *tensor_amax, int32_t *dev_status, void *stream);
-
-/*
- * quantize_nvfp4_weights -- quantize_nvfp4_pertoken of the stacked expert weights
- * W [rows x k] (one group), for the B operand of grouped_gemm_fwd_nvfp4.  Codes
- * and row scales are byte-identical to quantize_nvfp4_pertoken; the E4M3 block
- * scales go to the B-operand layout instead of the tiled one:
- *   for each 256-row block rb and each 64-deep step a (4 scales per row), a
- *   4096-byte block at offset (rb * (k/64) + a) * 4096 holding [T0 T0 T0 T0 T1 T1
- *   T1 T1], where T0 / T1 are the 512-byte tiles of the tiled layout for rows
- *   0..127 / 128..255 of the block (row i's 4 scales at (i % 32) * 16 +
- *   ((i % 128) / 32) * 4).
- * The four copies are the tensor core's 4x lane replication of B's scales, laid
- * out so that one 128-lane x 256-bit tensor-memory copy moves a step's scales
- * (two narrow copies otherwise); the weights' scale bytes grow from k/16 to k/4
- * per row.
- *
- *   x          device bf16 [rows x k]
- *   rows, k    rows a multiple of 256; k a multiple of 256, 256 <= k <= 8192
- *   codes      device uint8 [rows x k/2]
- *   sf         device uint8, fme_sf_bytes_nvfp4_weights(rows, k) bytes
- *   row_scale  device float [rows]
- */
-fme_status quantize_nvfp4_weights(const void *x, int64_t rows, int64_t k, uint8_t *codes, uint8_t *sf,
-                                  float *row_scale, int32_t *dev_status, void *stream);
 
 /*
  * swiglu_quantize_nvfp4 -- the activation between the forward GEMMs fused with
@@ -348,8 +322,10 @@ fme_status swiglu_backward_quantize_mxfp8(const void *gate_up, const void *dh, i
  * No split over K: a row's output does not depend on any other row.
  *
  *   a_codes, a_sf, a_scale  quantize_nvfp4_pertoken of X [m x k] with these offsets
- *   b_codes, b_sf, b_scale  quantize_nvfp4_weights of W [num_experts * n x k]
- *                           (expert e's rows are e*n .. e*n+n-1)
+ *   b_codes, b_sf, b_scale  quantize_nvfp4_pertoken of W [num_experts * n x k] as
+ *                           one group (offsets NULL): expert e's rows are
+ *                           e*n .. e*n+n-1, its scales the tiled layout's
+ *                           128-row blocks e*n/128 ..
  *   offsets        device int32 [num_experts + 1], rows of X per expert
  *   m, n, k        n a multiple of 256; k a multiple of 256
  *   y              device bf16 [m x n]
@@ -442,13 +418,10 @@ int64_t fme_colwise_ld(int64_t rows, int32_t num_groups);
 /* Bytes of moe_route's workspace (at least 16). */
 int64_t fme_route_workspace_bytes(int64_t tokens, int32_t top_k, int32_t num_experts);
 
-/* Bytes of the B-operand scale buffer written by quantize_nvfp4_weights (0 for
- * rows not a multiple of 256 or k not a multiple of 64). */
-int64_t fme_sf_bytes_nvfp4_weights(int64_t rows, int64_t k);
-
-/* Synchronises `stream`, copies *dev_status to the host and maps it to a status:
- * FME_OK, FME_ERR_DEVICE_BAD_OFFSETS or FME_ERR_DEVICE_TIMEOUT.  `raw` (may be
- * NULL) receives the raw bits. */
+/* Synchronises `stream`, copies *dev_status to the host and maps it to a status,
+ * the first of these whose bit is set: FME_ERR_DEVICE_BAD_OFFSETS,
+ * FME_ERR_DEVICE_BAD_INDEX, FME_ERR_DEVICE_TIMEOUT; FME_OK when none is.  `raw`
+ * (may be NULL) receives the raw bits. */
 fme_status fme_read_device_status(const int32_t *dev_status, void *stream, int32_t *raw);
 
 /* Static text for a status code. */

@@ -37,21 +37,6 @@ def unswizzle(sf_flat: np.ndarray, rows: int, c_logical: int, offsets=None) -> n
     return np.asarray(sf_flat)[idx]
 
 
-def unswizzle_weights(sf_flat: np.ndarray, rows: int, k: int) -> np.ndarray:
-    """B-operand scale bytes (quantize_nvfp4_weights) -> logical [rows x k/16]
-    matrix; asserts that the four copies of every tile agree."""
-    steps = k // 64
-    blk = np.asarray(sf_flat)[: (rows // 256) * steps * 4096].reshape(rows // 256, steps, 2, 4, 512)
-    assert (blk == blk[:, :, :, :1, :]).all(), "the four copies of a scale tile differ"
-    tiles = blk[:, :, :, 0, :]                           # [rb, step, half, 512]
-    i = np.arange(128)
-    cell = (i % 32) * 16 + (i // 32) * 4                 # row i's 4 scales in a 512-byte tile
-    out = np.empty((rows // 256, 2, 128, steps, 4), np.uint8)
-    for j in range(4):
-        out[..., j] = tiles[:, :, :, cell + j].transpose(0, 2, 3, 1)
-    return out.reshape(rows, steps * 4)
-
-
 def to_np(t) -> np.ndarray:
     return t.detach().cpu().numpy()
 

@@ -24,7 +24,7 @@ def declared_functions():
 
 def test_header_declares_the_five_calls():
     names = declared_functions()
-    for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_pertensor", "quantize_nvfp4_weights", "swiglu_quantize_nvfp4", "quantize_mxfp8",
+    for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_pertensor", "swiglu_quantize_nvfp4", "quantize_mxfp8",
                  "grouped_gemm_fwd_nvfp4",
                  "grouped_gemm_fwd_mxfp8",
                  "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8", "moe_route", "permute_quantize_nvfp4",
@@ -47,8 +47,6 @@ def test_helpers_closed_forms(lib):
     assert fme.sf_padded_rows(16384, 32) == 20352
     assert fme.sf_bytes(16384, 7168, 16, 32) == 20352 * 448
     assert fme.sf_bytes(100, 96, 32, 1) == 128 * 4          # 3 scales per row, rounded up to 4
-    assert fme.sf_bytes_nvfp4_weights(32 * 4096, 7168) == 32 * 16 * 112 * 4096   # k/4 bytes per row
-    assert fme.sf_bytes_nvfp4_weights(100, 256) == 0
     assert fme.colwise_ld(65536, 32) == ((65536 + 127 * 32) // 128) * 128
     assert lib.fme_version().startswith(b"fme")
     # route workspace: ceil(tokens * top_k / 1024) chunks x E counters, at least 16 bytes
@@ -84,14 +82,6 @@ def test_host_argument_checks(lib):
     assert qt(good, 10, 256, None, 1, good, good, good, None, None, _stream()) == 1    # no amax word
     assert qt(good, 10, 256, None, 3, good, good, good, good, None, _stream()) == 1    # groups without offsets
     assert qt(good, 10, 256, None, 1, good, good, good, odd, None, _stream()) == 2
-    qw = lib.quantize_nvfp4_weights
-    assert qw(good, -256, 256, good, good, good, None, _stream()) == 1
-    assert qw(good, 100, 256, good, good, good, None, _stream()) == 3     # rows % 256
-    assert qw(good, 256, 192, good, good, good, None, _stream()) == 3     # k % 256
-    assert qw(good, 256, 8448, good, good, good, None, _stream()) == 3
-    assert qw(None, 256, 256, good, good, good, None, _stream()) == 1
-    assert qw(good, 256, 256, good, odd, good, None, _stream()) == 2
-    assert qw(good, 0, 256, None, None, None, None, _stream()) == 0       # nothing to do
     sq = lib.swiglu_quantize_nvfp4
     assert sq(good, 10, 96, None, 1, good, good, good, None, None, _stream()) == 3      # inter % 64
     assert sq(good, 10, 8256, None, 1, good, good, good, None, None, _stream()) == 3

@@ -48,20 +48,6 @@ def _tiled_rows(sf_flat, prow, c_logical):
     return np.asarray(sf_flat)[sf_index(prow[:, None], c[None, :], c_logical)]
 
 
-def _replicated_rows(sf_flat, rows, k):
-    """Logical scale rows from the forward GEMM's replicated B-operand layout, after
-    checking that the four copies of every sampled word agree."""
-    r = rows[:, None]
-    c = np.arange(k // 16)[None, :]
-    base = (r // 256) * (k // 64) * 4096 + ((r % 256) // 128) * 2048 + (r % 32) * 16 + ((r % 128) // 32) * 4
-    idx = base + (c // 4) * 4096 + c % 4
-    flat = np.asarray(sf_flat)
-    copies = [flat[idx + 512 * j] for j in range(4)]
-    for j in range(1, 4):
-        assert np.array_equal(copies[0], copies[j]), f"copy {j} of the replicated scales differs"
-    return copies[0]
-
-
 def _cols(t, lo, hi, channels):
     """Rows lo..hi-1 of a device tensor restricted to the given columns."""
     import torch
@@ -81,7 +67,7 @@ def _check_nvfp4(orc, x, q, rows, prow, what):
     got_scale = to_np(scale[idx])
     assert np.array_equal(got_scale.view(np.uint32), oscale.view(np.uint32)), f"{what}: per-token scales differ"
     flat = to_np(sf)
-    got_sf = _replicated_rows(flat, rows, k) if prow is None else _tiled_rows(flat, prow, k // 16)
+    got_sf = _tiled_rows(flat, prow, k // 16)
     assert np.array_equal(got_sf, osf), f"{what}: block scales differ at {np.argwhere(got_sf != osf)[:5].tolist()}"
     bad = np.argwhere(got_codes != oc)
     assert bad.size == 0, f"{what}: {len(bad)} code bytes differ, first {bad[:5].tolist()}"
@@ -99,11 +85,10 @@ def test_full_size_nvfp4_weights(step, orc):
     rng = np.random.default_rng(12)
     for w, q in ((step.w_gu, step.wguq), (step.w_d, step.wdq)):
         n = w.shape[0]
-        # whole 8-row units at both ends and in the middle, plus random rows
-        unit = np.array([0, 1, 32, 33, 64, 65, 96, 97])
-        rows = np.unique(np.concatenate([unit, n - 128 + 30 + unit, (n // 2) + 14 + unit,
+        # rows at both ends, around a 128-row block boundary in the middle, and random rows
+        rows = np.unique(np.concatenate([[0, 1, 31, 32, 127, n - 1], (n // 2) + np.arange(-2, 3),
                                          rng.integers(0, n, size=40)]))
-        _check_nvfp4(orc, w, q, rows, None, f"weights {tuple(w.shape)}")
+        _check_nvfp4(orc, w, q, rows, rows, f"weights {tuple(w.shape)}")  # one group: padded row = row
 
 
 def test_full_size_mxfp8_rowwise(step, orc):

@@ -38,7 +38,7 @@ def gpu_fwd(fme, x, w, offsets, n, k):
     st = _status()
     off = _i32(offsets)
     a = fme.quantize_nvfp4_pertoken(x, off, status=st)
-    b = fme.quantize_nvfp4_weights(w, status=st)
+    b = fme.quantize_nvfp4_pertoken(w, status=st)
     y = fme.grouped_gemm_fwd_nvfp4(*a, *b, off, n, k, status=st)
     _ok(fme, st)
     return y
@@ -267,7 +267,7 @@ def test_gemm_bad_offsets_status(fme):
     w = bf16_tensor(synth.normal_bits((512, 256), 0.02, seed=2))
     st = _status()
     a = fme.quantize_nvfp4_pertoken(x, status=st)
-    b = fme.quantize_nvfp4_weights(w, status=st)
+    b = fme.quantize_nvfp4_pertoken(w, status=st)
     bad = torch.tensor([0, 50, 40], dtype=torch.int32, device="cuda")
     fme.grouped_gemm_fwd_nvfp4(*a, *b, bad, 256, 256, status=st)
     code, raw = fme.read_device_status(st)
@@ -395,7 +395,7 @@ def test_fwd_pertensor_comparator(fme, orc):
     loud = synth.bf16_bits(synth.bf16_float(x_bits[:128]) * np.float32(64.0))
     st = _status()
     w = bf16_tensor(w_bits)
-    wq = fme.quantize_nvfp4_weights(w, status=st)
+    wq = fme.quantize_nvfp4_pertoken(w, status=st)
 
     def fwd(xb, per_tensor):
         off = _i32([0, xb.shape[0]])

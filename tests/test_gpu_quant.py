@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 from fp8_moe_expert_gb300 import synth
-from tests.fmetest import bf16_tensor, to_np, unswizzle, unswizzle_weights
+from tests.fmetest import bf16_tensor, to_np, unswizzle
 from tests.golden import read_cases
 
 pytestmark = pytest.mark.gpu
@@ -222,24 +222,6 @@ def test_near_midpoint_rows_are_hard():
     assert np.array_equal(amax_b[:, 0], np.abs(v[:, 0, 0]))
     assert (np.abs(v[..., 1:15]) <= amax_b[..., None]).all()
     assert (x.reshape(32512, 128, 16)[..., 15] == 0x8000).all()
-
-
-@pytest.mark.parametrize("rows,k", [(256, 256), (512, 2048), (32 * 256, 7168)])
-def test_nvfp4_weights_layout(fme, orc, rows, k):
-    """quantize_nvfp4_weights: codes and row scales identical to the per-token
-    call, block scales equal to the oracle's, in the replicated B-operand layout
-    (every tile stored four times)."""
-    w_bits = synth.normal_bits((rows, k), 0.02, seed=rows + k)
-    w = bf16_tensor(w_bits)
-    st = _status()
-    codes, sf, scale = fme.quantize_nvfp4_weights(w, status=st)
-    assert fme.read_device_status(st)[0] == 0
-    oc, osf, oscale = orc.quant_nvfp4(w_bits)
-    assert np.array_equal(to_np(codes), oc)
-    assert np.array_equal(to_np(scale).view(np.uint32), oscale.view(np.uint32))
-    assert np.array_equal(unswizzle_weights(to_np(sf), rows, k), osf)
-    pc, psf, ps = run_nvfp4(fme, w_bits)
-    assert np.array_equal(pc, to_np(codes)) and np.array_equal(ps, to_np(scale))
 
 
 def test_nvfp4_batch_invariance_and_causality(fme, orc):
