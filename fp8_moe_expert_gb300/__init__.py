@@ -398,7 +398,15 @@ def moe_route(topk_ids, num_experts, *, offsets=None, row_of=None, src_row=None,
 def moe_route_noalloc(topk_ids, num_experts, offsets, row_of, src_row, *, status=None, stream=None):
     """moe_route into caller-owned outputs, with the library's static counters as
     the workspace: neither this call nor the library allocates memory."""
+    import torch
+
     tokens, top_k = topk_ids.shape
+    for name, t, n in (("topk_ids", topk_ids, tokens * top_k), ("offsets", offsets, num_experts + 1),
+                       ("row_of", row_of, tokens * top_k), ("src_row", src_row, tokens * top_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.numel() != n:
+            raise ValueError(f"moe_route_noalloc: {name} must be a contiguous int32 CUDA tensor of {n} elements")
+        if t.device != topk_ids.device:
+            raise ValueError(f"moe_route_noalloc: {name} is on {t.device}, topk_ids on {topk_ids.device}")
     st = lib().moe_route_noalloc(_ptr(topk_ids), tokens, top_k, num_experts, _ptr(offsets), _ptr(row_of),
                                  _ptr(src_row), _ptr(status), _stream(stream))
     _check(st, "moe_route_noalloc")

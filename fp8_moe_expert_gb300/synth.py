@@ -6,7 +6,7 @@ oracle take their inputs from here, and nothing else is shared between them.
 
 Workloads follow the expert shapes of "Scaling and Optimizing Frontier Model
 Training" ("MXFP8 expert kernels": 32 experts per rank, hidden 7168,
-intermediate 2048).  The recipe of each workload is written out in the design doc.
+intermediate 2048).  Each generator's docstring states its recipe.
 
 Two back ends:
   * numpy (``np.random.default_rng(seed)``, PCG64) for everything the CPU
@@ -35,6 +35,13 @@ def bf16_bits(a) -> np.ndarray:
     if nan.any():
         out[nan] = 0x7FC0
     return out
+
+
+def bf16_bits_np(t) -> np.ndarray:
+    """A torch bf16 tensor (any device) -> its uint16 bit patterns as numpy."""
+    import torch
+
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
 def bf16_float(bits) -> np.ndarray:

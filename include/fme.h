@@ -112,6 +112,12 @@ typedef int32_t fme_status;
  * whose scale code is 0 gets codes 0.  Rows are independent: a token's outputs
  * do not depend on any other row.
  *
+ * Passage: "Composer 2 Technical Report" (papercache.org summary), section 6.1,
+ * the NVFP4-variant paragraph (E2M1 values, an E4M3 scale per 16-element block,
+ * an FP32 scale per token) and the hardware-math paragraph (IEEE-compliant
+ * division when quantizing to this format); "Cursor Composer 2 report deep dive",
+ * section 1 (per-token scales: no batch variance, no leakage from later tokens).
+ *
  *   x          device bf16 [rows x k]
  *   rows, k    rows >= 0; k a multiple of 64, 64 <= k <= 8192
  *   offsets    device int32 [num_groups + 1] or NULL (see "Grouped rows");
@@ -197,7 +203,11 @@ fme_status moe_route(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int
  * ceil(tokens * top_k / 1024) * num_experts must not exceed it
  * (FME_ERR_UNSUPPORTED_SHAPE otherwise).  Same outputs, bit for bit, as
  * moe_route.  Calls share that array: they must be ordered on the device (one
- * stream, or streams joined by events), never concurrent.
+ * stream, or streams joined by events), never concurrent.  The array is part of
+ * the library's device code: it is created when that code is loaded on a
+ * device, which under CUDA's lazy module loading is the first call into
+ * libfme.so on that device (any call).  Make that first call before relying on
+ * the no-allocation property; the array then lives until the process exits.
  */
 #define FME_ROUTE_STATIC_WORDS (1 << 20)
 fme_status moe_route_noalloc(const int32_t *topk_ids, int64_t tokens, int32_t top_k, int32_t num_experts,
@@ -250,6 +260,12 @@ fme_status moe_combine(const void *y, int64_t rows_y, const int32_t *row_of, con
  * q = E4M3(x / X), round to nearest even, saturating at 448.  X is a power of
  * two, so x / X is exact and the fast division the pages allow for MXFP8 gives
  * the same codes.
+ *
+ * Passage: "Composer 2 Technical Report", section 6.1, the MXFP8 paragraph of the
+ * MoE backward (E4M3 values, an E8M0 scale per 32 elements) and the hardware-math
+ * paragraph (a fast divide is acceptable for MXFP8); "Scaling and Optimizing
+ * Frontier Model Training", "MXFP8 expert kernels".  The column-wise layout (blocks
+ * along tokens, restarted at each expert) feeds the weight gradient.
  *
  * axis | FME_MX_SCALE_CEIL: the round-up scale variant, X = 2^ceil(log2(amax /
  * 448)) (code clamp(ceil(log2(amax / 448)) + 127, 0, 254)), the smallest power of
@@ -321,6 +337,12 @@ fme_status swiglu_backward_quantize_mxfp8(const void *gate_up, const void *dh, i
  * epilogue applies (acc * S_x[t]) * S_w[e, n] in fp32 and rounds to bf16.
  * No split over K: a row's output does not depend on any other row.
  *
+ * Passage: "Composer 2 Technical Report", section 6.1, the NVFP4-variant paragraph
+ * (the per-token scale applied at the cost of GEMM-epilogue latency) and the
+ * block-scaled tensor-core MMA sentence (dequantization inside the
+ * systolic-array multiply); "Scaling and Optimizing Frontier Model Training",
+ * "MXFP8 expert kernels" (grouped GEMMs over the experts' routed tokens).
+ *
  *   a_codes, a_sf, a_scale  quantize_nvfp4_pertoken of X [m x k] with these offsets
  *   b_codes, b_sf, b_scale  quantize_nvfp4_pertoken of W [num_experts * n x k] as
  *                           one group (offsets NULL): expert e's rows are
@@ -360,6 +382,10 @@ fme_status grouped_gemm_fwd_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, c
  * the row-wise MXFP8 of dY [m x k] and B the column-wise MXFP8 of the stacked
  * weights W [num_experts * k x n] (one group), whose codes are [n x ldb].
  *
+ * Passage: "Composer 2 Technical Report", section 6.1, the MXFP8 paragraph of the
+ * MoE backward; "Scaling and Optimizing Frontier Model Training", "MXFP8 expert
+ * kernels" (MXFP8 grouped GEMMs in the expert layers' backward).
+ *
  *   a_codes, a_sf  quantize_mxfp8(ROWWISE) of A [m x k] with these offsets
  *   b_codes, b_sf  codes [n x ldb] and their scales (tiled, rows = n); expert e
  *                  uses columns e*k .. e*k+k-1, so ldb >= num_experts * k
@@ -379,10 +405,14 @@ fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
  * of H (same offsets) this is the weight gradient dW_e = dY_e^T H_e.  An
  * expert with no rows gets an all-zero Y_e.
  *
+ * Passage: "Composer 2 Technical Report", section 6.1, the MXFP8 paragraph of the
+ * MoE backward; "Scaling and Optimizing Frontier Model Training", "MXFP8 expert
+ * kernels" (MXFP8 grouped GEMMs in the expert layers' backward).
+ *
  *   a_codes, a_sf, lda  quantize_mxfp8(COLWISE) of dY [rows x m]: codes [m x lda]
  *   b_codes, b_sf, ldb  quantize_mxfp8(COLWISE) of H [rows x n]:  codes [n x ldb]
  *   padded_offsets  device int32 [num_experts + 1] written by those calls
- *   m, n            m a multiple of 128, n a multiple of 256
+ *   m, n            m and n multiples of 256, at most 65536
  *   y               device bf16 [num_experts x m x n]
  */
 fme_status grouped_gemm_wgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, int64_t lda,

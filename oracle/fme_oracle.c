@@ -39,7 +39,8 @@
  *     weight * y[row], each product and sum one fp32 operation, rounded once to
  *     bf16 at the end.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent (the plainest reading the rest of
+ * the pages supports, each named here):
  *   - per-token decode scale S_t = amax_t / (6 * 448), fp32, IEEE division;
  *   - block scale sb = RNE-satfinite-E4M3(amax_b / fl32(6 * S_t));
  *   - element code q = RNE-satfinite-E2M1(fl32(x / fl32(dec(sb) * S_t)));

@@ -41,11 +41,7 @@ def to_np(t) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
-def bf16_bits_np(t) -> np.ndarray:
-    """torch bf16 tensor -> uint16 bit patterns (numpy)."""
-    import torch
-
-    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+from fp8_moe_expert_gb300.synth import bf16_bits_np  # noqa: E402,F401  (re-exported for the tests)
 
 
 def bf16_tensor(bits: np.ndarray, device="cuda"):
