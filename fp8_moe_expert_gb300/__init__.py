@@ -22,6 +22,16 @@ MX_SCALE_CEIL = 0x100
 DEV_TIMEOUT = 0x1
 DEV_BAD_OFFSETS = 0x2
 DEV_BAD_INDEX = 0x4
+# status codes (fme_status) of include/fme.h
+OK = 0
+ERR_INVALID_ARGUMENT = 1
+ERR_MISALIGNED = 2
+ERR_UNSUPPORTED_SHAPE = 3
+ERR_UNSUPPORTED_DEVICE = 4
+ERR_CUDA = 5
+ERR_DEVICE_TIMEOUT = 6
+ERR_DEVICE_BAD_OFFSETS = 7
+ERR_DEVICE_BAD_INDEX = 8
 
 _lib = None
 _lock = threading.Lock()

@@ -26,7 +26,11 @@ constexpr int kMaxGroups = 1024;
 #ifndef FME_WAIT_LIMIT_NS
 #define FME_WAIT_LIMIT_NS 2000000000ull
 #endif
+#ifndef FME_WAIT_SPINS
+#define FME_WAIT_SPINS 32
+#endif
 constexpr uint64_t kWaitLimitNs = FME_WAIT_LIMIT_NS;
+constexpr int kWaitSpins = FME_WAIT_SPINS;  // barrier polls between two reads of the clock
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ void report(int32_t *status, int bits) {
@@ -61,6 +65,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// Counts `bytes` of the current phase's transaction as arrived without any copy
+// (for bytes that were expected but will never be sent).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -85,7 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < kWaitSpins; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
@@ -301,6 +312,37 @@ __device__ __forceinline__ void cluster_sync() {
 // thread's earlier global stores (measured: ~0.5 us per tile of the forward GEMM).
 __device__ __forceinline__ void arrive_remote_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Store to a 32-bit word of another CTA's shared memory; the reader sees it after
+// a barrier phase completed by arrive_remote_release and observed by
+// wait_acquire_cluster.
+__device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Arrive on another CTA's barrier after this thread's earlier memory operations
+// (release at cluster scope).
+__device__ __forceinline__ void arrive_remote_release(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Wait, up to limit_ns, for the phase of this CTA's barrier `bar` with the given
+// parity, acquiring at cluster scope what the arriving CTAs released.
+__device__ __forceinline__ bool wait_acquire_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
 }
 
 // 2-D tile load into this CTA's shared memory whose completion is counted on the

@@ -65,6 +65,8 @@ struct SharedStateMx {
   uint64_t acc_empty;
   uint64_t drain;
   uint64_t drain_cp[kCopiers];
+  uint64_t peer_fills_bar;  // the peer's producer has written peer_fills (leader)
+  uint32_t peer_fills;      // fills the peer's producer issued (leader)
   uint32_t tmem_base;
   int abort_flag;
   int ok_flag;
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.peer_fills_bar, 1);
     for (int i = 0; i < kCopiers; ++i) mbar_init(&s.drain_cp[i], 1);
     s.abort_flag = 0;
     fence_barrier_init();
@@ -163,16 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       if (stop) break;
     }
     // Every copy the pair issued lands before a CTA can exit (after an abort,
-    // stages may be filled that no MMA will read): the leader, whose barriers
-    // count both CTAs' bytes, waits for the last fill of each stage; the peer
-    // waits for the leader at the teardown's cluster barrier.  Fill f used stage
-    // f % S in phase (f / S) & 1.
-    if (rank == 0)
-      for (uint32_t j = 0; j < static_cast<uint32_t>(S) && j < filled; ++j) {
-        const uint32_t par = ((filled - 1 - j) / S) & 1;
-        mbar_drain(&s.sf_landed[j], par);
-        mbar_drain(&s.full[j], par);
-      }
+    // stages may be filled that no MMA will read).  All of them complete on the
+    // leader's barriers: its producer drains both rings from both producers'
+    // fill counts, before the teardown's cluster barrier releases the peer.
+    const uint32_t peer = exchange_fills(rank, filled, &s.peer_fills, &s.peer_fills_bar, p.status);
+    if (rank == 0) {
+      drain_pair_ring(s.sf_landed, S, filled, peer, C::kSfaBytes + C::kSfbBytes);
+      drain_pair_ring(s.full, S, filled, peer, kABytes + kBBytes);
+    }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------ MMA issuer (leader)
     uint32_t stage = 0, phase = 0, acc_phase = 0, buf = 0, buf_phase = 0;

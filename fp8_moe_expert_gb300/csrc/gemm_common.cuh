@@ -146,6 +146,48 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const Groups &s, in
   return tl;
 }
 
+// Wait, on the leader, until every copy either CTA of the pair issued into one
+// ring of stage barriers (`bars`, S stages) has landed.  The leader arms fill f
+// of the ring (stage f % S, phase (f / S) & 1) for both CTAs' bytes; each CTA's
+// copies complete on the leader's barrier.  `own` and `peer` are the fills each
+// producer issued.  A fill is read by the MMAs only once both halves landed, and
+// a producer reuses a stage only after the MMAs released it, so both counts lie
+// in [c, c + S] for the c fills consumed, and only the latest fill of a stage can
+// still be in flight.  After an abort the two counts may differ: a fill issued by
+// the peer alone was never armed, so the leader arms it for the peer's bytes; a
+// fill issued by the leader alone waits for peer bytes that will never come, so
+// the leader counts them as arrived.  Each wait is bounded (kDrainLimitNs).
+__device__ inline void drain_pair_ring(uint64_t *bars, int S, uint32_t own, uint32_t peer, uint32_t peer_bytes) {
+  const uint32_t last = own > peer ? own : peer;
+  for (uint32_t j = 0; j < static_cast<uint32_t>(S) && j < last; ++j) {
+    const uint32_t f = j + S * ((last - 1 - j) / S);  // latest fill of stage j
+    if (f >= own)
+      mbar_arrive_expect_tx(&bars[j], peer_bytes);
+    else if (f >= peer)
+      mbar_complete_tx(&bars[j], peer_bytes);
+    mbar_drain(&bars[j], (f / S) & 1);
+  }
+}
+
+// The producers' hand-over at the end of their loops: the peer's producer sends
+// its fill count to the leader (`fills_word` and `fills_bar` are the leader's
+// shared word and barrier, initialised with one arrival); the leader's producer
+// returns the peer's count, or its own if the count does not come within the
+// time any of the peer's waits can take (reported as a time-out).
+__device__ inline uint32_t exchange_fills(int rank, uint32_t filled, uint32_t *fills_word, uint64_t *fills_bar,
+                                          int32_t *status) {
+  if (rank != 0) {
+    pair::st_remote_u32(pair::map_to_rank(fills_word, 0), filled);
+    pair::arrive_remote_release(pair::map_to_rank(fills_bar, 0));
+    return filled;
+  }
+  if (!pair::wait_acquire_cluster(fills_bar, 0, kWaitLimitNs + kDrainLimitNs)) {
+    report(status, kDevTimeout);
+    return filled;
+  }
+  return *reinterpret_cast<volatile uint32_t *>(fills_word);
+}
+
 // Build the tile tables (the same in both CTAs of a pair); returns false in
 // every thread for malformed offsets.  `ok_flag` is a shared int.
 template <GemmKind K>

@@ -82,6 +82,8 @@ struct SharedState {
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
+  uint64_t peer_fills_bar;  // the peer's producer has written peer_fills (leader)
+  uint32_t peer_fills;      // operand fills the peer's producer issued (leader)
   uint32_t tmem_base;
   int abort_flag;
   int ok_flag;
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.peer_fills_bar, 1);
     s.abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -253,15 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
         if (stop) break;
       }
       // Every copy this CTA issued lands before the CTA can exit (after an abort,
-      // stages may be filled that no MMA will read): wait for the last fill of
-      // each stage, the leader also for the pair's operands.  Fill f used stage
-      // f % S in phase (f / S) & 1; stage j was last filled by fill
-      // j + S * ((filled - 1 - j) / S).
-      for (uint32_t j = 0; j < static_cast<uint32_t>(S) && j < filled; ++j) {
-        const uint32_t par = ((filled - 1 - j) / S) & 1;
-        mbar_drain(&s.sf_landed[j], par);
-        if (rank == 0) mbar_drain(&s.full[j], par);
-      }
+      // stages may be filled that no MMA will read).  The scale tiles complete on
+      // this CTA's own barriers: wait for the last fill of each stage (fill f used
+      // stage f % S in phase (f / S) & 1).  The operands complete on the leader's
+      // barriers: its producer drains them from both producers' fill counts,
+      // before the teardown's cluster barrier releases the peer.
+      for (uint32_t j = 0; j < static_cast<uint32_t>(S) && j < filled; ++j)
+        mbar_drain(&s.sf_landed[j], ((filled - 1 - j) / S) & 1);
+      const uint32_t peer = exchange_fills(rank, filled, &s.peer_fills, &s.peer_fills_bar, p.status);
+      if (rank == 0) drain_pair_ring(s.full, S, filled, peer, kABytes + kBBytes);
     } else if (warp == kMmaWarp && lane == 0 && rank == 0) {
       // ------------------------------------------------ MMA issuer (leader)
       uint32_t stage = 0, phase = 0, acc_phase = 0, buf = 0, buf_phase = 0;
@@ -316,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
 
   // Teardown: the pair meets once the leader's MMAs are drained, every copy has
   // landed and every epilogue has read its accumulator; then both CTAs free
-  // tensor memory together.
+  // tensor memory together.  (Nothing but `tmem` is used past the roles: a value
+  // live across them would hold a register in every role's loop.)
   tc_fence_before();
   __syncthreads();
   __syncwarp();

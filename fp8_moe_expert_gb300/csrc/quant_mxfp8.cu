@@ -341,15 +341,27 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
         const int cell = (r & 31) * 16 + (r >> 5) * 4;
         const uint16_t v = *reinterpret_cast<const uint16_t *>(&sfr[cell + 2 * half]);
         const int64_t tcol = half ? t_u : t_g;
-        *reinterpret_cast<uint16_t *>(row_sf + (pt.j * (cols / 128) + tcol) * 512 + cell + 2 * odd) = v;
+        if (r < pt.valid)  // padding rows of the row-wise layout stay unwritten
+          *reinterpret_cast<uint16_t *>(row_sf + (pt.j * (cols / 128) + tcol) * 512 + cell + 2 * odd) = v;
       }
     } else {
       if (tid < 32) {
         const uint4 v = *reinterpret_cast<const uint4 *>(&sfs[tid * 16]);
         *reinterpret_cast<uint4 *>(sf_t + (static_cast<int64_t>(cb) * (ld / 128) + pt.j) * 512 + tid * 16) = v;
       } else if (kRows && tid < 64) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[(tid - 32) * 16]);
-        *reinterpret_cast<uint4 *>(row_sf + (pt.j * cblocks + cb) * 512 + (tid - 32) * 16) = v;
+        // tile row i holds the row-wise scale words of rows i, i + 32, i + 64, i + 96;
+        // padding rows (past the group's end) stay unwritten
+        const int i = tid - 32;
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sfr[i * 16]);
+        uint8_t *dst = row_sf + (pt.j * cblocks + cb) * 512 + i * 16;
+        if (i + 96 < pt.valid) {
+          *reinterpret_cast<uint4 *>(dst) = v;
+        } else {
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (i + 32 * q < pt.valid) *reinterpret_cast<uint32_t *>(dst + 4 * q) = w[q];
+        }
       }
     }
   };

@@ -65,8 +65,9 @@
  *      ((pr / 128) * (C4 / 4) + c / 4) * 512 + (pr % 32) * 16 + ((pr % 128) / 32) * 4 + c % 4
  *   i.e. 512-byte tiles of 128 rows x 4 scales, the order in which the tensor
  *   core's block-scale operand is copied into tensor memory.  Bytes of padding
- *   rows and padding columns are left unwritten.  fme_sf_bytes() gives the
- *   buffer size.
+ *   rows are left unwritten; a row's padding columns (C <= c < C4, only when C is
+ *   not a multiple of 4) are written as 0, with the row's last four scales.
+ *   fme_sf_bytes() gives the buffer size.
  */
 #ifndef FME_H
 #define FME_H

@@ -165,3 +165,12 @@ def test_binding_refuses_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(fme, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         fme.lib()
+
+
+def test_binding_status_constants_match_the_header():
+    import re
+
+    text = open(HEADER).read()
+    for name, value in re.findall(r"#define FME_((?:OK|ERR_\w+|DEV_\w+))\s+(0x[0-9a-fA-F]+|\d+)", text):
+        if name.startswith("DEV_") or name.startswith("ERR_") or name == "OK":
+            assert getattr(fme, name) == int(value, 0), name
