@@ -630,20 +630,17 @@ def run_e2e(step, calls, args, world):
 
 
 # --------------------------------------------------------- oracle (CPU) timing --
-def oracle_sample(step, counts, rows_per_gemm, cols, rng_seed=0):
-    """Time the CPU oracle on a sample of the step: `rows_per_gemm` token rows of
-    one expert through every GEMM (all output columns if cols is None, else
-    `cols` sampled output columns; only the weight rows or columns those need
-    are quantized), plus `rows_per_gemm` channel rows of that expert's wgrad.
-    Inputs are copied to the host before the clock starts.
-    Returns (seconds, gemm_flops, description)."""
+def oracle_host_sample(step, counts, rows_per_gemm, cols, rng_seed=0):
+    """Host inputs of one oracle sample of the step: `rows_per_gemm` token rows of
+    one expert through every GEMM (all output columns if cols is None, else `cols`
+    sampled output columns; only the weight rows or columns those need), plus
+    `rows_per_gemm` channel rows of that expert's wgrad.  Returns (host arrays,
+    column selections, description)."""
     import numpy as np
     import torch
 
-    import oracle
     from fp8_moe_expert_gb300.synth import bf16_bits_np
 
-    orc = oracle.Oracle()
     E, H, I = step.E, step.H, step.I
     off = np.concatenate([[0], np.cumsum(counts)])
     live = [g for g, c in enumerate(counts) if c >= 2 * rows_per_gemm]
@@ -655,40 +652,171 @@ def oracle_sample(step, counts, rows_per_gemm, cols, rng_seed=0):
     def colsel(n):
         return np.arange(n) if cols is None else np.sort(rng.choice(n, size=min(cols, n), replace=False))
 
-    c_gu, c_d, c_dg, c_wg = colsel(2 * I), colsel(H), colsel(I), colsel(I)
-    ch = np.sort(rng.choice(H, size=rows_per_gemm, replace=False))
+    sel = {"gu": colsel(2 * I), "d": colsel(H), "dg": colsel(I), "wg": colsel(I),
+           "ch": np.sort(rng.choice(H, size=rows_per_gemm, replace=False))}
     host = {
         "x": bf16_bits_np(step.x[ri]), "h": bf16_bits_np(step.h[ri]), "dy": bf16_bits_np(step.dy[ri]),
-        "wgu": bf16_bits_np(step.w_gu[g * 2 * I:(g + 1) * 2 * I][torch.from_numpy(c_gu).to(step.dev)]),
+        "wgu": bf16_bits_np(step.w_gu[g * 2 * I:(g + 1) * 2 * I][torch.from_numpy(sel["gu"]).to(step.dev)]),
         "wd": bf16_bits_np(step.w_d[g * H:(g + 1) * H]),
         "dy_e": bf16_bits_np(step.dy[off[g]:off[g + 1]]), "h_e": bf16_bits_np(step.h[off[g]:off[g + 1]]),
+        "H": H,
     }
     n_e = int(counts[g])
+    desc = (f"expert {g} ({n_e} rows): {len(r)} token rows through gate/up ({len(sel['gu'])} cols), down "
+            f"({len(sel['d'])} cols), dgrad ({len(sel['dg'])} cols); wgrad {len(sel['ch'])} x {len(sel['wg'])} "
+            f"over {n_e} rows; quantization of every operand row/column those need included")
+    return host, sel, desc
+
+
+def oracle_run_sample(task):
+    """The oracle on one host sample (oracle_host_sample's arrays), on this process's
+    core: every quantization those GEMM rows need, then the GEMMs.  Returns
+    (seconds, gemm flops).  Module level, so that a spawned pool can run it."""
+    import numpy as np
+
+    import oracle
+
+    host, sel = task
+    orc = oracle.Oracle()
+    H = host["H"]
+    n_e = host["dy_e"].shape[0]
     t0 = time.perf_counter()
     # forward, NVFP4
     a = orc.dequant_nvfp4(*orc.quant_nvfp4(host["x"]))
     b = orc.dequant_nvfp4(*orc.quant_nvfp4(host["wgu"]))
     orc.gemm_abt(a, b)
     a = orc.dequant_nvfp4(*orc.quant_nvfp4(host["h"]))
-    b = orc.dequant_nvfp4(*orc.quant_nvfp4(np.ascontiguousarray(host["wd"][c_d])))
+    b = orc.dequant_nvfp4(*orc.quant_nvfp4(np.ascontiguousarray(host["wd"][sel["d"]])))
     orc.gemm_abt(a, b)
-    # backward, MXFP8: dgrad (W_down column-wise along the 7168 axis)
+    # backward, MXFP8: dgrad (W_down column-wise along the hidden axis)
     a = orc.dequant_mxfp8(*orc.quant_mxfp8_rows(host["dy"]))
-    wcols = np.ascontiguousarray(host["wd"][:, c_dg])
-    ct, st, _ = orc.quant_mxfp8_cols(wcols, np.array([0, H]))
+    ct, st, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(host["wd"][:, sel["dg"]]), np.array([0, H]))
     orc.gemm_abt(a, orc.dequant_mxfp8(ct, st)[:, :H])
     # wgrad: dY_e and H_e column-wise over the expert's rows
     e_off = np.array([0, n_e])
-    ca, sa, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(host["dy_e"][:, ch]), e_off)
-    cb, sb, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(host["h_e"][:, c_wg]), e_off)
+    ca, sa, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(host["dy_e"][:, sel["ch"]]), e_off)
+    cb, sb, _ = orc.quant_mxfp8_cols(np.ascontiguousarray(host["h_e"][:, sel["wg"]]), e_off)
     orc.gemm_abt(orc.dequant_mxfp8(ca, sa), orc.dequant_mxfp8(cb, sb))
     secs = time.perf_counter() - t0
-    k = len(r)
-    flops = 2 * k * (len(c_gu) * H + len(c_d) * I + len(c_dg) * H) + 2 * len(ch) * len(c_wg) * n_e
-    desc = (f"expert {g} ({n_e} rows): {k} token rows through gate/up ({len(c_gu)} cols), down ({len(c_d)} cols), "
-            f"dgrad ({len(c_dg)} cols); wgrad {len(ch)} x {len(c_wg)} over {n_e} rows; quantization of every "
-            f"operand row/column those need included")
+    k = host["x"].shape[0]
+    I = host["h"].shape[1]
+    flops = (2 * k * (len(sel["gu"]) * H + len(sel["d"]) * I + len(sel["dg"]) * H)
+             + 2 * len(sel["ch"]) * len(sel["wg"]) * n_e)
+    return secs, flops
+
+
+def oracle_sample(step, counts, rows_per_gemm, cols, rng_seed=0):
+    """Time the CPU oracle on one sample of the step, in this process (inputs are
+    on the host before the clock starts).  Returns (seconds, gemm_flops, description)."""
+    host, sel, desc = oracle_host_sample(step, counts, rows_per_gemm, cols, rng_seed)
+    secs, flops = oracle_run_sample((host, sel))
     return secs, flops, desc
+
+
+def oracle_quantize(task):
+    """One oracle quantizer over a block of rows (bf16 bits); returns seconds.
+    Column-wise blocks run along rows: a block of a multiple of 32 rows is
+    quantized exactly as those rows of the whole tensor."""
+    import numpy as np
+
+    import oracle
+
+    kind, x = task
+    orc = oracle.Oracle()
+    t0 = time.perf_counter()
+    if kind == "nvfp4":
+        orc.quant_nvfp4(x)
+    elif kind == "mxfp8_rows":
+        orc.quant_mxfp8_rows(x)
+    else:
+        orc.quant_mxfp8_cols(x, np.array([0, x.shape[0]]))
+    return time.perf_counter() - t0
+
+
+def _pool_ready(_):
+    import oracle
+
+    oracle.Oracle()
+    return os.getpid()
+
+
+def host_info():
+    """The host the CPU numbers were taken on: usable cores, CPU model, architecture."""
+    import platform
+
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for line in fh:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except AttributeError:
+        usable = os.cpu_count()
+    return {"nproc": usable, "cpu_count": os.cpu_count(), "cpu_model": model, "arch": platform.machine()}
+
+
+QUANT_KINDS = ("nvfp4", "mxfp8_rows", "mxfp8_cols")
+
+
+def quant_bytes(kind, rows, cols):
+    """Algorithmic bytes of one quantizer call: bf16 in, codes, scales (and the
+    per-token fp32 scale of NVFP4) out, as the GPU breakdown counts them."""
+    if kind == "nvfp4":
+        return rows * (2 * cols + cols // 2 + cols // 16 + 4)
+    return rows * (2 * cols + cols + cols // 32)
+
+
+def gpu_quantizer_batch(x_bits):
+    """The three quantizers on the GPU over the whole quantizer batch (bf16 bits,
+    uploaded once; larger than L2): GB/s by CUDA events, median of 5."""
+    import numpy as np
+    import torch
+
+    import fp8_moe_expert_gb300 as fme
+
+    rows, cols = x_bits.shape
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q4 = fme.quantize_nvfp4_pertoken(x, status=st)
+    q8r = fme.quantize_mxfp8(x, fme.ROWWISE, status=st)
+    q8c = fme.quantize_mxfp8(x, fme.COLWISE, status=st)
+    calls = {
+        "nvfp4": lambda: fme.quantize_nvfp4_pertoken(x, codes=q4[0], sf=q4[1], row_scale=q4[2], status=st),
+        "mxfp8_rows": lambda: fme.quantize_mxfp8(x, fme.ROWWISE, codes=q8r[0], sf=q8r[1], status=st),
+        "mxfp8_cols": lambda: fme.quantize_mxfp8(x, fme.COLWISE, codes=q8c[0], sf=q8c[1], padded_offsets=q8c[2],
+                                                 status=st),
+    }
+    out = {}
+    for kind, fn in calls.items():
+        fn()
+        ts = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        out[kind] = quant_bytes(kind, rows, cols) / (statistics.median(ts) * 1e-3) / 1e9
+    code, raw = fme.read_device_status(st)
+    if code != 0:
+        raise RuntimeError(f"device status {raw:#x} in the quantizer-batch timing")
+    return out
 
 
 def oracle_rows_sample(step):
@@ -743,10 +871,55 @@ def orc_bits(v):
 
 
 def cpu_baseline(step, counts):
-    secs, flops, desc = oracle_sample(step, counts, rows_per_gemm=16, cols=None)
-    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": desc, "seconds": round(secs, 3),
-            "next_rows_gbs": oracle_rows_sample(step)}
+    """The oracle, as it stands, on the host's cores: the step's GEMM sample on one
+    core and on every usable core (a spawned process pool, one sample per core),
+    and the three quantizers on the whole 16384 x 7168 quantizer batch (one core:
+    a 1024-row slice; every core: the whole tensor in row blocks), next to the
+    GPU's GB/s on the same tensor.  About 15-30 s of host time."""
+    import multiprocessing as mp
+
+    from fp8_moe_expert_gb300 import synth
+
+    info = host_info()
+    cores = max(1, int(info["nproc"] or 1))
+    s1, f1, desc = oracle_sample(step, counts, rows_per_gemm=16, cols=None)
+    tasks = []
+    for i in range(cores):
+        host, sel, _ = oracle_host_sample(step, counts, rows_per_gemm=16, cols=None, rng_seed=100 + i)
+        tasks.append((host, sel))
+    x_bits, _, _ = synth.quantizer_batch()
+    rows, cols = x_bits.shape
+    blk = (-(-rows // cores) + 31) // 32 * 32  # ceil(rows / cores), a multiple of 32
+    blocks = [x_bits[i:i + blk] for i in range(0, rows, blk)]
+    single, allcore = {}, {}
+    for kind in QUANT_KINDS:
+        part = x_bits[:1024]
+        single[kind] = quant_bytes(kind, part.shape[0], cols) / oracle_quantize((kind, part)) / 1e9
+    with mp.get_context("spawn").Pool(cores) as pool:
+        pool.map(_pool_ready, range(cores), chunksize=1)  # workers started and the oracle loaded
+        t0 = time.perf_counter()
+        res = pool.map(oracle_run_sample, tasks, chunksize=1)
+        wall = time.perf_counter() - t0
+        all_value = sum(f for _, f in res) / wall / 1e12
+        for kind in QUANT_KINDS:
+            t0 = time.perf_counter()
+            pool.map(oracle_quantize, [(kind, b) for b in blocks], chunksize=1)
+            allcore[kind] = quant_bytes(kind, rows, cols) / (time.perf_counter() - t0) / 1e9
+    gpu = gpu_quantizer_batch(x_bits)
+    return {
+        "value": all_value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        "sample": f"{cores} samples in parallel, one per core, each: {desc}",
+        "single_core": {"value": f1 / s1 / 1e12, "unit": "TFLOP/s", "cores": 1, "seconds": round(s1, 3),
+                        "sample": desc},
+        "all_core_seconds": round(wall, 3),
+        "host": info,
+        "quantizers_16384x7168_gbs": {
+            kind: {"oracle_1_core": round(single[kind], 4), f"oracle_{cores}_cores": round(allcore[kind], 4),
+                   "gpu": round(gpu[kind], 1)} for kind in QUANT_KINDS},
+        "quantizer_samples": "one core: rows 0-1023 of the batch; every core: the whole batch in blocks of "
+                             f"{blk} rows (wall clock, transfer to the workers included); GPU: the whole batch",
+        "next_rows_gbs": oracle_rows_sample(step),
+    }
 
 
 def run_reference(args, rank, world, local_rank):
@@ -775,7 +948,8 @@ def run_reference(args, rank, world, local_rank):
         "data": "synthetic (same seeded workload as the CUDA arm)",
         "config": {"workload": args.workload, "experts": step.E, "hidden": step.H, "intermediate": step.I,
                    "routed_rows": step.R},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc,
+                         "host": host_info()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -250,16 +250,17 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     fence_barrier_init();
   }
   __syncthreads();
-  // input row of output row r: r itself, or the gathered token (checked)
-  auto src_of = [&](int64_t r) -> int64_t {
-    if (gather == nullptr) return r;
-    const int64_t g = __ldg(gather + r) / gather_div;
+  // the gathered token of a gather entry (checked)
+  auto token_of = [&](int32_t entry) -> int64_t {
+    const int64_t g = entry / gather_div;
     if (g < 0 || g >= gather_limit) {
       report(status, kDevBadIndex);
       return 0;
     }
     return g;
   };
+  // input row of output row r: r itself, or the gathered token
+  auto src_of = [&](int64_t r) -> int64_t { return gather == nullptr ? r : token_of(__ldg(gather + r)); };
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       const int64_t r = row_at(s);
@@ -275,6 +276,11 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
   int i = 0, s = 0;
   uint32_t parity = 0;
   int g_cur = 0;  // thread 0: group of the current row (activations)
+  // thread 0, gathering: the gather entry of the next row to refill, loaded one
+  // row ahead so that its latency overlaps a row's work instead of delaying the
+  // refill's copy
+  int32_t next_entry = 0;
+  if (gather != nullptr && tid == 0 && row_at(stages) < rows) next_entry = __ldg(gather + row_at(stages));
   int64_t row = row_at(0);
   for (; row < rows; ++i, row += stride) {
     const bool ok = mbar_wait(&bars[s], parity, &abort_flag, status);
@@ -317,9 +323,11 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     if (tid == 0) {
       const int64_t next = row + stages * stride;
       if (next < rows) {
+        const int64_t src = gather == nullptr ? next : token_of(next_entry);
         fence_proxy_async_shared();
         mbar_arrive_expect_tx(&bars[s], row_bytes);
-        bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + src_of(next) * row_elems, row_bytes, &bars[s]);
+        bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + src * row_elems, row_bytes, &bars[s]);
+        if (gather != nullptr && next + stride < rows) next_entry = __ldg(gather + next + stride);
       }
     }
     if (++s == stages) {
