@@ -20,18 +20,25 @@
 // four warpgroups:
 //   warps 0-3   scale writers (both CTAs), warp w owning tensor-memory lane
 //               quarter w: per stage, read the stage's scale tiles from shared
-//               memory (where TMA put them), tcgen05.st them into the next free
-//               buffer of a tensor-memory ring in the layout the MMA reads, and
+//               memory (where TMA put them), tcgen05.st them into the stage's own
+//               tensor-memory scale buffer in the layout the MMA reads, and
 //               arrive on the leader's "scales full" barrier;
 //   warp 4      TMA producer (both CTAs): A, B and their scale tiles into a
 //               5-stage ring; A and B complete on the leader's "full" barrier
 //               (the leader's MMAs read both CTAs' tiles), the scale tiles on
 //               this CTA's own "scales landed" barrier;
 //   warp 5      allocates 512 tensor-memory columns in both CTAs together; in the
-//               leader, one thread issues the MMAs; commits free the stage and the
-//               scale buffer in both CTAs and, at the end of a tile, fill both
-//               CTAs' accumulators;
+//               leader, one thread issues the MMAs; one commit per two stages
+//               frees both stages (and their scale buffers) in both CTAs, and at
+//               the end of a tile a commit fills both CTAs' accumulators;
 //   warps 8-15  epilogue (both CTAs): see epilogue_warp.
+// Why one commit per two stages: in a microbenchmark of back-to-back MMAs (128
+// cycles per M = 256, N = 256, K = 64 MMA at 1.96 GHz), a wait on a commit issued
+// one four-MMA stage earlier cost the pipe 100-150 ns per stage, however deep the
+// ring, while one waited commit per eight MMAs cost nothing; without loads or
+// scales this ring then runs at the MMA rate (measured 263 ns per stage).  A
+// stage's tensor-memory scale buffer is free when the producer may refill the
+// stage, so the writers wait only for the scale tiles to land.
 // Registers: launched at 128 per thread; the writers and the producer/MMA
 // warpgroup give some back (setmaxnreg) so that the epilogue holds its whole
 // accumulator share (128 values per thread).
@@ -46,7 +53,7 @@ constexpr int kThreads = 512;  // 4 scale writers, producer, MMA, 2 idle, 8 epil
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kEpilogueWarp = 8;  // first of 8
-constexpr int kSfBufs = 4;        // tensor-memory scale buffers between the writers and the MMA issuer
+constexpr int kGroupBars = 4;     // ring of "group done" barriers (one commit per two fills)
 // Register budgets per thread (launch: 65536 / 512 = 128): writers, producer/MMA
 // warpgroup, the two epilogue warpgroups; 128 * (96 + 64 + 2 * 176) = 65536.
 constexpr uint32_t kRegsWriter = 96;
@@ -59,6 +66,7 @@ constexpr int kAtoms = 4;                   // 512-byte scale tiles per 128 rows
 constexpr int kSfaBytes = 512 * kAtoms;     // this CTA's 128 A rows
 constexpr int kSfbBytes = 2 * 512 * kAtoms;  // the tile's 256 B rows: [rows 0-127][rows 128-255]
 constexpr int kStages = 5;                  // ring depth when the shared memory allows
+constexpr int kSfBufs = kStages;            // one tensor-memory scale buffer per stage
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 // Tensor-memory scale ring after the 256 accumulator columns: all buffers' B
 // columns (4 steps x 8), then all buffers' A columns (4 steps x 4), so that every
@@ -76,9 +84,8 @@ static_assert(kSfaBase + kSfBufs * kSfaCols <= kTmemCols, "tensor memory budget"
 struct SharedState {
   uint64_t full[kMaxStages];       // the stage's A and B tiles (both CTAs) have landed (leader)
   uint64_t sf_landed[kMaxStages];  // this CTA's scale tiles of the stage have landed
-  uint64_t empty[kMaxStages];      // the stage's MMAs are done (both CTAs, by commit)
-  uint64_t sf_full[kSfBufs];       // every writer of the pair has stored buffer b (leader)
-  uint64_t sf_empty[kSfBufs];      // the MMAs reading buffer b are done (both CTAs, by commit)
+  uint64_t sf_full[kMaxStages];    // every writer of the pair has stored the stage's scales (leader)
+  uint64_t grp_done[kGroupBars];   // the MMAs of fills 2c and 2c + 1 are done (both CTAs, by commit c)
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -149,12 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
     for (int i = 0; i < S; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.sf_landed[i], 1);
-      mbar_init(&s.empty[i], 1);
-    }
-    for (int i = 0; i < kSfBufs; ++i) {
       mbar_init(&s.sf_full[i], kSfFullArrivals);
-      mbar_init(&s.sf_empty[i], 1);
     }
+    for (int i = 0; i < kGroupBars; ++i) mbar_init(&s.grp_done[i], 1);
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
@@ -185,18 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
     regs_dec<kRegsWriter>();
     const int q = warp;
     const uint32_t leader_sf_full = pair::map_to_rank(&s.sf_full[0], 0);
-    uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
+    uint32_t stage = 0, phase = 0;
     bool stop = false;
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
       const Tile tl = tile_at<kKind>(p, grp, t, rank);
       for (int ks = 0; ks < tl.num_k; ++ks) {
-        if (!mbar_wait(&s.sf_landed[stage], phase, abort_flag, p.status) ||
-            !mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status)) {
+        // The stage's scale tiles have landed, so the producer has seen the MMAs
+        // of the stage's previous fill (the last readers of its tensor-memory
+        // scale buffer) finish.
+        if (!mbar_wait<true>(&s.sf_landed[stage], phase, abort_flag, p.status)) {
           stop = true;
           break;
         }
         tc_fence_after();
-        write_scales(tmem, q, lane, buf, smem_sfa + stage * kSfaBytes, smem_sfb + stage * kSfbBytes);
+        write_scales(tmem, q, lane, stage, smem_sfa + stage * kSfaBytes, smem_sfb + stage * kSfbBytes);
         // The stores are complete in tensor memory once tcgen05.wait::st returns, and
         // the leader reads this buffer only after the barrier phase completes, so the
         // peer's arrive needs no memory ordering of its own: a cluster-scope release
@@ -207,17 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
         __syncwarp();
         if (lane == 0) {
           if (rank == 0)
-            mbar_arrive(&s.sf_full[buf]);
+            mbar_arrive(&s.sf_full[stage]);
           else
-            pair::arrive_remote_relaxed(leader_sf_full + buf * 8);
+            pair::arrive_remote_relaxed(leader_sf_full + stage * 8);
         }
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
-        }
-        if (++buf == kSfBufs) {
-          buf = 0;
-          buf_phase ^= 1;
         }
       }
     }
@@ -225,15 +227,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
     regs_dec<kRegsControl>();
     if (warp == kProducerWarp && lane == 0) {
       // -------------------------------------------------------------- producer
-      uint32_t stage = 0, phase = 0;
+      uint32_t stage = 0;
       uint32_t filled = 0;  // stages filled so far (for the drain below)
       for (int64_t t = pair_id; t < total; t += pairs) {
         const Tile tl = tile_at<kKind>(p, grp, t, rank);
         bool stop = false;
         for (int ks = 0; ks < tl.num_k; ++ks) {
-          if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.status)) {
-            stop = true;
-            break;
+          // Fill f reuses the stage of fill f - S, whose MMAs commit (f - S) / 2 covers.
+          if (filled >= static_cast<uint32_t>(S)) {
+            const uint32_t c = (filled - S) >> 1;
+            if (!mbar_wait<true>(&s.grp_done[c % kGroupBars], (c / kGroupBars) & 1, abort_flag, p.status)) {
+              stop = true;
+              break;
+            }
           }
           // scale tiles first, on this CTA's own barrier: the writers start on them
           // while the operands are still arriving
@@ -248,10 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
           pair::tma_load_2d(smem_a + stage * kABytes, &p.map_a, bar, tl.a_x0 + ks * kStageKBytes, tl.a_y);
           pair::tma_load_2d(smem_b + stage * kBBytes, &p.map_b, bar, tl.b_x0 + ks * kStageKBytes, tl.b_y);
           ++filled;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (++stage == S) stage = 0;
         }
         if (stop) break;
       }
@@ -267,21 +270,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
       if (rank == 0) drain_pair_ring(s.full, S, filled, peer, kABytes + kBBytes);
     } else if (warp == kMmaWarp && lane == 0 && rank == 0) {
       // ------------------------------------------------ MMA issuer (leader)
-      uint32_t stage = 0, phase = 0, acc_phase = 0, buf = 0, buf_phase = 0;
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      uint32_t fill = 0;  // fills consumed so far
       bool stop = false;
       for (int64_t t = pair_id; t < total && !stop; t += pairs) {
         const Tile tl = tile_at<kKind>(p, grp, t, 0);
-        if (!mbar_wait(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
+        if (!mbar_wait<true>(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         for (int ks = 0; ks < tl.num_k; ++ks) {
-          if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
-              !mbar_wait(&s.sf_full[buf], buf_phase, abort_flag, p.status)) {
+          if (!mbar_wait<true>(&s.full[stage], phase, abort_flag, p.status) ||
+              !mbar_wait<true>(&s.sf_full[stage], phase, abort_flag, p.status)) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_t = tmem + kSfaBase + buf * kSfaCols;
-          const uint32_t sfb_t = tmem + kSfbBase + buf * kSfbCols;
+          const uint32_t sfa_t = tmem + kSfaBase + stage * kSfaCols;
+          const uint32_t sfb_t = tmem + kSfbBase + stage * kSfbCols;
           const uint32_t a_s = smem_u32(smem_a + stage * kABytes);
           const uint32_t b_s = smem_u32(smem_b + stage * kBBytes);
 #pragma unroll
@@ -291,15 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
             const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
             pair::mma_nvf4(tmem, ad, bd, pair::idesc_nvf4(kBN), sfa_t + 4 * kk, sfb_t + 8 * kk, acc);
           }
-          pair::commit_both(&s.empty[stage]);
-          pair::commit_both(&s.sf_empty[buf]);
+          // One commit per two fills: waiting on a commit costs the tensor pipe time
+          // unless the MMAs of about two stages separate it from the wait.
+          if (fill & 1) pair::commit_both(&s.grp_done[(fill >> 1) % kGroupBars]);
+          ++fill;
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
-          }
-          if (++buf == kSfBufs) {
-            buf = 0;
-            buf_phase ^= 1;
           }
         }
         if (stop) break;
