@@ -140,8 +140,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     uint32_t filled = 0;  // stages filled so far (for the drain below)
     for (int64_t t = pair_id; t < total; t += pairs) {
       const Tile tl = tile_at<K>(p, grp, t, rank);
+      // wgrad: the pairs' i-th tiles (a "wave") stream K forward for even i and
+      // backward for odd i, so that a wave starts on the B panels' K range the
+      // previous wave read last, which is still in L2 (a wave reads every B panel
+      // of a large expert again).
+      const bool reverse = K == GemmKind::kWgradMxfp8 && ((t / pairs) & 1);
       bool stop = false;
-      for (int ks = 0; ks < tl.num_k; ++ks) {
+      for (int ks_ = 0; ks_ < tl.num_k; ++ks_) {
+        const int ks = reverse ? tl.num_k - 1 - ks_ : ks_;
         if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.status)) {
           stop = true;
           break;
