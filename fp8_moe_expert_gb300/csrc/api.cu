@@ -103,6 +103,28 @@ fme_status encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint
   return FME_OK;
 }
 
+// bf16 matrix [rows x cols] (row stride cols * 2 bytes) for bulk tensor stores of
+// 32 x 32 boxes with the 64-byte swizzle.
+fme_status encode_bf16_out(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn;
+  fme_status st = get_encoder(&fn);
+  if (st != FME_OK) return st;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (output) failed (CUresult %d)", static_cast<int>(r));
+    g_last_cuda_error = buf;
+    return FME_ERR_CUDA;
+  }
+  return FME_OK;
+}
+
 // Tiled scales of a tensor as a 2-D map of 8-byte words: one row per 128-row
 // block (`row_bytes` bytes each), boxes of `box_tiles` 512-byte tiles x `box_rows`
 // blocks, no swizzle, zero fill out of bounds.
@@ -465,6 +487,7 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * n / 128, (k / 64) * 512, 4,
                              2)) != FME_OK)
     return st;
+  if ((st = encode_bf16_out(&a.map_y, y, n, m)) != FME_OK) return st;
   a.a_scale = a_scale;
   a.b_scale = b_scale;
   a.offsets = offsets;
