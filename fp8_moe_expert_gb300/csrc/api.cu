@@ -531,6 +531,7 @@ fme_status grouped_gemm_fwd_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, c
   if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * n / 128, (k / 128) * 512, 1,
                              2)) != FME_OK)
     return st;
+  if ((st = encode_bf16_out(&a.map_y, y, n, m)) != FME_OK) return st;
   a.offsets = offsets;
   a.num_experts = num_experts;
   a.m = m;
@@ -568,6 +569,7 @@ fme_status grouped_gemm_dgrad_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf,
       FME_OK)
     return st;
   if ((st = encode_scales_2d(&a.map_sfb, b_sf, n / 128, (ldb / 128) * 512, 1, 2)) != FME_OK) return st;
+  if ((st = encode_bf16_out(&a.map_y, y, n, m)) != FME_OK) return st;
   a.offsets = offsets;
   a.num_experts = num_experts;
   a.m = m;
@@ -616,6 +618,9 @@ static fme_status wgrad_call(const uint8_t *a_codes, const uint8_t *a_sf, int64_
   if ((st = encode_scales_2d(&a.map_sfa, sabase, has_positions ? m / 128 : 1, (lda_e / 128) * 512, 1, 1)) != FME_OK)
     return st;
   if ((st = encode_scales_2d(&a.map_sfb, sbbase, has_positions ? n / 128 : 2, (ldb_e / 128) * 512, 1, 2)) != FME_OK)
+    return st;
+  // dW [num_experts * m x n] bf16 for bulk stores (the fp32 accumulate writes with plain stores)
+  if (!accumulate && (st = encode_bf16_out(&a.map_y, y, n, static_cast<uint64_t>(num_experts) * m)) != FME_OK)
     return st;
   a.offsets = padded_offsets;
   a.num_experts = num_experts;

@@ -78,7 +78,7 @@ struct LaunchGemm {
   GemmKind kind;
   CUtensorMap map_a, map_b;      // operand codes, uint8, 128-byte swizzle
   CUtensorMap map_sfa, map_sfb;  // tiled scales viewed as [128-row blocks x 8-byte words]
-  CUtensorMap map_y;             // NVFP4 forward: the bf16 output, 32 x 32 boxes, 64-byte swizzle
+  CUtensorMap map_y;             // the bf16 output [rows x n], 32 x 32 boxes, 64-byte swizzle (not the fp32 accumulate)
   const float *a_scale, *b_scale;  // forward only
   const int32_t *offsets;          // row offsets (fwd, dgrad) or padded offsets (wgrad)
   int32_t num_experts;

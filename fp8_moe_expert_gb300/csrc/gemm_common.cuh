@@ -283,8 +283,8 @@ __device__ __forceinline__ void store_block(__nv_bfloat16 *dst, int64_t ld, int 
   __syncwarp();
 }
 
-// The same 32 x 32 block written by one bulk tensor store (the NVFP4 forward,
-// every row of the block in the expert): the staging layout above is the 64-byte
+// The same 32 x 32 block written by one bulk tensor store (every bf16 output; all
+// rows of the block in the expert): the staging layout above is the 64-byte
 // swizzle of the output map's 32 x 32 box (16-byte chunk j of row r at chunk
 // j ^ ((r >> 1) & 3)).  Lane 0 issues the store; the block is rewritten only after
 // the previous store has read it.  Measured against store_block: the MMA stages of
@@ -407,18 +407,18 @@ __device__ __forceinline__ void epilogue_warp(const LaunchGemm &p, const Groups 
       continue;
     }
     const int warp_rows = tl.rows_valid - 32 * q;  // rows of this warp's 32 that are the expert's
+    // this CTA's first output row in map_y (wgrad: expert e's dW rows start at e * m)
+    const int32_t out_row = K == GemmKind::kWgradMxfp8 ? static_cast<int32_t>(tl.e * p.m) + tl.a_y : tl.a_y;
     if (warp_rows > 0) {
       __nv_bfloat16 *ywarp = y + tl.y_off + static_cast<int64_t>(32 * q) * p.n + c0;
       auto emit = [&](const uint32_t(&v)[32], int c) {
         uint32_t packed[16];
         convert_chunk<K>(packed, v, sa, sw + 32 * c);
-        if (K == GemmKind::kFwdNvfp4 && warp_rows >= 32) {
-          store_block_tma(&p.map_y, tl.n0 + c0 + 32 * c, tl.a_y + 32 * q, stage_blk, lane, packed);
+        if (warp_rows >= 32) {
+          store_block_tma(&p.map_y, tl.n0 + c0 + 32 * c, out_row + 32 * q, stage_blk, lane, packed);
         } else {
-          if (K == GemmKind::kFwdNvfp4) {  // a bulk store may still be reading the block
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-          }
+          if (lane == 0) bulk_wait_read_all();  // a bulk store may still be reading the block
+          __syncwarp();
           store_block(ywarp + 32 * c, p.n, warp_rows, stage_blk, lane, packed);
         }
       };
@@ -428,7 +428,7 @@ __device__ __forceinline__ void epilogue_warp(const LaunchGemm &p, const Groups 
       emit(v3, 3);
     }
   }
-  if (K == GemmKind::kFwdNvfp4 && lane == 0) bulk_wait_all();  // the bulk stores are done before the CTA exits
+  if (lane == 0) bulk_wait_all();  // the bulk stores are done before the CTA exits
 }
 
 // A pair-cluster launch of `kernel` on as many pairs as the work and the SMs allow.
