@@ -22,13 +22,17 @@
 //   warp 1      allocates 512 tensor-memory columns in both CTAs together; in the
 //               leader, one thread issues the block-scaled MMAs
 //               (kind::mxf8f6f4.block_scale.scale_vec::1X, M = 256, N = 256, the
-//               scale id selecting the byte); commits free the stage in both CTAs
-//               and, at the end of a tile, fill both CTAs' accumulators;
+//               scale id selecting the byte); one commit per two stages frees both
+//               stages (and their scale buffers) in both CTAs, and at the end of a
+//               tile a commit fills both CTAs' accumulators;
 //   warps 10-11 in the leader, one thread of each copies its share of the
-//               stage's three scale tiles into a ring of 4 tensor-memory buffers
-//               (tcgen05.cp.cta_group::2.32x128b.warpx4: the copy replicates a
-//               tile's 32 rows into all four lane quarters, which B needs) ahead
-//               of the MMAs;
+//               stage's three scale tiles into the stage's own tensor-memory
+//               buffer (tcgen05.cp.cta_group::2.32x128b.warpx4: the copy
+//               replicates a tile's 32 rows into all four lane quarters, which B
+//               needs) ahead of the MMAs; a stage's tiles land only after both
+//               producers saw the buffer's previous readers finish.
+// Against a commit per stage and a separate scale-buffer ring: dgrad 2.40 ->
+// 2.34 ms, wgrad 2.45 -> 2.38 ms on the 262144-row step.
 //   warps 2-9   epilogue (both CTAs): see epilogue_warp.
 #include "gemm_common.cuh"
 
@@ -37,7 +41,7 @@ namespace fme {
 constexpr int kThreads = 384;    // producer, MMA, 8 epilogue warps, 2 scale copiers
 constexpr int kCopierWarp = 10;  // and 11
 constexpr int kCopiers = 2;
-constexpr int kSfBuffers = 4;  // tensor-memory scale buffers between the copiers and the MMA issuer
+constexpr int kGroupBars = 4;   // ring of "group done" barriers (one commit per two stages)
 
 struct CfgMx {
   static constexpr int kSfaBytes = 512;      // this CTA's 128 rows: one tile per 128-K stage
@@ -52,15 +56,14 @@ struct CfgMx {
   static constexpr int kOperandTx = 2 * (kABytes + kBBytes);
   static constexpr int kScaleTx = 2 * (kSfaBytes + kSfbBytes);
   static_assert(kStages <= kMaxStages, "stage count");
-  static_assert(kBN + kSfBuffers * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
+  static_assert(kBN + kStages * kSfCols <= static_cast<int>(kTmemCols), "tensor memory budget");
 };
 
 struct SharedStateMx {
   uint64_t full[kMaxStages];       // the stage's A and B tiles have landed
   uint64_t sf_landed[kMaxStages];  // the stage's scale tiles have landed
-  uint64_t empty[kMaxStages];
-  uint64_t sf_full[kSfBuffers];   // scales of a stage are in tensor-memory buffer b (one arrival per copier)
-  uint64_t sf_empty[kSfBuffers];  // the MMAs reading buffer b are done
+  uint64_t sf_full[kMaxStages];   // the stage's scales are in its tensor-memory buffer (one arrival per copier)
+  uint64_t grp_done[kGroupBars];  // the MMAs of fills 2c and 2c + 1 are done (both CTAs, by commit c)
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -102,12 +105,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     for (int i = 0; i < S; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.sf_landed[i], 1);
-      mbar_init(&s.empty[i], 1);
-    }
-    for (int i = 0; i < kSfBuffers; ++i) {
       mbar_init(&s.sf_full[i], kCopiers);
-      mbar_init(&s.sf_empty[i], 1);
     }
+    for (int i = 0; i < kGroupBars; ++i) mbar_init(&s.grp_done[i], 1);
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, kAccEmptyArrivals);
     mbar_init(&s.drain, 1);
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0;
     uint32_t filled = 0;  // stages filled so far (for the drain below)
     for (int64_t t = pair_id; t < total; t += pairs) {
       const Tile tl = tile_at<K>(p, grp, t, rank);
@@ -148,9 +148,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       bool stop = false;
       for (int ks_ = 0; ks_ < tl.num_k; ++ks_) {
         const int ks = reverse ? tl.num_k - 1 - ks_ : ks_;
-        if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.status)) {
-          stop = true;
-          break;
+        // Fill f reuses the stage (and its tensor-memory scale buffer) of fill
+        // f - S, whose MMAs commit (f - S) / 2 covers.
+        if (filled >= static_cast<uint32_t>(S)) {
+          const uint32_t c = (filled - S) >> 1;
+          if (!mbar_wait<true>(&s.grp_done[c % kGroupBars], (c / kGroupBars) & 1, abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
         }
         // Scales first, on their own barrier: the copiers start on them while the
         // operands are still arriving, so the tensor-memory copies are done by the
@@ -164,10 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         pair::tma_load_2d(smem_a + stage * kABytes, &p.map_a, bar, tl.a_x0 + ks * kStageKBytes, tl.a_y);
         pair::tma_load_2d(smem_b + stage * kBBytes, &p.map_b, bar, tl.b_x0 + ks * kStageKBytes, tl.b_y);
         ++filled;
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1;
-        }
+        if (++stage == S) stage = 0;
       }
       if (stop) break;
     }
@@ -182,22 +184,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------ MMA issuer (leader)
-    uint32_t stage = 0, phase = 0, acc_phase = 0, buf = 0, buf_phase = 0;
+    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    uint32_t fill = 0;  // fills consumed so far
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
       const Tile tl = tile_at<K>(p, grp, t, 0);
       if (tl.num_k == 0) continue;
-      if (!mbar_wait(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
+      if (!mbar_wait<true>(&s.acc_empty, acc_phase ^ 1, abort_flag, p.status)) break;
       tc_fence_after();
       for (int ks = 0; ks < tl.num_k; ++ks) {
-        if (!mbar_wait(&s.full[stage], phase, abort_flag, p.status) ||
-            !mbar_wait(&s.sf_full[buf], buf_phase, abort_flag, p.status)) {
+        if (!mbar_wait<true>(&s.full[stage], phase, abort_flag, p.status) ||
+            !mbar_wait<true>(&s.sf_full[stage], phase, abort_flag, p.status)) {
           stop = true;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa_t = sf_base + buf * C::kSfCols;
+        const uint32_t sfa_t = sf_base + stage * C::kSfCols;
         const uint32_t sfb_t = sfa_t + C::kSfaCols;
         const uint32_t a_s = smem_u32(smem_a + stage * kABytes);
         const uint32_t b_s = smem_u32(smem_b + stage * kBBytes);
@@ -208,15 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
           pair::mma_mxf8(tmem, ad, bd, pair::idesc_mxf8(kBN, kk), sfa_t, sfb_t, acc);
         }
-        pair::commit_both(&s.empty[stage]);
-        pair::commit_local(&s.sf_empty[buf]);
+        // one commit per two fills (see gemm_nvfp4.cu: a waited commit per four
+        // MMAs costs the tensor pipe time)
+        if (fill & 1) pair::commit_both(&s.grp_done[(fill >> 1) % kGroupBars]);
+        ++fill;
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
-        }
-        if (++buf == kSfBuffers) {
-          buf = 0;
-          buf_phase ^= 1;
         }
       }
       if (stop) break;
@@ -233,19 +234,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     // earlier stages, then arrive on the buffer's "full" barrier.  Copier 0
     // takes A and B's rows 128-255, copier 1 B's rows 0-127.
     const int who = warp - kCopierWarp;
-    uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
+    uint32_t stage = 0, phase = 0;
     bool stop = false;
     const uint32_t sf_base = tmem + kBN;
     for (int64_t t = pair_id; t < total && !stop; t += pairs) {
       const Tile tl = tile_at<K>(p, grp, t, 0);
       for (int ks = 0; ks < tl.num_k; ++ks) {
-        if (!mbar_wait(&s.sf_landed[stage], phase, abort_flag, p.status) ||
-            !mbar_wait(&s.sf_empty[buf], buf_phase ^ 1, abort_flag, p.status)) {
+        // The stage's scale tiles have landed, so both producers have seen the
+        // MMAs of the stage's previous fill (the last readers of its buffer) finish.
+        if (!mbar_wait<true>(&s.sf_landed[stage], phase, abort_flag, p.status)) {
           stop = true;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa_t = sf_base + buf * C::kSfCols;
+        const uint32_t sfa_t = sf_base + stage * C::kSfCols;
         const uint32_t sfb_t = sfa_t + C::kSfaCols;
         const uint32_t sfa_s = smem_u32(smem_sfa + stage * C::kSfaBytes);
         const uint32_t sfb_s = smem_u32(smem_sfb + stage * C::kSfbBytes);
@@ -255,14 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         } else {
           pair::copy_scales(sfb_t, desc_scale_tile(sfb_s));
         }
-        pair::commit_local(&s.sf_full[buf]);
+        pair::commit_local(&s.sf_full[stage]);
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
-        }
-        if (++buf == kSfBuffers) {
-          buf = 0;
-          buf_phase ^= 1;
         }
       }
     }
