@@ -211,7 +211,7 @@ __device__ __forceinline__ uint4 swiglu_uint4(const uint4 &g, const uint4 &u) {
 // kSwiGLU: the row is produced from a gate/up row [g (k values) | u (k values)]
 // staged whole in shared memory: h = silu(g) * u rounded to bf16, optionally
 // written to h_out, then quantized exactly as a bf16 input row would be.
-template <int R, bool kSwiGLU>
+template <int R, bool kSwiGLU, bool kGather>
 __global__ void __launch_bounds__(kNvMaxThreads, 4)
     nvfp4_pertoken_kernel(const uint16_t *__restrict__ x, int64_t rows, int k, const int32_t *__restrict__ offsets,
                           int num_groups, uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     return g;
   };
   // input row of output row r: r itself, or the gathered token
-  auto src_of = [&](int64_t r) -> int64_t { return gather == nullptr ? r : token_of(__ldg(gather + r)); };
+  auto src_of = [&](int64_t r) -> int64_t { return kGather ? token_of(__ldg(gather + r)) : r; };
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       const int64_t r = row_at(s);
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
   // row ahead so that its latency overlaps a row's work instead of delaying the
   // refill's copy
   int32_t next_entry = 0;
-  if (gather != nullptr && tid == 0 && row_at(stages) < rows) next_entry = __ldg(gather + row_at(stages));
+  if (kGather && tid == 0 && row_at(stages) < rows) next_entry = __ldg(gather + row_at(stages));
   int64_t row = row_at(0);
   for (; row < rows; ++i, row += stride) {
     const bool ok = mbar_wait(&bars[s], parity, &abort_flag, status);
@@ -323,11 +323,11 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
     if (tid == 0) {
       const int64_t next = row + stages * stride;
       if (next < rows) {
-        const int64_t src = gather == nullptr ? next : token_of(next_entry);
+        const int64_t src = kGather ? token_of(next_entry) : next;
         fence_proxy_async_shared();
         mbar_arrive_expect_tx(&bars[s], row_bytes);
         bulk_load(nv_smem + static_cast<size_t>(s) * row_bytes, x + src * row_elems, row_bytes, &bars[s]);
-        if (gather != nullptr && next + stride < rows) next_entry = __ldg(gather + next + stride);
+        if (kGather && next + stride < rows) next_entry = __ldg(gather + next + stride);
       }
     }
     if (++s == stages) {
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kNvMaxThreads, 4)
 // / R rounded up to warps.  CTAs per SM: as many as 1024 threads and the
 // shared-memory budget allow with at least 3 stages each; stages: the rest of
 // the budget, 3 to 16 rows.
-template <int R, bool kSwiGLU>
+template <int R, bool kSwiGLU, bool kGather>
 static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   const int64_t nblk = a.k / 16;
   const int64_t row_bytes = a.k * (kSwiGLU ? 4 : 2);
@@ -423,7 +423,7 @@ static cudaError_t launch_nvfp4(const LaunchNvfp4 &a) {
   int64_t stages = (kNvSmemBudget / per_sm - fixed) / (row_bytes + 8);
   stages = stages < 3 ? 3 : (stages > 16 ? 16 : stages);
   const size_t smem = nv_smem_bytes(static_cast<int>(stages), row_bytes, a.num_groups);
-  auto kernel = nvfp4_pertoken_kernel<R, kSwiGLU>;
+  auto kernel = nvfp4_pertoken_kernel<R, kSwiGLU, kGather>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int64_t cap = static_cast<int64_t>(a.num_sms) * per_sm;
@@ -477,8 +477,9 @@ cudaError_t launch_quantize_nvfp4_pertensor(const LaunchNvfp4 &a, float *tensor_
 // thread are slower).  The SwiGLU rows (twice the bytes per block) keep one block
 // per thread up to 256 blocks, measured 4% faster there.
 cudaError_t launch_quantize_nvfp4(const LaunchNvfp4 &a) {
-  if (a.swiglu) return a.k / 16 > kNvMaxThreads ? launch_nvfp4<2, true>(a) : launch_nvfp4<1, true>(a);
-  return launch_nvfp4<2, false>(a);
+  // the gathered variant is a kernel of its own, so the plain rows carry no gather code
+  if (a.swiglu) return a.k / 16 > kNvMaxThreads ? launch_nvfp4<2, true, false>(a) : launch_nvfp4<1, true, false>(a);
+  return a.gather != nullptr ? launch_nvfp4<2, false, true>(a) : launch_nvfp4<2, false, false>(a);
 }
 
 }  // namespace fme
