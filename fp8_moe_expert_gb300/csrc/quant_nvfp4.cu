@@ -125,8 +125,15 @@ __device__ __forceinline__ uint2 e2m1_step_codes(const uint32_t (&w)[8], float e
   for (int i = 0; i < 8; ++i) {
     const float2 x = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
     const float2 n = __fmul2_rn(x, nr2);
+#ifdef FME_TEST_APPROX_DIVIDE
+    // Test build only (tests/test_gpu_division_control.py): the approximate
+    // quotient x * rcp.approx(e) of a fast divide, without the correction step.
+    const float2 q = n;
+    (void)e2;
+#else
     const float2 rho = __ffma2_rn(n, e2, x);
     const float2 q = __ffma2_rn(rho, nr2, n);
+#endif
     t[2 * i] = q.x;
     t[2 * i + 1] = q.y;
   }
