@@ -367,7 +367,11 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     if not args.no_extras:
-        line["extras"] = run_extras(step, args, bf16_burst)
+        # the extras follow the step back to back; their clocks are recorded apart,
+        # since the instruction-bound ones follow the SM clock where copies do not
+        with ClockSampler(local_rank) as extras_clocks:
+            line["extras"] = run_extras(step, args, bf16_burst)
+        line["extras_clocks"] = extras_clocks.summary()
     if not args.no_e2e:
         line["e2e"] = run_e2e(step, calls, args, world)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
