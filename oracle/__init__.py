@@ -87,12 +87,13 @@ def _declare(lib):
     lib.fme_orc_dequant_mxfp8.argtypes = [P, P, I64, I64, P]
     lib.fme_orc_gemm_abt.argtypes = [P, P, I64, I64, I64, P]
     lib.fme_orc_swiglu.argtypes = [P, I64, I64, P]
+    lib.fme_orc_swiglu_f64.argtypes = [P, I64, I64, P]
     lib.fme_orc_route.argtypes = [P, I64, I32, P, P, P]
     lib.fme_orc_swiglu_bwd.argtypes = [P, P, I64, I64, P]
     lib.fme_orc_combine.argtypes = [P, P, P, I64, I32, I64, P]
     for name in ("fme_orc_e2m1_encode_array", "fme_orc_e4m3_encode_array", "fme_orc_quant_nvfp4",
                  "fme_orc_dequant_nvfp4", "fme_orc_quant_mxfp8_rows", "fme_orc_quant_mxfp8_cols",
-                 "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt", "fme_orc_swiglu", "fme_orc_route", "fme_orc_swiglu_bwd",
+                 "fme_orc_dequant_mxfp8", "fme_orc_gemm_abt", "fme_orc_swiglu", "fme_orc_swiglu_f64", "fme_orc_route", "fme_orc_swiglu_bwd",
                  "fme_orc_quant_nvfp4_pertensor", "fme_orc_quant_mxfp8_rows_ceil", "fme_orc_quant_mxfp8_cols_ceil",
                  "fme_orc_combine"):
         getattr(lib, name).restype = None
@@ -227,6 +228,15 @@ class Oracle:
         inter = two_inter // 2
         h = np.empty((rows, inter), np.float64)
         self.lib.fme_orc_swiglu(_p(y), rows, inter, _p(h))
+        return h
+
+    def swiglu_f64(self, y_gu) -> np.ndarray:
+        """h = silu(g) * u in fp64 for fp64 rows [g | u] (e.g. the fp64 gate/up GEMM)."""
+        y = np.ascontiguousarray(y_gu, np.float64)
+        rows, two_inter = y.shape
+        inter = two_inter // 2
+        h = np.empty((rows, inter), np.float64)
+        self.lib.fme_orc_swiglu_f64(_p(y), rows, inter, _p(h))
         return h
 
     def swiglu_bwd(self, y_gu_bits, dh_bits) -> np.ndarray:

@@ -448,6 +448,20 @@ void fme_orc_swiglu(const uint16_t *y_gu, int64_t rows, int64_t inter, double *h
     }
 }
 
+/* The same activation on fp64 rows [g | u] (the gate/up GEMM's exact outputs,
+ * not rounded to bf16): h [rows x inter] = silu(g) * u in fp64. */
+void fme_orc_swiglu_f64(const double *y_gu, int64_t rows, int64_t inter, double *h) {
+    for (int64_t t = 0; t < rows; ++t) {
+        const double *row = y_gu + t * 2 * inter;
+        for (int64_t j = 0; j < inter; ++j) {
+            const double g = row[j];
+            const double u = row[inter + j];
+            const double silu = g / (1.0 + exp(-g));
+            h[t * inter + j] = silu * u;
+        }
+    }
+}
+
 /* d(gate/up) [rows x 2 inter] of h = silu(g) * u for the upstream gradient dh
  * [rows x inter] (bf16), in fp64: with s = 1 / (1 + e^-g) (the logistic function),
  * dh/dg = dh * u * (s + g * s * (1 - s)) and dh/du = dh * g * s; row t of the

@@ -426,6 +426,26 @@ def check_swiglu_vs_scipy(orc):
     assert np.allclose(h, want, rtol=4e-16, atol=1e-300)
 
 
+def check_swiglu_f64(orc):
+    """The fp64-input activation: equal to the bf16-input one on bf16 values (same
+    definition, other entry); against scipy's logistic function on fp64 values with
+    full mantissas; h(g, u) - h(-g, u) = g u on those values too; gate and up read
+    from the right halves (a swapped pair changes h, since silu is not odd)."""
+    from scipy.special import expit
+
+    rng = np.random.default_rng(23)
+    g = synth.bf16_float(synth.bf16_bits(rng.standard_normal((6, 64)) * 4.0))
+    u = synth.bf16_float(synth.bf16_bits(rng.standard_normal((6, 64))))
+    rows = np.concatenate([g, u], axis=1).astype(np.float64)
+    assert np.array_equal(orc.swiglu_f64(rows), orc.swiglu(_swiglu_rows(g, u)))
+    gf = rng.standard_normal((5, 48)) * 6.0
+    uf = rng.standard_normal((5, 48))
+    h = orc.swiglu_f64(np.concatenate([gf, uf], axis=1))
+    assert np.allclose(h, gf * expit(gf) * uf, rtol=4e-16, atol=1e-300)
+    hn = orc.swiglu_f64(np.concatenate([-gf, uf], axis=1))
+    assert np.allclose(h - hn, gf * uf, rtol=1e-13, atol=1e-300)
+
+
 def check_mxfp8_ceil_scale_brute_force(orc):
     """Round-up scale rule on every positive finite bf16 amax (one 32-block per
     value, the amax in the block's first element): the code is the smallest c

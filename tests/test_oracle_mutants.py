@@ -49,6 +49,10 @@ MUTANTS = {
     "swiglu_gate_up_halves_swapped": ("const double g = (double)bf16_value(row[j]);\n            const double u = (double)bf16_value(row[inter + j]);",
                                       "const double u = (double)bf16_value(row[j]);\n            const double g = (double)bf16_value(row[inter + j]);"),
     "swiglu_drops_up": ("h[t * inter + j] = g / (1.0 + exp(-g)) * u;", "h[t * inter + j] = g / (1.0 + exp(-g));"),
+    "swiglu_f64_sigmoid_of_minus_g": ("const double silu = g / (1.0 + exp(-g));",
+                                      "const double silu = g / (1.0 + exp(g));"),
+    "swiglu_f64_halves_swapped": ("            const double g = row[j];\n            const double u = row[inter + j];",
+                                  "            const double u = row[j];\n            const double g = row[inter + j];"),
     "mx_ceil_ignores_exact_powers": ("const int up = (m == 0.5) ? e2 - 1 : e2;", "const int up = e2;"),
     "mx_ceil_is_floor": ("const int up = (m == 0.5) ? e2 - 1 : e2;", "const int up = e2 - 1;"),
     "mx_ceil_divides_by_256": ("frexp((double)amax / 448.0, &e2);", "frexp((double)amax / 256.0, &e2);"),
