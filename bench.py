@@ -413,6 +413,21 @@ def run_extras(step, args, bf16_peak):
     ms = a.elapsed_time(b) / args.steps
     gbs = sw_bytes / (ms * 1e-3) / 1e9
     out["swiglu_quantize_nvfp4"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    # f1's variant: SwiGLU in the gate/up GEMM's epilogue (bf16 h out, half the
+    # bytes of gate/up), then the per-token NVFP4 quantization of h; its chain
+    # against the gate/up GEMM followed by the fused SwiGLU + NVFP4 quantization
+    fl_gu = 2 * R * 2 * I * H
+    ms_sw = _time_call(lambda: f.grouped_gemm_fwd_nvfp4_swiglu(*step.xq, *step.wguq, off, 2 * I, H, h=h_out,
+                                                               status=st), args.steps)
+    ach = fl_gu / (ms_sw * 1e-3) / 1e12
+    ms_q = _time_call(lambda: f.quantize_nvfp4_pertoken(h_out, off, codes=step.hq[0], sf=step.hq[1],
+                                                        row_scale=step.hq[2], status=st), args.steps)
+    ms_gu = _time_call(lambda: f.grouped_gemm_fwd_nvfp4(*step.xq, *step.wguq, off, 2 * I, H, y=step.y_gu,
+                                                        status=st), args.steps)
+    out["gemm_fwd_gate_up_swiglu"] = {"ms": round(ms_sw, 4), "TFLOP/s": round(ach, 1),
+                                      "frac_fp4": round(ach / (bf16_peak * 6), 3),
+                                      "chain_ms": round(ms_sw + ms_q, 4),
+                                      "unfused_chain_ms": round(ms_gu + ms, 4)}
     del h_out
     for name, fn, flops in (
             ("gemm_fwd_gate_up_mxfp8",

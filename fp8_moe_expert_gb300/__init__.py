@@ -80,6 +80,8 @@ SYMBOLS = {
                                                "p", "p"]),
     "grouped_gemm_fwd_nvfp4": ("i32", ["p", "p", "p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p",
                                        "p"]),
+    "grouped_gemm_fwd_nvfp4_swiglu": ("i32", ["p", "p", "p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p",
+                                              "p", "p"]),
     "grouped_gemm_fwd_mxfp8": ("i32", ["p", "p", "p", "p", "p", "i32", "i64", "i64", "i64", "p", "p", "p"]),
     "grouped_gemm_dgrad_mxfp8": ("i32", ["p", "p", "p", "p", "i64", "p", "i32", "i64", "i64", "i64", "p", "p",
                                          "p"]),
@@ -335,6 +337,24 @@ def grouped_gemm_fwd_nvfp4(a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offse
                                       _stream(stream))
     _check(st, "grouped_gemm_fwd_nvfp4")
     return y
+
+
+def grouped_gemm_fwd_nvfp4_swiglu(a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offsets, n, k, *, h=None,
+                                  status=None, stream=None):
+    """The gate/up projection's NVFP4 forward with SwiGLU in the epilogue:
+    h [m x n / 2] = silu(gate) * up (bf16), gate and up the first and last n / 2
+    rows of each expert's weights."""
+    import torch
+
+    m = a_codes.shape[0]
+    e = offsets.numel() - 1
+    if h is None:
+        h = _empty((m, n // 2), torch.bfloat16, a_codes.device)
+    st = lib().grouped_gemm_fwd_nvfp4_swiglu(_ptr(a_codes), _ptr(a_sf), _ptr(a_scale), _ptr(b_codes), _ptr(b_sf),
+                                             _ptr(b_scale), _ptr(offsets), e, m, n, k, _ptr(h), _ptr(status),
+                                             _stream(stream))
+    _check(st, "grouped_gemm_fwd_nvfp4_swiglu")
+    return h
 
 
 def grouped_gemm_fwd_mxfp8(a_codes, a_sf, b_codes, b_sf, offsets, n, k, *, y=None, status=None, stream=None):

@@ -456,10 +456,11 @@ fme_status swiglu_backward_quantize_mxfp8(const void *gate_up, const void *dh, i
   return err == cudaSuccess ? FME_OK : cuda_fail(err, "swiglu_backward_quantize_mxfp8 launch");
 }
 
-fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
-                                  const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
-                                  const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n, int64_t k,
-                                  void *y, int32_t *dev_status, void *stream) {
+// The NVFP4 forward, plain (y [m x n]) or with the SwiGLU epilogue (y = h [m x n / 2]).
+static fme_status fwd_nvfp4(bool swiglu, const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
+                            const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale, const int32_t *offsets,
+                            int32_t num_experts, int64_t m, int64_t n, int64_t k, void *y, int32_t *dev_status,
+                            void *stream) {
   if (m < 0 || n < 0 || k < 0 || check_groups(num_experts) != FME_OK) return FME_ERR_INVALID_ARGUMENT;
   if (n % 256 != 0 || n == 0 || k % 256 != 0 || k == 0 || k > 65536) return FME_ERR_UNSUPPORTED_SHAPE;
   if (m > (int64_t(1) << 31) - 1 || static_cast<int64_t>(num_experts) * n > (int64_t(1) << 31) - 1)
@@ -474,7 +475,7 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   fme_status st = current_device(&sms);
   if (st != FME_OK) return st;
   fme::LaunchGemm a{};
-  a.kind = fme::GemmKind::kFwdNvfp4;
+  a.kind = swiglu ? fme::GemmKind::kFwdNvfp4Swiglu : fme::GemmKind::kFwdNvfp4;
   if ((st = encode_u8_2d(&a.map_a, a_codes, k / 2, m, k / 2, 128)) != FME_OK) return st;
   if ((st = encode_u8_2d(&a.map_b, b_codes, k / 2, static_cast<uint64_t>(num_experts) * n, k / 2, 128)) != FME_OK)
     return st;
@@ -483,11 +484,12 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
       FME_OK)
     return st;
   // B scales: the same tiled layout (the stacked weights are one group of
-  // num_experts * n rows); a stage takes 4 tiles of each of the tile's two 128-row blocks
+  // num_experts * n rows); a stage takes 4 tiles of each of the tile's two 128-row
+  // blocks, adjacent (one copy) or, with SwiGLU, a gate and an up block (two copies)
   if ((st = encode_scales_2d(&a.map_sfb, b_sf, static_cast<uint64_t>(num_experts) * n / 128, (k / 64) * 512, 4,
-                             2)) != FME_OK)
+                             swiglu ? 1 : 2)) != FME_OK)
     return st;
-  if ((st = encode_bf16_out(&a.map_y, y, n, m)) != FME_OK) return st;
+  if ((st = encode_bf16_out(&a.map_y, y, swiglu ? n / 2 : n, m)) != FME_OK) return st;
   a.a_scale = a_scale;
   a.b_scale = b_scale;
   a.offsets = offsets;
@@ -500,7 +502,24 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
   a.num_sms = sms;
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t err = fme::launch_grouped_gemm(a);
-  return err == cudaSuccess ? FME_OK : cuda_fail(err, "grouped_gemm_fwd_nvfp4 launch");
+  return err == cudaSuccess ? FME_OK
+                            : cuda_fail(err, swiglu ? "grouped_gemm_fwd_nvfp4_swiglu launch" : "grouped_gemm_fwd_nvfp4 launch");
+}
+
+fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
+                                  const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
+                                  const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n, int64_t k,
+                                  void *y, int32_t *dev_status, void *stream) {
+  return fwd_nvfp4(false, a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offsets, num_experts, m, n, k, y,
+                   dev_status, stream);
+}
+
+fme_status grouped_gemm_fwd_nvfp4_swiglu(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
+                                         const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
+                                         const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n,
+                                         int64_t k, void *h, int32_t *dev_status, void *stream) {
+  return fwd_nvfp4(true, a_codes, a_sf, a_scale, b_codes, b_sf, b_scale, offsets, num_experts, m, n, k, h,
+                   dev_status, stream);
 }
 
 fme_status grouped_gemm_fwd_mxfp8(const uint8_t *a_codes, const uint8_t *a_sf, const uint8_t *b_codes,

@@ -50,6 +50,25 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ------------------------------------------------------------ fp32 arithmetic --
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// silu(g) * u in fp32 (SwiGLU, h = silu(gate) * up), sigma in the form that cannot
+// overflow: t = e^-|g| (the square of e^(-|g|/2), so that it rounds into the
+// subnormal range instead of flushing while g e^g is still representable),
+// sigma = (g >= 0 ? 1 : t) / (1 + t).  Relative error a few 2^-17 at most (the
+// fast exponential), far below bf16's.
+__device__ __forceinline__ float silu_times(float g, float u) {
+  const float s = __expf(-0.5f * fabsf(g));
+  const float t = s * s;
+  const float sig = (g >= 0.0f ? 1.0f : t) * rcp_approx(1.0f + t);
+  return g * sig * u;
+}
+
 // ------------------------------------------------------------------ mbarrier --
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

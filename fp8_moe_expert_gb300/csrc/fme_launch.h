@@ -72,7 +72,12 @@ struct LaunchMxfp8 {
   bool ceil_scale = false;  // row-wise / column-wise only: X = 2^ceil(log2(amax / 448))
 };
 
-enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2, kFwdMxfp8 = 3 };
+// kFwdNvfp4Swiglu: the NVFP4 forward of the gate/up projection with h = silu(gate) * up
+// formed in the epilogue (output [rows x n / 2]).
+enum class GemmKind { kFwdNvfp4 = 0, kDgradMxfp8 = 1, kWgradMxfp8 = 2, kFwdMxfp8 = 3, kFwdNvfp4Swiglu = 4 };
+__host__ __device__ constexpr bool is_fwd_nvfp4(GemmKind k) {
+  return k == GemmKind::kFwdNvfp4 || k == GemmKind::kFwdNvfp4Swiglu;
+}
 
 struct LaunchGemm {
   GemmKind kind;

@@ -299,6 +299,7 @@ static cudaError_t launch_mx(const LaunchGemm &in) {
 cudaError_t launch_grouped_gemm(const LaunchGemm &a) {
   switch (a.kind) {
     case GemmKind::kFwdNvfp4:
+    case GemmKind::kFwdNvfp4Swiglu:
       return launch_grouped_gemm_nvfp4(a);
     case GemmKind::kDgradMxfp8:
       return launch_mx<GemmKind::kDgradMxfp8>(a);

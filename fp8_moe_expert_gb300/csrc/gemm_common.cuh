@@ -45,7 +45,7 @@ constexpr int kAccEmptyArrivals = 2 * 8;  // one per epilogue warp of the pair
 constexpr int64_t kGemmSmemLimit = 227 * 1024 - 1024;
 
 // Elements of K per pipeline stage: one 128-byte swizzle row of codes.
-__host__ __device__ constexpr int k_per_stage(GemmKind k) { return k == GemmKind::kFwdNvfp4 ? 256 : 128; }
+__host__ __device__ constexpr int k_per_stage(GemmKind k) { return is_fwd_nvfp4(k) ? 256 : 128; }
 
 // Group tables (G + 1 entries each) in dynamic shared memory, after the operand
 // ring and the output staging boxes.
@@ -128,7 +128,19 @@ __device__ __forceinline__ Tile tile_at(const LaunchGemm &p, const Groups &s, in
     tl.a_x0 = 0;
     tl.sfa_row = s.tiles[e] + static_cast<int32_t>(mb);
     tl.sfa_x0 = 0;
-    if (K == GemmKind::kFwdNvfp4 || K == GemmKind::kFwdMxfp8) {
+    if (K == GemmKind::kFwdNvfp4Swiglu) {
+      // W_gu stacked as [gate rows (n / 2) | up rows (n / 2)] per expert: the leader
+      // stages tile nb's 128 gate rows, the peer the matching 128 up rows, so that
+      // accumulator columns 0-127 are gate and 128-255 up of the same 128 h columns;
+      // their scale blocks (n / 256 blocks apart) are fetched one by one
+      const int64_t brow = static_cast<int64_t>(e) * p.n + nb * kHalfN;
+      tl.b_y = static_cast<int32_t>(brow + rank * (p.n / 2));
+      tl.b_x0 = 0;
+      tl.sfb_row = static_cast<int32_t>(brow / 128);
+      tl.sfb_x0 = 0;
+      tl.n0 = static_cast<int32_t>(nb * kHalfN);  // first h column
+      tl.y_off = r0 * (p.n / 2) + nb * kHalfN;
+    } else if (K == GemmKind::kFwdNvfp4 || K == GemmKind::kFwdMxfp8) {
       // B = stacked weights, expert e's rows e*n .. e*n+n-1, K contiguous; their
       // scales in the quantizers' tiled layout (one group: 128-row blocks in order)
       const int64_t brow = static_cast<int64_t>(e) * p.n + nb * kBN;
@@ -256,6 +268,25 @@ __device__ __forceinline__ void convert_chunk(uint32_t (&packed)[16], const uint
   }
 }
 
+// SwiGLU of 32 consecutive h columns of one row: the gate and up accumulators
+// scaled as the plain forward scales its outputs ((acc * S_x[t]) * S_w[n], fp32),
+// h = silu(g) * u in fp32 (silu_times), rounded to bf16, two per word.  `swg` and
+// `swu` point at the 32 gate and the 32 matching up column scales.
+__device__ __forceinline__ void swiglu_chunk(uint32_t (&packed)[16], const uint32_t (&vg)[32],
+                                             const uint32_t (&vu)[32], float sa, const float *swg, const float *swu) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 bg = *reinterpret_cast<const float2 *>(swg + 2 * j);
+    const float2 bu = *reinterpret_cast<const float2 *>(swu + 2 * j);
+    const float2 g = __fmul2_rn(
+        __fmul2_rn(make_float2(__uint_as_float(vg[2 * j]), __uint_as_float(vg[2 * j + 1])), make_float2(sa, sa)), bg);
+    const float2 u = __fmul2_rn(
+        __fmul2_rn(make_float2(__uint_as_float(vu[2 * j]), __uint_as_float(vu[2 * j + 1])), make_float2(sa, sa)), bu);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(silu_times(g.x, u.x), silu_times(g.y, u.y));
+    packed[j] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+}
+
 // A 32 x 32 block of bf16 outputs (row `lane` of the warp's 32 rows in
 // `packed`) to global memory through the warp's 2 KB staging block: row r's
 // 16-byte chunk j goes to chunk j ^ ((r >> 1) & 3) of its 64-byte staging row
@@ -340,25 +371,36 @@ __device__ __forceinline__ void epilogue_warp(const LaunchGemm &p, const Groups 
     // the forward's scales of this warp's rows and columns, fetched while the MMAs run
     float sa = 1.0f;
     float4 swv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (K == GemmKind::kFwdNvfp4) {
+    if (is_fwd_nvfp4(K)) {
       if (valid) sa = __ldg(p.a_scale + tl.a_y + r);
-      swv = __ldg(reinterpret_cast<const float4 *>(p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0 + c0) +
-                  lane);
+      if (K == GemmKind::kFwdNvfp4Swiglu) {
+        // lanes 0-15: the scales of this warp's 64 gate columns, lanes 16-31: of the matching up columns
+        swv = __ldg(reinterpret_cast<const float4 *>(p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0 + half * 64 +
+                                                     (lane >= 16 ? p.n / 2 : 0)) +
+                    (lane & 15));
+      } else {
+        swv = __ldg(reinterpret_cast<const float4 *>(p.b_scale + static_cast<int64_t>(tl.e) * p.n + tl.n0 + c0) +
+                    lane);
+      }
     }
     if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) break;
     tc_fence_after();
     uint32_t v0[32], v1[32], v2[32], v3[32];
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + c0;
-    tmem_ld_32x32(taddr, v0);
-    tmem_ld_32x32(taddr + 32, v1);
-    tmem_ld_32x32(taddr + 64, v2);
-    tmem_ld_32x32(taddr + 96, v3);
+    // v0, v1 from columns ta.., v2, v3 from tb..: this warp's 128 columns, or (SwiGLU)
+    // its 64 gate columns and the matching 64 up columns
+    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t ta = K == GemmKind::kFwdNvfp4Swiglu ? tq + half * 64 : tq + c0;
+    const uint32_t tb = K == GemmKind::kFwdNvfp4Swiglu ? tq + kHalfN + half * 64 : tq + c0 + 64;
+    tmem_ld_32x32(ta, v0);
+    tmem_ld_32x32(ta + 32, v1);
+    tmem_ld_32x32(tb, v2);
+    tmem_ld_32x32(tb + 32, v3);
     tmem_wait_ld();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) pair::arrive_remote_relaxed(leader_acc_empty);  // registers hold the data
     acc_phase ^= 1;
-    if (K == GemmKind::kFwdNvfp4) {
+    if (is_fwd_nvfp4(K)) {
       reinterpret_cast<float4 *>(sw)[lane] = swv;
       __syncwarp();
     }
@@ -409,7 +451,25 @@ __device__ __forceinline__ void epilogue_warp(const LaunchGemm &p, const Groups 
     const int warp_rows = tl.rows_valid - 32 * q;  // rows of this warp's 32 that are the expert's
     // this CTA's first output row in map_y (wgrad: expert e's dW rows start at e * m)
     const int32_t out_row = K == GemmKind::kWgradMxfp8 ? static_cast<int32_t>(tl.e * p.m) + tl.a_y : tl.a_y;
-    if (warp_rows > 0) {
+    if (warp_rows > 0 && K == GemmKind::kFwdNvfp4Swiglu) {
+      // h [rows x n / 2]: this warp's 64 h columns of the tile's 128
+      const int64_t ldh = p.n / 2;
+      const int oc0 = half * 64;
+      __nv_bfloat16 *hwarp = y + tl.y_off + static_cast<int64_t>(32 * q) * ldh + oc0;
+      auto emit_h = [&](const uint32_t(&vg)[32], const uint32_t(&vu)[32], int c) {
+        uint32_t packed[16];
+        swiglu_chunk(packed, vg, vu, sa, sw + 32 * c, sw + 64 + 32 * c);
+        if (warp_rows >= 32) {
+          store_block_tma(&p.map_y, tl.n0 + oc0 + 32 * c, out_row + 32 * q, stage_blk, lane, packed);
+        } else {
+          if (lane == 0) bulk_wait_read_all();  // a bulk store may still be reading the block
+          __syncwarp();
+          store_block(hwarp + 32 * c, ldh, warp_rows, stage_blk, lane, packed);
+        }
+      };
+      emit_h(v0, v2, 0);
+      emit_h(v1, v3, 1);
+    } else if (warp_rows > 0) {
       __nv_bfloat16 *ywarp = y + tl.y_off + static_cast<int64_t>(32 * q) * p.n + c0;
       auto emit = [&](const uint32_t(&v)[32], int c) {
         uint32_t packed[16];

@@ -48,7 +48,6 @@ namespace fme {
 
 namespace {
 
-constexpr GemmKind kKind = GemmKind::kFwdNvfp4;
 constexpr int kThreads = 512;  // 4 scale writers, producer, MMA, 2 idle, 8 epilogue warps
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -128,6 +127,8 @@ __device__ __forceinline__ void write_scales(uint32_t tmem, int q, int lane, uin
   tmem_st_32x32_x16(tmem + lanes + kSfaBase + b * kSfaCols, va);
 }
 
+// kKind: kFwdNvfp4, or kFwdNvfp4Swiglu (SwiGLU epilogue, h = silu(gate) * up).
+template <GemmKind kKind>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const __grid_constant__ LaunchGemm p) {
   __shared__ SharedState s;
   extern __shared__ uint8_t dyn_smem[];
@@ -247,8 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
           const uint32_t sbar = pair::map_to_rank(&s.sf_landed[stage], rank);
           pair::tma_load_2d(smem_sfa + stage * kSfaBytes, &p.map_sfa, sbar, (tl.sfa_x0 + ks * kAtoms) * 64,
                             tl.sfa_row);
-          pair::tma_load_2d(smem_sfb + stage * kSfbBytes, &p.map_sfb, sbar, (tl.sfb_x0 + ks * kAtoms) * 64,
-                            tl.sfb_row);
+          if (kKind == GemmKind::kFwdNvfp4Swiglu) {
+            // the gate and the up block of B's scales, n / 256 blocks apart
+            pair::tma_load_2d(smem_sfb + stage * kSfbBytes, &p.map_sfb, sbar, (tl.sfb_x0 + ks * kAtoms) * 64,
+                              tl.sfb_row);
+            pair::tma_load_2d(smem_sfb + stage * kSfbBytes + kSfbBytes / 2, &p.map_sfb, sbar,
+                              (tl.sfb_x0 + ks * kAtoms) * 64, tl.sfb_row + static_cast<int32_t>(p.n / 256));
+          } else {
+            pair::tma_load_2d(smem_sfb + stage * kSfbBytes, &p.map_sfb, sbar, (tl.sfb_x0 + ks * kAtoms) * 64,
+                              tl.sfb_row);
+          }
           if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], kOperandTx);
           const uint32_t bar = pair::map_to_rank(&s.full[stage], 0);
           pair::tma_load_2d(smem_a + stage * kABytes, &p.map_a, bar, tl.a_x0 + ks * kStageKBytes, tl.a_y);
@@ -336,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_nvfp4_kernel(const _
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm_nvfp4(const LaunchGemm &in) {
+template <GemmKind K>
+cudaError_t launch_gemm_nvfp4_kind(const LaunchGemm &in) {
   LaunchGemm a = in;
   a.stages = kStages;
   while (a.stages > 2 && gemm_smem_bytes(a.stages, kStageBytes, a.num_experts) > kGemmSmemLimit) --a.stages;
@@ -345,10 +355,15 @@ cudaError_t launch_grouped_gemm_nvfp4(const LaunchGemm &in) {
   // built with fewer registers at launch would leave the epilogue's increase
   // waiting forever, so it is never launched.
   cudaFuncAttributes fa{};
-  cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_nvfp4_kernel);
+  cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_nvfp4_kernel<K>);
   if (err != cudaSuccess) return err;
   if (fa.numRegs != 65536 / kThreads) return cudaErrorInvalidConfiguration;
-  return launch_pairs(grouped_gemm_nvfp4_kernel, a, kThreads, smem_bytes, gemm_tile_bound(a));
+  return launch_pairs(grouped_gemm_nvfp4_kernel<K>, a, kThreads, smem_bytes, gemm_tile_bound(a));
+}
+
+cudaError_t launch_grouped_gemm_nvfp4(const LaunchGemm &in) {
+  return in.kind == GemmKind::kFwdNvfp4Swiglu ? launch_gemm_nvfp4_kind<GemmKind::kFwdNvfp4Swiglu>(in)
+                                              : launch_gemm_nvfp4_kind<GemmKind::kFwdNvfp4>(in);
 }
 
 }  // namespace fme

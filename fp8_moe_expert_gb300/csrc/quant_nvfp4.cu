@@ -62,12 +62,6 @@ __device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ float rcp_approx(float v) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
-  return r;
-}
-
 // Two E2M1 codes (one byte) of the IEEE quotients fl32(lo/e), fl32(hi/e).
 __device__ __forceinline__ uint32_t e2m1_pair_exact(uint32_t w, float e) {
   return e2m1_pair(__fdiv_rn(__uint_as_float(w << 16), e), __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), e));
@@ -189,17 +183,6 @@ constexpr int kNvSmemBudget = 220 * 1024;  // shared memory aimed for per SM
 // [G+1 group offsets][G+1 tile counts].
 __host__ __device__ __forceinline__ size_t nv_smem_bytes(int stages, int64_t row_bytes, int num_groups) {
   return static_cast<size_t>(stages) * (row_bytes + 8) + 8 * static_cast<size_t>(num_groups + 1);
-}
-
-// silu(g) * u in fp32, sigma in the form that cannot overflow: t = e^-|g| (the
-// square of e^(-|g|/2), so that it rounds into the subnormal range instead of
-// flushing while g e^g is still representable), sigma = (g >= 0 ? 1 : t) / (1 + t).
-// Relative error a few 2^-17 at most (the fast exponential), far below bf16's.
-__device__ __forceinline__ float silu_times(float g, float u) {
-  const float s = __expf(-0.5f * fabsf(g));
-  const float t = s * s;
-  const float sig = (g >= 0.0f ? 1.0f : t) * rcp_approx(1.0f + t);
-  return g * sig * u;
 }
 
 // SwiGLU of two bf16 words: gate (g.lo, g.hi) and up (u.lo, u.hi) -> the bf16 word

@@ -17,6 +17,8 @@
  *                             row-wise and column-wise for the gate/up gradients.
  *   grouped_gemm_fwd_nvfp4    Y_e = X_e W_e^T per expert, per-token scales applied
  *                             in the epilogue, bf16 out.
+ *   grouped_gemm_fwd_nvfp4_swiglu   the gate/up projection of the same product with
+ *                             h = silu(gate) * up formed in the epilogue, bf16 h out.
  *   grouped_gemm_fwd_mxfp8    the same product with MXFP8 operands (no per-token scale).
  *   grouped_gemm_dgrad_mxfp8  dX_e = dY_e W_e per expert, bf16 out.
  *   grouped_gemm_wgrad_mxfp8  dW_e = dY_e^T H_e per expert, bf16 out (or added into
@@ -357,6 +359,39 @@ fme_status grouped_gemm_fwd_nvfp4(const uint8_t *a_codes, const uint8_t *a_sf, c
                                   const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
                                   const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n,
                                   int64_t k, void *y, int32_t *dev_status, void *stream);
+
+/*
+ * grouped_gemm_fwd_nvfp4_swiglu -- the NVFP4 forward of the gate/up projection with
+ * the activation in the epilogue: for every row t of expert e and every column j
+ * of the intermediate width I = n / 2,
+ *   g = S_x[t] * S_w[e, j]     * sum_k A'[t,k] B'_e[j, k]        (gate)
+ *   u = S_x[t] * S_w[e, I + j] * sum_k A'[t,k] B'_e[I + j, k]    (up)
+ *   h[t, j] = silu(g) * u,  silu(v) = v / (1 + e^-v),
+ * g and u as grouped_gemm_fwd_nvfp4 forms them in fp32 before its bf16 rounding
+ * (not rounded here), h evaluated in fp32 with a fast exponential and reciprocal
+ * (relative error a few 2^-17) and rounded to bf16.  h then goes to
+ * quantize_nvfp4_pertoken for the down projection: its per-token scale needs the
+ * whole row of h, which no single output tile holds.
+ *
+ * Passages: as grouped_gemm_fwd_nvfp4 ("Composer 2 Technical Report", section 6.1,
+ * the NVFP4-variant paragraph and the block-scaled MMA sentence).  The pages name
+ * the gate/up projection but not its activation; SwiGLU with the gate in the
+ * first n / 2 rows of each expert's W and the up projection in the last n / 2 is
+ * this library's reading (the same as swiglu_quantize_nvfp4's [g | u] rows).
+ *
+ *   a_codes, a_sf, a_scale  quantize_nvfp4_pertoken of X [m x k] with these offsets
+ *   b_codes, b_sf, b_scale  quantize_nvfp4_pertoken of W_gu [num_experts * n x k] as
+ *                           one group: expert e's gate rows e*n .. e*n+I-1, its up
+ *                           rows e*n+I .. e*n+n-1
+ *   offsets        device int32 [num_experts + 1], rows of X per expert
+ *   m, n, k        n (= 2 I) a multiple of 256; k a multiple of 256
+ *   h              device bf16 [m x n / 2]
+ * Errors and status words as grouped_gemm_fwd_nvfp4.
+ */
+fme_status grouped_gemm_fwd_nvfp4_swiglu(const uint8_t *a_codes, const uint8_t *a_sf, const float *a_scale,
+                                         const uint8_t *b_codes, const uint8_t *b_sf, const float *b_scale,
+                                         const int32_t *offsets, int32_t num_experts, int64_t m, int64_t n,
+                                         int64_t k, void *h, int32_t *dev_status, void *stream);
 
 /*
  * grouped_gemm_fwd_mxfp8 -- the MXFP8 forward: Y[t, :] = sum_k A'[t,k] B'_e[:,k] for

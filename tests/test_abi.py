@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_five_calls():
     names = declared_functions()
     for call in ("quantize_nvfp4_pertoken", "quantize_nvfp4_pertensor", "swiglu_quantize_nvfp4", "quantize_mxfp8",
-                 "grouped_gemm_fwd_nvfp4",
+                 "grouped_gemm_fwd_nvfp4", "grouped_gemm_fwd_nvfp4_swiglu",
                  "grouped_gemm_fwd_mxfp8",
                  "grouped_gemm_dgrad_mxfp8", "grouped_gemm_wgrad_mxfp8", "moe_route", "permute_quantize_nvfp4",
                  "permute_quantize_mxfp8", "moe_combine", "swiglu_backward_quantize_mxfp8"):

@@ -235,6 +235,9 @@ def test_gemms_stay_inside(fme, case):
     gy, y = out((rows, n), torch.bfloat16)
     fme.grouped_gemm_fwd_nvfp4(*a, *b, off, n, k, y=y, status=st)
     gy.check_guards("forward NVFP4 y")
+    gh, h = out((rows, n // 2), torch.bfloat16)
+    fme.grouped_gemm_fwd_nvfp4_swiglu(*a, *b, off, n, k, h=h, status=st)
+    gh.check_guards("forward NVFP4 SwiGLU h")
     am = fme.quantize_mxfp8(x, fme.ROWWISE, off, status=st)
     bm = fme.quantize_mxfp8(w, fme.ROWWISE, status=st)
     gy, y = out((rows, n), torch.bfloat16)
