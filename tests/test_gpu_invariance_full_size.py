@@ -11,7 +11,7 @@ are checked here end to end on the device:
     every expert -- the empty ones included -- so that each expert's last tile
     gains rows and every later expert's rows and scale tiles move; the original
     rows' NVFP4 codes, block scales and row scales, both forward GEMMs' outputs
-    (gate/up and down), and their MXFP8 row-wise codes, scales and dgrad outputs
+    (gate/up, its SwiGLU form's h, and down), and their MXFP8 row-wise codes, scales and dgrad outputs
     must not change by a single bit;
   * the quantizer batch (16384 x 7168, 0.1% hot channels, 1% small rows): a
     seeded permutation and a seeded split into ragged chunks give every row the
@@ -117,7 +117,13 @@ def test_future_rows_change_no_earlier_output(fme, extended):
     y2 = fme.grouped_gemm_fwd_nvfp4(*q2, *wgu, off2, 2 * inter, hid, status=st)
     _ok(fme, st)
     assert _same(y2[pos], y1), "gate/up outputs of the original rows moved"
-    del q1, q2, wgu, y1, y2
+    del y1, y2
+    # the same projection with SwiGLU in the epilogue (h of the original rows)
+    h1 = fme.grouped_gemm_fwd_nvfp4_swiglu(*q1, *wgu, off, 2 * inter, hid, status=st)
+    h2 = fme.grouped_gemm_fwd_nvfp4_swiglu(*q2, *wgu, off2, 2 * inter, hid, status=st)
+    _ok(fme, st)
+    assert _same(h2[pos], h1), "SwiGLU outputs of the original rows moved"
+    del q1, q2, wgu, h1, h2
 
     # ---- forward, NVFP4: H -> down
     h = synth.torch_normal((rows, inter), 1.0, 43)
