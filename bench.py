@@ -413,21 +413,6 @@ def run_extras(step, args, bf16_peak):
     ms = a.elapsed_time(b) / args.steps
     gbs = sw_bytes / (ms * 1e-3) / 1e9
     out["swiglu_quantize_nvfp4"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
-    # f1's variant: SwiGLU in the gate/up GEMM's epilogue (bf16 h out, half the
-    # bytes of gate/up), then the per-token NVFP4 quantization of h; its chain
-    # against the gate/up GEMM followed by the fused SwiGLU + NVFP4 quantization
-    fl_gu = 2 * R * 2 * I * H
-    ms_sw = _time_call(lambda: f.grouped_gemm_fwd_nvfp4_swiglu(*step.xq, *step.wguq, off, 2 * I, H, h=h_out,
-                                                               status=st), args.steps)
-    ach = fl_gu / (ms_sw * 1e-3) / 1e12
-    ms_q = _time_call(lambda: f.quantize_nvfp4_pertoken(h_out, off, codes=step.hq[0], sf=step.hq[1],
-                                                        row_scale=step.hq[2], status=st), args.steps)
-    ms_gu = _time_call(lambda: f.grouped_gemm_fwd_nvfp4(*step.xq, *step.wguq, off, 2 * I, H, y=step.y_gu,
-                                                        status=st), args.steps)
-    out["gemm_fwd_gate_up_swiglu"] = {"ms": round(ms_sw, 4), "TFLOP/s": round(ach, 1),
-                                      "frac_fp4": round(ach / (bf16_peak * 6), 3),
-                                      "chain_ms": round(ms_sw + ms_q, 4),
-                                      "unfused_chain_ms": round(ms_gu + ms, 4)}
     del h_out
     for name, fn, flops in (
             ("gemm_fwd_gate_up_mxfp8",
@@ -458,6 +443,43 @@ def run_extras(step, args, bf16_peak):
                                          "frac_fp8": round(ach / (bf16_peak * 2), 3)}
     del acc
     out.update(run_gate_up_bwd_extras(step, args, hbm, bf16_peak))  # reuses the dY column-wise buffers
+    h_out = torch.empty_like(step.h)
+    # f1's variant, timed last (its FP4 GEMMs run at full power, and the calls timed
+    # after them would start power-capped): SwiGLU in the gate/up GEMM's epilogue (bf16 h out, half the
+    # bytes of gate/up), then the per-token NVFP4 quantization of h; its chain
+    # against the gate/up GEMM followed by the fused SwiGLU + NVFP4 quantization
+    fl_gu = 2 * R * 2 * I * H
+    calls_f1 = {
+        "fused": lambda: f.grouped_gemm_fwd_nvfp4_swiglu(*step.xq, *step.wguq, off, 2 * I, H, h=h_out, status=st),
+        "quant_h": lambda: f.quantize_nvfp4_pertoken(h_out, off, codes=step.hq[0], sf=step.hq[1],
+                                                     row_scale=step.hq[2], status=st),
+        "plain": lambda: f.grouped_gemm_fwd_nvfp4(*step.xq, *step.wguq, off, 2 * I, H, y=step.y_gu, status=st),
+        "swiglu_quant": lambda: f.swiglu_quantize_nvfp4(step.y_gu, off, codes=step.hq[0], sf=step.hq[1],
+                                                        row_scale=step.hq[2], status=st),
+    }
+    # the four calls interleaved, each bracketed by its own events, so that both chains
+    # see the same clocks; medians over args.steps rounds
+    for fn in calls_f1.values():
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    evs = {k: [] for k in calls_f1}
+    for _ in range(args.steps):
+        for k, fn in calls_f1.items():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            evs[k].append((e0, e1))
+    torch.cuda.synchronize()
+    med = {k: statistics.median(e0.elapsed_time(e1) for e0, e1 in v) for k, v in evs.items()}
+    ach = fl_gu / (med["fused"] * 1e-3) / 1e12
+    out["gemm_fwd_gate_up_swiglu"] = {"ms": round(med["fused"], 4), "TFLOP/s": round(ach, 1),
+                                      "frac_fp4": round(ach / (bf16_peak * 6), 3),
+                                      "chain_ms": round(med["fused"] + med["quant_h"], 4),
+                                      "unfused_chain_ms": round(med["plain"] + med["swiglu_quant"], 4),
+                                      "plain_gemm_ms": round(med["plain"], 4)}
+    del h_out
     return out
 
 
