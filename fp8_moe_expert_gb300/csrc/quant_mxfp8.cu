@@ -397,6 +397,28 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
 #pragma unroll
       for (int pass = 0; pass < 8; ++pass)
         *reinterpret_cast<uint4 *>(&tile[pass * 16 + (tid >> 4)][(tid & 15) * 8]) = pre[pass];
+      if constexpr (kRows) {
+        // the row-wise pass from the registers the tile came in: the four lanes of a
+        // row's 32-block (8 values each) take its amax with two shuffles, and each
+        // lane writes its 8 codes (a warp: two full 128-byte rows).  Measured against
+        // the pass re-reading the staged tile: 1.371-1.434 -> 1.320 ms for the
+        // 262144 x 7168 row + column quantization, outputs bit-identical.
+        const int seg = tid & 15;
+#pragma unroll
+        for (int pass = 0; pass < 8; ++pass) {
+          const int r = pass * 16 + (tid >> 4);
+          const uint4 v = pre[pass];
+          uint32_t m = absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w));
+          m = absmax_bf16x2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+          m = absmax_bf16x2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+          const uint32_t code = mx_code<kCeil>(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
+          const float sc = mx_inv_scale(code);
+          const uint2 wv = make_uint2(e4m3x4_words(v.x, v.y, sc), e4m3x4_words(v.z, v.w, sc));
+          if (r < cur.valid)  // rows past the group's end are not stored
+            *reinterpret_cast<uint2 *>(row_codes + (cur.src0 + r) * cols + cb * 128 + seg * 8) = wv;
+          if ((seg & 3) == 0) sfr[(r & 31) * 16 + (r >> 5) * 4 + (seg >> 2)] = static_cast<uint8_t>(code);
+        }
+      }
     }
     __syncthreads();
     if (staged) write_staged(prev, buf ^ 1);
@@ -457,7 +479,8 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
       sfs[(c & 31) * 16 + (c >> 5) * 4 + b] = static_cast<uint8_t>(code_lo);
       sfs[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + b] = static_cast<uint8_t>(code_hi);
     }
-    if (kRows) {
+    if (kSw) {
+      // the SwiGLU backward's row-wise pass, from the staged d(gate/up) tile:
       // thread = (row r, 32-column block b) for 2 of the tile's 512 pairs; a
       // quarter-warp takes 8 consecutive rows of one block (conflict-free 16-byte
       // reads); rows past the group's end are not stored
@@ -484,7 +507,7 @@ __global__ void __launch_bounds__(256, 2) mxfp8_cols_kernel(const uint16_t *__re
 #pragma unroll
         for (int q = 0; q < 8; ++q) words[q] = e4m3x4_words(w[2 * q], w[2 * q + 1], s);
         if (r < cur.valid) {
-          const int col = kSw ? (b < 2 ? cb * 64 + 32 * b : inter + cb * 64 + 32 * (b - 2)) : cb * 128 + 32 * b;
+          const int col = b < 2 ? cb * 64 + 32 * b : inter + cb * 64 + 32 * (b - 2);
           uint4 *dst = reinterpret_cast<uint4 *>(row_codes + (cur.src0 + r) * cols + col);
           dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
           dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
