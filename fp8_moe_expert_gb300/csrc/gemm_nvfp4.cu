@@ -1,7 +1,9 @@
 // gemm_nvfp4.cu -- the NVFP4 grouped GEMM of the forward, Y_e = X_e W_e^T, on the
 // tcgen05 tensor cores (kind::mxf4nvf4.block_scale.scale_vec::4X, M = 256 over a
 // CTA pair, N = 256, K = 64 per MMA), the per-token and per-column FP32 scales
-// applied in the epilogue.
+// applied in the epilogue.  A second form (kFwdNvfp4Swiglu) runs the gate/up
+// projection with h = silu(gate) * up formed in the epilogue: the leader stages a
+// tile's gate rows, its peer the matching up rows (gemm_common.cuh, tile_at).
 //
 // "Composer 2 Technical Report" (papercache.org summary), section 6.1: the NVFP4
 // variant of the MoE forward (E2M1 values, an E4M3 scale per 16-element block,
